@@ -1,0 +1,203 @@
+"""CPU oracle for the Mixtral sparse mixture-of-experts feed-forward layer.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product imports this package; only
+``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg (and
+its ``--impl reference`` arm) may.  It wraps ``moe_oracle.c`` (plain C, double
+accumulation, compiled with gcc) through ctypes and shares no code with the
+CUDA library.
+
+Arrays are numpy: fp32 tensors as ``float32``, bf16 tensors as ``uint16`` bit
+patterns.  Layouts: x [T,d], W_g [E,d], W1/W3 [E,ffn,d], W2 [E,d,ffn].
+
+Pins: every function here is checked in ``tests/test_oracle_pins.py`` against
+closed forms, brute force and invariants that the pages fix; none is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB = os.path.join(_HERE, "libmoe_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16 = 0, 1
+
+# No -ffast-math and no FMA contraction: the arithmetic is the source's, in order.
+CFLAGS = ["-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+          "-fno-fast-math", "-ffp-contract=off", "-Wall", "-Wextra"]
+
+
+def build(src: str = _SRC, out: str = _LIB) -> str:
+    """Compile the oracle with gcc; returns the shared-object path."""
+    cmd = ["gcc", *CFLAGS, "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    return out
+
+
+def _declare(lib):
+    c_void_p, c_int = ctypes.c_void_p, ctypes.c_int
+    lib.oracle_moe_forward.argtypes = [
+        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+        c_int, c_int, c_int, c_int, c_int, c_int,
+        c_void_p, c_void_p, c_void_p, c_void_p, c_int]
+    lib.oracle_moe_forward.restype = c_int
+    lib.oracle_router.argtypes = [c_void_p, c_void_p, c_void_p, c_int, c_int,
+                                  c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]
+    lib.oracle_router.restype = c_int
+    lib.oracle_route.argtypes = [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p,
+                                 c_void_p, c_void_p, c_void_p, c_void_p]
+    lib.oracle_route.restype = c_int
+    lib.oracle_rmsnorm.argtypes = [c_void_p, c_int, c_int, ctypes.c_double, c_int, c_void_p]
+    lib.oracle_rmsnorm.restype = c_int
+    lib.oracle_add.argtypes = [c_void_p, c_void_p, ctypes.c_size_t, c_int, c_void_p]
+    lib.oracle_add.restype = c_int
+    lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
+    lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_double.restype = ctypes.c_double
+    lib.oracle_max_threads.argtypes = []
+    lib.oracle_max_threads.restype = c_int
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the oracle library.  ``path`` selects
+    another build of the same source (the mutation tests use this)."""
+    global _lib
+    if path is not None:
+        return Oracle(_declare(ctypes.CDLL(path)))
+    with _lock:
+        if _lib is None:
+            stale = (not os.path.exists(_LIB) or
+                     os.path.getmtime(_LIB) < os.path.getmtime(_SRC))
+            if stale:
+                build()
+            _lib = Oracle(_declare(ctypes.CDLL(_LIB)))
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data
+
+
+def _dt_code(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:
+        return BF16
+    raise TypeError(f"oracle takes float32 or uint16 (bf16 bits), got {a.dtype}")
+
+
+class Oracle:
+    """Thin ctypes marshalling over one build of ``moe_oracle.c``."""
+
+    def __init__(self, lib):
+        self.lib = lib
+
+    def max_threads(self) -> int:
+        return self.lib.oracle_max_threads()
+
+    def moe_forward(self, x, Wg, W1, W3, W2, k, bias=None, threads=0):
+        """Whole layer.  Returns (out, logits fp32 [T,E], idx int32 [T,k],
+        gates float64 [T,k]); ``out`` has x's element type."""
+        x = np.ascontiguousarray(x)
+        dt = _dt_code(x)
+        T, d = x.shape
+        E = Wg.shape[0]
+        ffn = W1.shape[1]
+        Wg = np.ascontiguousarray(Wg)
+        W1 = [np.ascontiguousarray(w) for w in W1]
+        W3 = [np.ascontiguousarray(w) for w in W3]
+        W2 = [np.ascontiguousarray(w) for w in W2]
+        for w in (Wg, *W1, *W3, *W2):
+            assert w.dtype == x.dtype
+        assert Wg.shape == (E, d)
+        assert all(w.shape == (ffn, d) for w in W1 + W3)
+        assert all(w.shape == (d, ffn) for w in W2)
+        arr = ctypes.c_void_p * E
+        p1 = arr(*[w.ctypes.data for w in W1])
+        p3 = arr(*[w.ctypes.data for w in W3])
+        p2 = arr(*[w.ctypes.data for w in W2])
+        b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+        out = np.empty_like(x)
+        logits = np.empty((T, E), np.float32)
+        idx = np.empty((T, k), np.int32)
+        gates = np.empty((T, k), np.float64)
+        rc = self.lib.oracle_moe_forward(
+            _ptr(x), _ptr(Wg), _ptr(b), p1, p3, p2, T, d, ffn, E, k, dt,
+            _ptr(out), _ptr(logits), _ptr(idx), _ptr(gates), int(threads))
+        if rc != 0:
+            raise RuntimeError(f"oracle_moe_forward failed: {rc}")
+        return out, logits, idx, gates
+
+    def router(self, x, Wg, k, bias=None):
+        x = np.ascontiguousarray(x)
+        dt = _dt_code(x)
+        T, d = x.shape
+        E = Wg.shape[0]
+        Wg = np.ascontiguousarray(Wg)
+        assert Wg.dtype == x.dtype and Wg.shape == (E, d)
+        b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+        logits = np.empty((T, E), np.float32)
+        idx = np.empty((T, k), np.int32)
+        gates = np.empty((T, k), np.float64)
+        rc = self.lib.oracle_router(_ptr(x), _ptr(Wg), _ptr(b), T, d, E, k, dt,
+                                    _ptr(logits), _ptr(idx), _ptr(gates))
+        if rc != 0:
+            raise RuntimeError(f"oracle_router failed: {rc}")
+        return logits, idx, gates
+
+    def route(self, logits, k):
+        """Grouping from given fp32 logits: (idx, gates, counts, offsets, perm, inv)."""
+        logits = np.ascontiguousarray(logits, dtype=np.float32)
+        T, E = logits.shape
+        idx = np.empty((T, k), np.int32)
+        gates = np.empty((T, k), np.float64)
+        counts = np.empty(E, np.int32)
+        offsets = np.empty(E + 1, np.int32)
+        perm = np.empty(T * k, np.int32)
+        inv = np.empty(T * k, np.int32)
+        rc = self.lib.oracle_route(_ptr(logits), T, E, k, _ptr(idx), _ptr(gates),
+                                   _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv))
+        if rc != 0:
+            raise RuntimeError(f"oracle_route failed: {rc}")
+        return idx, gates, counts, offsets, perm, inv
+
+    def rmsnorm(self, x, eps=1e-5):
+        x = np.ascontiguousarray(x)
+        dt = _dt_code(x)
+        T, d = x.shape
+        y = np.empty_like(x)
+        rc = self.lib.oracle_rmsnorm(_ptr(x), T, d, float(eps), dt, _ptr(y))
+        if rc != 0:
+            raise RuntimeError(f"oracle_rmsnorm failed: {rc}")
+        return y
+
+    def add(self, a, b):
+        a = np.ascontiguousarray(a)
+        b = np.ascontiguousarray(b)
+        assert a.dtype == b.dtype and a.shape == b.shape
+        z = np.empty_like(a)
+        rc = self.lib.oracle_add(_ptr(a), _ptr(b), a.size, _dt_code(a), _ptr(z))
+        if rc != 0:
+            raise RuntimeError(f"oracle_add failed: {rc}")
+        return z
+
+    def to_bf16(self, v: float) -> int:
+        return int(self.lib.oracle_double_to_bf16(float(v)))
+
+    def from_bf16(self, h: int) -> float:
+        return float(self.lib.oracle_bf16_to_double(int(h)))
+
+
+def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns (uint16) to float64 (exact)."""
+    return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)

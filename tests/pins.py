@@ -1,0 +1,419 @@
+"""Pins for the CPU oracle: facts the pages and plain mathematics fix, each
+checked against the oracle without using the oracle's own formulas.
+
+Each pin takes an ``oracle.Oracle`` (any build of ``oracle/moe_oracle.c``) and
+raises AssertionError on a mismatch.  ``test_oracle_pins.py`` runs them on the
+real build; ``test_oracle_mutants.py`` runs them on builds with a planted
+mistake and checks that some pin fails for each.
+
+Where a pin needs a second computation it is a different one: a closed form
+worked by hand, a library routine (numpy sort/matmul, torch casts), or a dense
+brute force that evaluates every expert.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+from oracle import bf16_bits_to_f64
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def silu(u):
+    return u / (1.0 + math.exp(-u))
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _rand_layer(rng, T, d, ffn, E, scale=1.0):
+    x = rng.standard_normal((T, d)).astype(np.float32) * np.float32(scale)
+    Wg = (rng.standard_normal((E, d)) / math.sqrt(d)).astype(np.float32)
+    W1 = (rng.standard_normal((E, ffn, d)) / math.sqrt(d)).astype(np.float32)
+    W3 = (rng.standard_normal((E, ffn, d)) / math.sqrt(d)).astype(np.float32)
+    W2 = (rng.standard_normal((E, d, ffn)) / math.sqrt(ffn)).astype(np.float32)
+    return x, Wg, W1, W3, W2
+
+
+def _dense_swiglu(x, W1, W3, W2):
+    """Textbook SwiGLU FFN on a batch of row vectors, float64 matmuls."""
+    x = x.astype(np.float64)
+    u = x @ W1.astype(np.float64).T
+    v = x @ W3.astype(np.float64).T
+    h = u / (1.0 + np.exp(-u)) * v
+    return h @ W2.astype(np.float64).T
+
+
+# ---------------------------------------------------------------------------
+# 1. A worked example, done by hand.
+#
+# d=2, ffn=2, E=3, k=2, fp32.  a = fp32(ln 3), so exp(-a) = 1/3 up to fp32.
+#   W_g = [[a,0],[0,a],[0,0]]
+#   expert 0: W1=[[1,0],[0,1]]  W3=[[2,0],[1,3]]  W2=[[1,0],[1,2]]
+#   expert 1: W1=[[0,1],[1,0]]  W3=[[1,1],[1,0]]  W2=[[0,1],[2,0]]
+#   expert 2: W1=[[-1,0],[0,1]] W3=[[1,0],[0,1]]  W2=[[1,1],[0,1]]
+# (row c of W1/W3 is feature c's input weights; row n of W2 is output n's.)
+# With s1=silu(1), s2=silu(2), m1=silu(-1):
+#   t0 x=[1,0]:  logits (a,0,0): keeps 0, then 1 (tie with 2 -> lower index);
+#                gates 3/4, 1/4.
+#                e0: u=(1,0) v=(2,1) h=(2s1,0) y=(2s1,2s1)
+#                e1: u=(0,1) v=(1,1) h=(0,s1)  y=(s1,0)
+#                out = (1.75 s1, 1.5 s1)
+#   t1 x=[1,2]:  logits (a,2a,0): keeps 1 then 0; gates 3/4, 1/4.
+#                e1: u=(2,1) v=(3,1) h=(3s2,s1) y=(s1,6s2)
+#                e0: u=(1,2) v=(2,7) h=(2s1,7s2) y=(2s1,2s1+14s2)
+#                out = (1.25 s1, 0.5 s1 + 8 s2)
+#   t2 x=[-1,-1]: logits (-a,-a,0): keeps 2, then 0 (tie with 1); gates 3/4, 1/4.
+#                e2: u=(1,-1) v=(-1,-1) h=(-s1,-m1) y=(-s1-m1,-m1)
+#                e0: u=(-1,-1) v=(-2,-4) h=(-2m1,-4m1) y=(-2m1,-10m1)
+#                out = (-0.75 s1 - 1.25 m1, -3.25 m1)
+# Grouping: expert 0 gets (t0,slot0),(t1,slot1),(t2,slot1); expert 1 gets
+# (t0,slot1),(t1,slot0); expert 2 gets (t2,slot0):
+#   counts (3,2,1), offsets (0,3,5,6), perm (0,3,5,1,2,4), inv (0,3,4,1,5,2).
+# ---------------------------------------------------------------------------
+
+def hand_example():
+    a = np.float32(math.log(3.0))
+    x = np.array([[1, 0], [1, 2], [-1, -1]], np.float32)
+    Wg = np.array([[a, 0], [0, a], [0, 0]], np.float32)
+    W1 = np.array([[[1, 0], [0, 1]], [[0, 1], [1, 0]], [[-1, 0], [0, 1]]], np.float32)
+    W3 = np.array([[[2, 0], [1, 3]], [[1, 1], [1, 0]], [[1, 0], [0, 1]]], np.float32)
+    W2 = np.array([[[1, 0], [1, 2]], [[0, 1], [2, 0]], [[1, 1], [0, 1]]], np.float32)
+    s1, s2, m1 = silu(1.0), silu(2.0), silu(-1.0)
+    out = np.array([[1.75 * s1, 1.5 * s1],
+                    [1.25 * s1, 0.5 * s1 + 8 * s2],
+                    [-0.75 * s1 - 1.25 * m1, -3.25 * m1]])
+    return dict(x=x, Wg=Wg, W1=W1, W3=W3, W2=W2, out=out,
+                idx=np.array([[0, 1], [1, 0], [2, 0]]),
+                gates=np.array([[0.75, 0.25]] * 3),
+                counts=np.array([3, 2, 1]), offsets=np.array([0, 3, 5, 6]),
+                perm=np.array([0, 3, 5, 1, 2, 4]), inv=np.array([0, 3, 4, 1, 5, 2]))
+
+
+def pin_hand_example(o):
+    h = hand_example()
+    out, logits, idx, gates = o.moe_forward(h["x"], h["Wg"], h["W1"], h["W3"], h["W2"], 2)
+    assert np.array_equal(idx, h["idx"]), idx
+    assert np.allclose(gates, h["gates"], rtol=0, atol=1e-7), gates
+    assert np.allclose(out, h["out"], rtol=1e-6, atol=1e-7), (out, h["out"])
+    ridx, rg, counts, offsets, perm, inv = o.route(logits, 2)
+    assert np.array_equal(ridx, h["idx"])
+    assert np.array_equal(counts, h["counts"]), counts
+    assert np.array_equal(offsets, h["offsets"]), offsets
+    assert np.array_equal(perm, h["perm"]), perm
+    assert np.array_equal(inv, h["inv"]), inv
+
+
+def pin_hand_example_bf16(o):
+    """Same example stored as bf16: every input is exact in bf16 except a,
+    whose bf16 rounding moves the gates by < 1e-2; outputs round once."""
+    h = hand_example()
+    to = lambda a: torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    out, _, idx, gates = o.moe_forward(to(h["x"]), to(h["Wg"]), to(h["W1"]),
+                                       to(h["W3"]), to(h["W2"]), 2)
+    assert np.array_equal(idx, h["idx"])
+    a16 = float(torch.tensor(math.log(3.0)).to(torch.bfloat16).float())
+    g0 = 1.0 / (1.0 + math.exp(-a16))
+    g = np.array([[g0, 1 - g0]] * 3)
+    # t1's gates compare 2a with a: same difference a
+    assert np.allclose(gates, g, atol=1e-12)
+    s1, s2, m1 = silu(1.0), silu(2.0), silu(-1.0)
+    exp = np.array([[g0 * 2 * s1 + (1 - g0) * s1, g0 * 2 * s1],
+                    [g0 * s1 + (1 - g0) * 2 * s1, g0 * 6 * s2 + (1 - g0) * (2 * s1 + 14 * s2)],
+                    [g0 * (-s1 - m1) + (1 - g0) * (-2 * m1), g0 * (-m1) + (1 - g0) * (-10 * m1)]])
+    got = bf16_bits_to_f64(out)
+    assert np.all(np.abs(got - exp) <= np.abs(exp) * 2.0 ** -8 + 1e-12), (got, exp)
+
+
+# ---------------------------------------------------------------------------
+# 2. Router: gates and selection.
+# ---------------------------------------------------------------------------
+
+def pin_gates_sum_and_renormalised_softmax(o):
+    rng = _rng(1)
+    for E, k in ((8, 2), (5, 2), (3, 1), (16, 2), (2, 2)):
+        logits = (rng.standard_normal((200, E)) * 3).astype(np.float32)
+        idx, gates, *_ = o.route(logits, k)
+        assert np.all(np.abs(gates.sum(1) - 1.0) <= 4e-16)
+        if k == 1:
+            assert np.all(gates == 1.0)
+        l64 = logits.astype(np.float64)
+        p = np.exp(l64 - l64.max(1, keepdims=True))
+        p /= p.sum(1, keepdims=True)
+        sel = np.take_along_axis(p, idx.astype(np.int64), 1)
+        ref = sel / sel.sum(1, keepdims=True)
+        assert np.allclose(gates, ref, rtol=1e-13, atol=1e-15)
+        # slot 0 carries the larger gate
+        assert np.all(gates[:, 0] >= gates[:, -1])
+
+
+def pin_selection_bruteforce(o):
+    rng = _rng(2)
+    for E, k in ((8, 2), (4, 2), (6, 1), (32, 2)):
+        # coarse values make ties common
+        logits = rng.integers(-3, 4, size=(300, E)).astype(np.float32) * np.float32(0.5)
+        idx, *_ = o.route(logits, k)
+        for t in range(logits.shape[0]):
+            key = sorted(range(E), key=lambda e: (-float(logits[t, e]), e))
+            assert list(idx[t]) == key[:k], (t, logits[t], idx[t])
+            if k == 2:
+                best = max(logits[t, a] + logits[t, b]
+                           for a, b in itertools.combinations(range(E), 2))
+                assert logits[t, idx[t, 0]] + logits[t, idx[t, 1]] == best
+
+
+def pin_zero_router(o):
+    rng = _rng(3)
+    x, Wg, W1, W3, W2 = _rand_layer(rng, 7, 16, 24, 6)
+    Wg[:] = 0
+    out, logits, idx, gates = o.moe_forward(x, Wg, W1, W3, W2, 2)
+    assert np.all(logits == 0)
+    assert np.all(idx == np.array([0, 1]))
+    assert np.all(gates == 0.5)
+    ref = 0.5 * _dense_swiglu(x, W1[0], W3[0], W2[0]) + 0.5 * _dense_swiglu(x, W1[1], W3[1], W2[1])
+    assert np.allclose(out, ref, rtol=1e-5, atol=1e-6)
+
+
+def pin_duplicate_router_rows(o):
+    """Two experts with identical router weights always tie; the lower index
+    is taken first."""
+    rng = _rng(4)
+    x, Wg, W1, W3, W2 = _rand_layer(rng, 50, 16, 8, 6)
+    Wg[4] = Wg[1] * 10
+    Wg[1] = Wg[4]
+    _, logits, idx, _ = o.moe_forward(x, Wg, W1, W3, W2, 2)
+    assert np.array_equal(logits[:, 1], logits[:, 4])
+    for t in range(50):
+        if 1 in idx[t] or 4 in idx[t]:
+            pos1 = list(idx[t]).index(1) if 1 in idx[t] else None
+            pos4 = list(idx[t]).index(4) if 4 in idx[t] else None
+            assert pos1 is not None          # 4 never beats 1
+            if pos4 is not None:
+                assert pos1 < pos4
+
+
+def pin_router_bias(o):
+    """A bias added to the logits: big enough to force experts 0 and 1."""
+    rng = _rng(5)
+    x, Wg, W1, W3, W2 = _rand_layer(rng, 20, 16, 8, 8)
+    bias = np.array([100.0, 50.0, 0, 0, 0, 0, -1, -2], np.float32)
+    logits0, _, _ = o.router(x, Wg, 2)
+    logits, idx, gates = o.router(x, Wg, 2, bias=bias)
+    assert np.all(idx == np.array([0, 1]))
+    assert np.allclose(logits, logits0 + bias, rtol=0, atol=1e-4)
+
+
+def pin_router_logits_exact(o):
+    """Logits are the dot products rounded once to fp32: checked with small
+    integers, where every product and sum is exact."""
+    rng = _rng(6)
+    x = rng.integers(-8, 9, size=(30, 40)).astype(np.float32)
+    Wg = rng.integers(-8, 9, size=(7, 40)).astype(np.float32)
+    logits, _, _ = o.router(x, Wg, 2)
+    ref = x.astype(np.int64) @ Wg.astype(np.int64).T
+    assert np.array_equal(logits, ref.astype(np.float32))
+
+
+# ---------------------------------------------------------------------------
+# 3. Grouping tokens by expert.
+# ---------------------------------------------------------------------------
+
+def pin_route_invariants(o):
+    rng = _rng(7)
+    for T, E, k in ((257, 8, 2), (64, 3, 1), (1, 8, 2), (100, 2, 2), (40, 32, 2)):
+        logits = rng.standard_normal((T, E)).astype(np.float32)
+        idx, gates, counts, offsets, perm, inv = o.route(logits, k)
+        assert counts.sum() == T * k
+        assert np.array_equal(counts, np.bincount(idx.ravel(), minlength=E))
+        assert offsets[0] == 0 and offsets[-1] == T * k
+        assert np.array_equal(np.diff(offsets), counts)
+        assert np.array_equal(np.sort(perm), np.arange(T * k))      # bijection
+        assert np.array_equal(inv[perm], np.arange(T * k))          # inv o perm = id
+        assert np.array_equal(perm[inv], np.arange(T * k))
+        flat = idx.ravel()
+        for e in range(E):
+            rows = perm[offsets[e]:offsets[e + 1]]
+            assert np.all(flat[rows] == e)
+            assert np.all(np.diff(rows // k) > 0)                    # ascending tokens
+
+
+def pin_route_empty(o):
+    logits = np.zeros((0, 8), np.float32)
+    idx, gates, counts, offsets, perm, inv = o.route(logits, 2)
+    assert counts.sum() == 0 and np.all(offsets == 0)
+
+
+def pin_forward_matches_route(o):
+    """The forward's own selection equals grouping from its logits."""
+    rng = _rng(8)
+    x, Wg, W1, W3, W2 = _rand_layer(rng, 33, 16, 8, 8)
+    _, logits, idx, gates = o.moe_forward(x, Wg, W1, W3, W2, 2)
+    ridx, rg, *_ = o.route(logits, 2)
+    assert np.array_equal(idx, ridx) and np.array_equal(gates, rg)
+
+
+# ---------------------------------------------------------------------------
+# 4. Expert FFN and the whole layer.
+# ---------------------------------------------------------------------------
+
+def pin_dense_bruteforce(o):
+    """Sparse result == all E experts evaluated densely, weighted by the full
+    softmax masked to the kept experts and renormalised."""
+    rng = _rng(9)
+    for T, d, ffn, E, k in ((16, 8, 12, 5, 2), (9, 6, 10, 4, 1), (12, 4, 4, 8, 2)):
+        x, Wg, W1, W3, W2 = _rand_layer(rng, T, d, ffn, E)
+        out, logits, idx, _ = o.moe_forward(x, Wg, W1, W3, W2, k)
+        l64 = (x.astype(np.float64) @ Wg.astype(np.float64).T).astype(np.float32)
+        assert np.allclose(logits, l64, rtol=0, atol=1e-6)
+        l = logits.astype(np.float64)
+        mask = np.zeros_like(l, dtype=bool)
+        order = np.argsort(-l, axis=1, kind="stable")[:, :k]
+        np.put_along_axis(mask, order, True, 1)
+        p = np.exp(l - l.max(1, keepdims=True))
+        w = np.where(mask, p, 0.0)
+        w /= w.sum(1, keepdims=True)
+        ys = np.stack([_dense_swiglu(x, W1[e], W3[e], W2[e]) for e in range(E)], 1)
+        ref = (w[:, :, None] * ys).sum(1)
+        assert np.allclose(out, ref, rtol=2e-6, atol=2e-7), np.abs(out - ref).max()
+
+
+def pin_single_expert_dense(o):
+    """E=1, k=1: the layer is one dense SwiGLU FFN."""
+    rng = _rng(10)
+    x, Wg, W1, W3, W2 = _rand_layer(rng, 11, 12, 20, 1)
+    out, _, idx, gates = o.moe_forward(x, Wg, W1, W3, W2, 1)
+    assert np.all(idx == 0) and np.all(gates == 1.0)
+    ref = _dense_swiglu(x, W1[0], W3[0], W2[0])
+    assert np.allclose(out, ref, rtol=2e-6, atol=2e-7)
+
+
+def pin_identical_experts(o):
+    """All experts equal: the gates sum to 1, so any routing gives the dense FFN."""
+    rng = _rng(11)
+    x, Wg, W1, W3, W2 = _rand_layer(rng, 21, 10, 14, 6)
+    W1[:] = W1[0]
+    W3[:] = W3[0]
+    W2[:] = W2[0]
+    out, *_ = o.moe_forward(x, Wg, W1, W3, W2, 2)
+    ref = _dense_swiglu(x, W1[0], W3[0], W2[0])
+    assert np.allclose(out, ref, rtol=2e-6, atol=2e-7)
+
+
+def pin_token_independence(o):
+    """Tokens are processed independently: permuting them permutes the
+    outputs bit for bit, and duplicated tokens give identical rows."""
+    rng = _rng(12)
+    x, Wg, W1, W3, W2 = _rand_layer(rng, 24, 8, 12, 8)
+    x[5] = x[17]
+    out, _, idx, _ = o.moe_forward(x, Wg, W1, W3, W2, 2)
+    assert np.array_equal(out[5], out[17]) and np.array_equal(idx[5], idx[17])
+    p = rng.permutation(24)
+    outp, *_ = o.moe_forward(x[p], Wg, W1, W3, W2, 2)
+    assert np.array_equal(outp, out[p])
+
+
+def pin_down_projection_linear(o):
+    """Doubling W2 doubles the output exactly (a power-of-two scale commutes
+    with every rounding)."""
+    rng = _rng(13)
+    x, Wg, W1, W3, W2 = _rand_layer(rng, 10, 8, 12, 4)
+    out, *_ = o.moe_forward(x, Wg, W1, W3, W2, 2)
+    out2, *_ = o.moe_forward(x, Wg, W1, W3, W2 * 2, 2)
+    assert np.array_equal(out2, out * 2)
+
+
+def pin_silu_limits(o):
+    """One expert, one feature: a large positive gate input passes u*v
+    through, a large negative one gives 0 (silu(u) -> u, -> 0)."""
+    x = np.array([[1.0]], np.float32)
+    Wg = np.array([[0.0]], np.float32)
+    for u, expect in ((40.0, 40.0 * 3.0 * 0.5), (-40.0, 0.0), (0.0, 0.0)):
+        W1 = np.array([[[u]]], np.float32)
+        W3 = np.array([[[3.0]]], np.float32)
+        W2 = np.array([[[0.5]]], np.float32)
+        out, *_ = o.moe_forward(x, Wg, W1, W3, W2, 1)
+        assert abs(float(out[0, 0]) - expect) <= 1e-5 * max(1.0, abs(expect)), (u, out)
+
+
+# ---------------------------------------------------------------------------
+# 5. Number formats and the stacked-layer helpers.
+# ---------------------------------------------------------------------------
+
+def pin_bf16_rounding(o):
+    rng = _rng(14)
+    vals = np.concatenate([rng.standard_normal(4000) * 10.0 ** rng.integers(-6, 6, 4000),
+                           [0.0, -0.0, 1.0, -1.0, 65504.0, 1e-40]]).astype(np.float32)
+    # exact bf16 midpoints: a bf16 value plus half its ulp
+    base = torch.from_numpy(rng.standard_normal(2000).astype(np.float32)).to(torch.bfloat16).float()
+    mids = (base.view(torch.int32) + 0x8000).view(torch.float32).numpy()
+    vals = np.concatenate([vals, mids])
+    lib = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    mine = np.array([o.to_bf16(float(v)) for v in vals], np.uint16)
+    assert np.array_equal(mine, lib), np.flatnonzero(mine != lib)[:5]
+    # one rounding from double: 1 + 2^-8 + 2^-30 is above the midpoint between
+    # 1 and 1 + 2^-7, although its fp32 rounding lands exactly on it
+    assert o.to_bf16(1.0 + 2.0 ** -8 + 2.0 ** -30) == 0x3F81
+    assert o.to_bf16(1.0 + 2.0 ** -8) == 0x3F80          # tie -> even
+    assert o.to_bf16(1.0 + 3 * 2.0 ** -8) == 0x3F82      # tie -> even (up)
+    for h in (0x3F80, 0xBF81, 0x0001, 0x7F7F):
+        b = np.array([h], np.uint16)
+        assert o.from_bf16(h) == float(bf16_bits_to_f64(b)[0])
+
+
+def pin_rmsnorm(o):
+    eps = 1e-5
+    c = np.float32(0.01)
+    x = np.full((2, 64), c, np.float32)
+    x[1] = -c
+    y = o.rmsnorm(x, eps)
+    ref = float(c) / math.sqrt(float(c) ** 2 + eps)
+    assert np.allclose(y[0], ref, rtol=1e-6) and np.allclose(y[1], -ref, rtol=1e-6)
+    rng = _rng(15)
+    x = rng.standard_normal((8, 96)).astype(np.float32)
+    y = o.rmsnorm(x, eps)
+    lib = torch.nn.functional.rms_norm(torch.from_numpy(x).double(), (96,), eps=eps).float().numpy()
+    assert np.allclose(y, lib, rtol=1e-6, atol=1e-7)
+
+
+def pin_add(o):
+    a = np.array([1.0, 2.0 ** 20, -3.5], np.float32)
+    b = np.array([2.0 ** -30, 1.0, 3.5], np.float32)
+    z = o.add(a, b)
+    assert np.array_equal(z, np.array([1.0, 2.0 ** 20 + 1, 0.0], np.float32))
+    to = lambda v: np.array([o.to_bf16(t) for t in v], np.uint16)
+    zb = o.add(to([1.0, 256.0]), to([2.0 ** -9, 1.0]))
+    # 1 + 2^-9 rounds to 1 (below the midpoint); 256 + 1 is a tie -> 256 (even)
+    assert list(zb) == [0x3F80, 0x4380]
+
+
+# ---------------------------------------------------------------------------
+# 6. The pages' printed numbers for the Mixtral shape.
+# ---------------------------------------------------------------------------
+
+def pin_page_shape_numbers(o=None):
+    with open(os.path.join(GOLDEN, "mixtral_shape.json")) as f:
+        g = json.load(f)
+    from sparse_mixture_experts_58_b300.inputs import MIXTRAL_SHAPE
+    v = g["values"]
+    assert MIXTRAL_SHAPE["d"] == v["hidden_dimension"]
+    assert MIXTRAL_SHAPE["ffn"] == v["expert_ffn_intermediate_dimension"]
+    assert MIXTRAL_SHAPE["E"] == v["experts_per_layer"]
+    assert MIXTRAL_SHAPE["k"] == v["active_experts_per_token"]
+    per_proj = MIXTRAL_SHAPE["d"] * MIXTRAL_SHAPE["ffn"]
+    assert round(per_proj / 1e6, 1) == v["params_per_projection_millions"]
+    ffn_total = 3 * per_proj * MIXTRAL_SHAPE["E"] * v["layers"]
+    assert round(ffn_total / 1e9) == v["ffn_params_billions"]
+    assert abs(ffn_total / 1e9 + v["other_params_billions"] - v["total_params_billions"]) < 0.15
+    active = 3 * per_proj * MIXTRAL_SHAPE["k"] * v["layers"] + v["other_params_billions"] * 1e9
+    assert abs(active / 1e9 - v["active_params_billions"]) < 0.1
+    assert MIXTRAL_SHAPE["k"] / MIXTRAL_SHAPE["E"] == v["fraction_active"]
+
+
+ALL = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
