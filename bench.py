@@ -1,0 +1,434 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE feed-forward layer (hidden 4096, expert width 14336,
+8 experts, top-2, bf16) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode|prefill|skewed]
+    python bench.py --impl reference ...      # the CPU oracle, timed as the reference arm
+
+One step = one whole layer forward (router, grouping, both grouped expert
+GEMMs, combine) over one batch of T tokens already resident in HBM.  Prints
+one JSON line (rank 0).  With N > 1 (torchrun) every rank runs its own batch
+against replicated weights: no data-path collective; the timed region is
+bracketed by barriers and the slowest rank's time is reported ("weak"
+scaling).  Every step streams the layer's 2.8 GB of expert weights, far more
+than the 126 MB L2, so no flush is needed between steps.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (d4096 ffn14336 E8 top2 bf16) + % of HBM/TC roofline"
+PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+    return dist
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    """Largest value over ranks (outside any timed region)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_token_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own batch of tokens (weights are shared)."""
+    return base_seed + 7919 * rank
+
+
+# ---------------------------------------------------------------- peaks, clocks
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in PEAKS_FALLBACK}, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+class ClockSampler:
+    """NVML samples (SM clock, max clock, clock-event reasons) every few ms
+    while running; read-only."""
+
+    REASONS = {
+        "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4,
+        "hw_slowdown": 0x8, "sync_boost": 0x10, "sw_thermal_slowdown": 0x20,
+        "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
+        "display_clock_setting": 0x100,
+    }
+
+    def __init__(self, index: int, period_s: float = 0.005):
+        self.samples = []
+        self.period = period_s
+        self.ok = False
+        self.max_mhz = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as e:  # no NVML: report that instead of clocks
+            self.err = repr(e)
+        self._stop = threading.Event()
+        self._t = None
+
+    def _run(self):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                mhz = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
+                rs = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.samples.append((mhz, rs))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+
+    def stop(self):
+        if self._t is not None:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok:
+            return {"error": getattr(self, "err", "nvml unavailable")}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        mhz = [m for m, _ in self.samples]
+        seen = 0
+        for _, r in self.samples:
+            seen |= r
+        reasons = [name for name, bit in self.REASONS.items() if seen & bit and name != "gpu_idle"]
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(mhz), "reasons": reasons, "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------- workload
+
+WORKLOAD_NAMES = {
+    "decode": "Mixtral MoE layer, decode: T=16, d=4096, ffn=14336, E=8, top-2, bf16",
+    "prefill": "Mixtral MoE layer, prefill: T=4096, d=4096, ffn=14336, E=8, top-2, bf16",
+    "skewed": "Mixtral MoE layer, skewed routing: T=8192, bias [+2,+1,0,0,0,0,-1,-2], "
+              "5% duplicate tokens, d=4096, ffn=14336, E=8, top-2, bf16",
+}
+
+
+def algorithmic(T, d, ffn, E, k, n_touched, rows_per_expert=None):
+    """Algorithmic FLOPs and HBM bytes of one layer forward (what the method
+    must do: touched experts' weights once, the router weights, x in, out)."""
+    flops = T * (2 * k * 3 * d * ffn + 2 * d * E)
+    bytes_ = n_touched * 3 * d * ffn * 2 + d * E * 2 + 2 * T * d * 2 + T * E * 4
+    return flops, bytes_
+
+
+def gemm1_algorithmic(rows, d, ffn, n_touched):
+    """Gate/up grouped GEMM, per launch: FLOPs and bytes (W1+W3 of touched
+    experts, grouped rows in, hidden activations out)."""
+    flops = 4 * rows * d * ffn
+    bytes_ = n_touched * 2 * d * ffn * 2 + rows * d * 2 + rows * ffn * 2
+    return flops, bytes_
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    """Times the CPU oracle (as it stands) on the host cores, on bounded
+    samples of the same workload.  Rank 0 only."""
+    if rank != 0:
+        return 0
+    import torch
+
+    import oracle
+    from sparse_mixture_experts_58_b300 import inputs
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x, layer = inputs.make_named(args.config, device=dev)
+    T = x.shape[0]
+    k = layer.meta["k"]
+    host = inputs.layer_to_host(layer)
+    xh = inputs.to_host(x)
+    o = oracle.load()
+    cores = o.max_threads()
+    n = max(1, min(T, cores))          # one token per host thread per step
+    rng = __import__("numpy").random.default_rng(0)
+
+    def step(i):
+        rows = rng.choice(T, size=n, replace=False)
+        o.moe_forward(xh[rows], *host[:4], k, bias=host[4])
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAMES[args.config], "T": T},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} seeded tokens of the {T}-token batch per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline(x, layer, k, budget_s=12.0):
+    """The oracle as it stands on all host threads, on the benchmark batch,
+    repeated until about `budget_s` of CPU wall time."""
+    import oracle
+    from sparse_mixture_experts_58_b300 import inputs
+    o = oracle.load()
+    host = inputs.layer_to_host(layer)
+    T = x.shape[0]
+    n = min(T, 64)
+    xh = inputs.to_host(x[:n])
+    done, t_total, reps = 0, 0.0, 0
+    while t_total < budget_s and reps < 50:
+        t0 = time.perf_counter()
+        o.moe_forward(xh, *host[:4], k, bias=host[4])
+        t_total += time.perf_counter() - t0
+        done += n
+        reps += 1
+    return {"value": done / t_total, "unit": "tokens/s", "cores": o.max_threads(),
+            "kind": "oracle",
+            "sample": f"first {n} tokens of the batch, {reps} pass(es), {t_total:.1f} s"}
+
+
+# ---------------------------------------------------------------- our arm
+
+def measure(args, rank, world, local):
+    import torch
+
+    from sparse_mixture_experts_58_b300 import inputs, moe
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    cfg = dict(inputs.WORKLOADS[args.config])
+    T, d, ffn, E, k = cfg["T"], cfg["d"], cfg["ffn"], cfg["E"], cfg["k"]
+
+    # weights shared by every rank; tokens per rank
+    gen = inputs.generator(cfg["seed"], dev)
+    x0, _ = inputs.draw_tokens(gen, T, d, "bf16", dev, cfg.get("dup_frac", 0.0))
+    layer = inputs.draw_weights(gen, d, ffn, E, "bf16", dev, cfg.get("bias"))
+    if rank > 0:
+        x0, _ = inputs.draw_tokens(inputs.generator(rank_token_seed(cfg["seed"], rank), dev),
+                                   T, d, "bf16", dev, cfg.get("dup_frac", 0.0))
+    x = x0.contiguous()
+    out = torch.empty_like(x)
+    ws = moe.Workspace(dev)
+    bias = layer.bias
+
+    def step():
+        moe.forward(x, layer.Wg, layer.W1, layer.W3, layer.W2, k, bias=bias, out=out,
+                    workspace=ws)
+
+    # routing of this batch (for the touched-expert byte count)
+    _, idx, _ = moe.router(x, layer.Wg, k, bias)
+    counts = torch.bincount(idx.flatten().long(), minlength=E).cpu()
+    n_touched = int((counts > 0).sum())
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local)
+
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    barrier(world)
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    elapsed_max = reduce_max(elapsed, world, dev)
+    status = moe.device_status(clear=True)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    # -- per-stage breakdown through the stage entry points (same kernels),
+    #    events on the launching stream between stages
+    stage_names = ["router", "route", "permute", "gate_up_swiglu", "down", "combine"]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(stage_names) + 1)]
+    acc = [0.0] * len(stage_names)
+    n_rep = max(3, min(args.steps, 50))
+    for rep in range(n_rep + 2):
+        evs[0].record(stream)
+        logits, _, _ = moe.router(x, layer.Wg, k, bias)
+        evs[1].record(stream)
+        _, gates2, _, offsets, perm, inv = moe.route_from_logits(logits, k)
+        evs[2].record(stream)
+        xp = moe.permute(x, perm, k)
+        evs[3].record(stream)
+        h = moe.expert_swiglu(xp, offsets, layer.W1, layer.W3)
+        evs[4].record(stream)
+        y = moe.expert_down(h, offsets, layer.W2, T, k)
+        evs[5].record(stream)
+        moe.combine(y, gates2, inv, T, k, torch.bfloat16)
+        evs[6].record(stream)
+        torch.cuda.synchronize()
+        if rep >= 2:
+            for i in range(len(stage_names)):
+                acc[i] += evs[i].elapsed_time(evs[i + 1]) / 1e3
+    stage_s = [a / n_rep for a in acc]
+    del h, y, xp
+
+    # -- end to end through the public C ABI with host buffers
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty_like(x_host, pin_memory=True)
+    x_dev = torch.empty_like(x)
+    out_dev = torch.empty_like(x)
+
+    def e2e_step():
+        moe.forward_host_io(x_host, layer.Wg, layer.W1, layer.W3, layer.W2, k, bias=bias,
+                            out_host=out_host, x_dev=x_dev, out_dev=out_dev, workspace=ws)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_elapsed = reduce_max(e0.elapsed_time(e1) / 1e3, world, dev)
+
+    if rank != 0:
+        return 0
+
+    peaks, peak_src = load_peaks()
+    flops, bytes_ = algorithmic(T, d, ffn, E, k, n_touched)
+    t_step = elapsed_max / args.steps
+    t_roof = max(bytes_ / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+    layer_bound = "hbm" if bytes_ / peaks["hbm_gbs"] > flops / (peaks["bf16_tflops"] * 1e3) else "tensor"
+
+    g_flops, g_bytes = gemm1_algorithmic(T * k, d, ffn, n_touched)
+    t_g = stage_s[3]
+    g_bound = "hbm" if g_bytes / (peaks["hbm_gbs"] * 1e9) > g_flops / (peaks["bf16_tflops"] * 1e12) else "tensor"
+    if g_bound == "hbm":
+        achieved, peak, unit = g_bytes / t_g / 1e9, peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = g_flops / t_g / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+
+    line = {
+        "metric": METRIC,
+        "value": T * world * args.steps / elapsed_max,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t_step * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded x~N(0,1), weights~N(0,1/fan_in), random init",
+        "config": {
+            "workload": WORKLOAD_NAMES[args.config], "T": T, "d": d, "ffn": ffn, "E": E, "k": k,
+            "tokens_per_gpu": T, "parallelism": f"replicas x{world} (no data-path collective)",
+            "l2": "no flush: each step streams the touched experts' weights "
+                  f"({n_touched * 3 * d * ffn * 2 / 1e9:.2f} GB) > 126 MB L2",
+            "experts_touched": n_touched, "rows_per_expert": counts.tolist(),
+        },
+        "roofline": {
+            "kernel": "grouped gate/up GEMM + SwiGLU (tcgen05)",
+            "bound": g_bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "peak_source": f"{peak_src} (burst)",
+            "traffic": None,
+            "algorithmic_per_launch": {"bytes": g_bytes, "flops": g_flops},
+            "launch_us": t_g * 1e6,
+        },
+        "layer_roofline": {
+            "bound": layer_bound, "roofline_us": t_roof * 1e6, "measured_us": t_step * 1e3 * 1e3,
+            "frac": t_roof / t_step, "algorithmic_bytes": bytes_, "algorithmic_flops": flops,
+            "frac_vs_sustained_tc": (max(bytes_ / (peaks["hbm_gbs"] * 1e9),
+                                         flops / (peaks["bf16_tflops_sustained"] * 1e12)) / t_step),
+        },
+        "stages_us": {n: s * 1e6 for n, s in zip(stage_names, stage_s)},
+        "e2e": {"value": T * world * args.steps / e2e_elapsed, "unit": "tokens/s",
+                "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2},
+        "gpu_launches": moe.forward_launches(T, d, ffn, E, k, moe.BF16) * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(x, layer, k)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=sorted(WORKLOAD_NAMES), default="decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return measure(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

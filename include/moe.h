@@ -1,0 +1,205 @@
+/*
+ * moe.h -- C ABI of libmoe.so: the Mixtral sparse mixture-of-experts
+ * feed-forward layer on an NVIDIA B300 (sm_103a).
+ *
+ * The layer (sources named by page title and passage):
+ *   - Router: a linear layer, logits = x . W_g, one score per expert; the two
+ *     largest are kept, the others are set to -inf, and a softmax over the
+ *     kept scores gives the gates ("Mixtral of Experts" (azimuth.plus),
+ *     router paragraph; two experts per token: "Mixtral of Experts"
+ *     (tellworld.net), "How Mixtral 8x7B is built").
+ *   - Experts: each a SwiGLU feed-forward network with its own weights
+ *     ("Mixtral of Experts" (azimuth.plus), expert paragraph) -- gate, up and
+ *     down projections 4096 -> 14336 -> 4096 ("Mixtral > Architecture
+ *     Overview", parameter-count paragraph):
+ *        y_e(x) = W2[e] . ( silu(W1[e] . x) * (W3[e] . x) ),  silu(u) = u/(1+e^-u).
+ *   - Only the chosen experts run; their outputs are summed weighted by the
+ *     gates ("Mixtral & Sparse MoE (2024) > The Solution", routing paragraph;
+ *     "Mixtral" curriculum page, flow "scores experts -> run chosen MLPs ->
+ *     weighted expert outputs"):
+ *        out[t] = sum_j gates[t][j] * y_{idx[t][j]}(x[t]).
+ *   - Every token is independent of every other ("Mixtral > Architecture
+ *     Overview", paragraph on sparse feed-forward computation).
+ *
+ * Readings where the pages are silent: ties between equal logits go to the
+ * lower expert index and slot 0 holds the larger logit; W1 is the gate and W3
+ * the up projection; silu has beta = 1; the router has no bias (the optional
+ * per-expert bias is added to the fp32 logits before selection, for skewed
+ * benchmarks); every token's k rows are computed (no capacity limit).
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers owned by the caller, unless the name
+ *     says host.  The weight-pointer arrays W1/W3/W2 are HOST arrays of E
+ *     device pointers, read during the call only.
+ *   - Layouts are row-major and dense:
+ *       x, out  [T][d]          W_g [E][d]
+ *       W1[e], W3[e] [ffn][d]   (row c = input weights of hidden feature c)
+ *       W2[e]   [d][ffn]        (row n = input weights of output feature n)
+ *     In the pages' row-vector notation x.W1 this is W1 . x here.
+ *   - dtype MOE_BF16: x, W_g, W1/W3/W2, out are bf16; router logits, gates and
+ *     every accumulation are fp32; the expert hidden activation h is stored
+ *     as bf16 and the expert outputs as fp32.  MOE_F32: everything fp32, with
+ *     plain fp32 FMAs (never TF32).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without synchronising.  Arguments are
+ *     validated on the host before anything is enqueued; on any error nothing
+ *     is launched.  Faults inside kernels surface at the caller's next
+ *     synchronisation; bounded waits inside the kernels that expire set a
+ *     device status word read by moe_device_status().
+ *   - The library allocates no device memory: scratch comes from the caller's
+ *     `workspace` (size from moe_workspace_bytes, 256-byte aligned).  Calls on
+ *     different streams need different workspaces.
+ *   - Limits: 1 <= E <= 32, k in {1, 2}, T >= 0 (T = 0 is a no-op).  bf16 needs
+ *     d and ffn multiples of 64 and 16-byte aligned tensors; fp32 needs d a
+ *     multiple of 4.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_ARG = -1,         /* null pointer, negative size, k > E, ...       */
+    MOE_ERR_UNSUPPORTED = -2, /* E > 32, k > 2, alignment or shape limits      */
+    MOE_ERR_WORKSPACE = -3,   /* workspace missing, too small or misaligned    */
+    MOE_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed          */
+    MOE_ERR_DEVICE = -5       /* a kernel's bounded wait expired (status word) */
+} moe_status;
+
+#define MOE_MAX_EXPERTS 32
+
+/* Text for a status code (static storage). */
+const char *moe_strerror(int status);
+
+/* Library version, e.g. 100 = 0.1.0. */
+int moe_version(void);
+
+/* Scratch bytes moe_forward needs for this shape; written to *bytes.
+ * Returns MOE_OK or an argument error. */
+int moe_workspace_bytes(int T, int d, int ffn, int E, int k, int dtype, size_t *bytes);
+
+/*
+ * The whole layer: out = MoE(x).  Runs the router, the grouping by expert,
+ * the two grouped expert GEMMs and the gated combine on `stream`.
+ *   router_bias: NULL or a device fp32 [E] added to the logits.
+ *   workspace: device scratch of at least moe_workspace_bytes(...) bytes.
+ */
+int moe_forward(const void *x, const void *W_g, const float *router_bias,
+                const void *const *W1, const void *const *W3, const void *const *W2,
+                int T, int d, int ffn, int E, int k, int dtype, void *out,
+                void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Same as moe_forward, with the tokens and the result in HOST memory: copies
+ * x_host -> x_dev, runs the layer into out_dev, copies out_dev -> out_host,
+ * all enqueued on `stream`.  The caller synchronises the stream before
+ * reading out_host; page-locked host buffers make the copies asynchronous.
+ */
+int moe_forward_host_io(const void *x_host, void *out_host, void *x_dev, void *out_dev,
+                        const void *W_g, const float *router_bias,
+                        const void *const *W1, const void *const *W3,
+                        const void *const *W2, int T, int d, int ffn, int E, int k,
+                        int dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Router stage: logits [T][E] fp32 (x . W_g + bias, fp32 accumulation),
+ * idx [T][k] int32 (slot 0 = larger logit, ties to the lower index),
+ * gates [T][k] fp32 (softmax over the k kept logits).
+ */
+int moe_router(const void *x, const void *W_g, const float *router_bias, int T, int d,
+               int E, int k, int dtype, float *logits, int *idx, float *gates,
+               void *stream);
+
+/* Scratch bytes for moe_route_from_logits. */
+int moe_route_workspace_bytes(int T, int E, int k, size_t *bytes);
+
+/*
+ * Selection and grouping from given fp32 logits [T][E]:
+ *   idx, gates as in moe_router;
+ *   counts [E]: rows routed to each expert; offsets [E+1]: exclusive prefix
+ *   sum (offsets[E] = T*k);
+ *   perm [T*k]: row r of the expert-grouped order holds (token t, slot j) as
+ *   t*k + j, rows of one expert in ascending token order;
+ *   inv [T*k]: inv[t*k + j] = r.
+ * Deterministic: identical logits give bit-identical outputs.
+ */
+int moe_route_from_logits(const float *logits, int T, int E, int k, int *idx,
+                          float *gates, int *counts, int *offsets, int *perm, int *inv,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Gather: x_perm[r] = x[perm[r] / k] for r < T*k (exact copies).
+ */
+int moe_permute(const void *x, const int *perm, int T, int d, int k, int dtype,
+                void *x_perm, void *stream);
+
+/*
+ * Grouped gate/up projections with the SwiGLU product, for rows grouped by
+ * expert (rows offsets[e] .. offsets[e+1]-1 belong to expert e):
+ *   h[r][c] = silu(sum_i x_perm[r][i] W1[e][c][i]) * (sum_i x_perm[r][i] W3[e][c][i])
+ * x_perm [rows][d], h [rows][ffn] (dtype), offsets device int32 [E+1].
+ * bf16 runs on the tcgen05 tensor cores (fp32 accumulation in tensor memory);
+ * fp32 on plain FMAs.
+ */
+int moe_expert_swiglu(const void *x_perm, const int *offsets, const void *const *W1,
+                      const void *const *W3, int rows, int d, int ffn, int E, int dtype,
+                      void *h, void *stream);
+
+/* Split count moe_expert_down uses for this shape (>= 1); written to *splits. */
+int moe_down_splits(int T, int d, int ffn, int E, int k, int dtype, int *splits);
+
+/*
+ * Grouped down projection: y[s][r][n] = sum_{c in split s} h[r][c] W2[e][n][c],
+ * fp32 partial sums [splits][rows][d], splits from moe_down_splits(T, ...)
+ * with rows = T*k.  The full y is the sum over s (taken in moe_combine).
+ */
+int moe_expert_down(const void *h, const int *offsets, const void *const *W2, int T,
+                    int d, int ffn, int E, int k, int dtype, float *y_partial,
+                    void *stream);
+
+/*
+ * Gated combine: out[t][n] = sum_j gates[t][j] * (sum_s y[s][inv[t*k+j]][n]),
+ * fp32 sums in fixed order, one rounding to dtype.
+ */
+int moe_combine(const float *y_partial, int splits, const float *gates, const int *inv,
+                int T, int d, int k, int dtype, void *out, void *stream);
+
+/*
+ * Stacked-layer helper (not part of the layer itself): if `add` is not NULL,
+ * x <- round(x + add) in place; then xn = x / sqrt(mean(x^2) + eps) with
+ * gain 1 (RMSNorm before each feed-forward sub-block of a Mistral decoder,
+ * "Mixtral of Experts" (azimuth.plus), decoder paragraph).  [T][d], dtype.
+ */
+int moe_add_rmsnorm(void *x, const void *add, void *xn, int T, int d, float eps,
+                    int dtype, void *stream);
+
+/*
+ * Device status word: synchronises `stream`, writes the word to *status
+ * (0 = no kernel reported a problem; otherwise the code of the first expired
+ * bounded wait) and clears it if `clear` is non-zero.
+ */
+int moe_device_status(void *stream, int *status, int clear);
+
+/*
+ * Self-test of the bounded-wait path: launches one tiny kernel that waits on
+ * a barrier nothing arrives at, with the given limit in nanoseconds (clamped
+ * to 1 us .. 100 ms); it gives up, records the expiry in the status word and
+ * returns, leaving the context usable.
+ */
+int moe_selftest_wait_timeout(unsigned int limit_ns, void *stream);
+
+/* Number of kernels moe_forward launches for this shape (for launch counts). */
+int moe_forward_launches(int T, int d, int ffn, int E, int k, int dtype, int *launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,485 @@
+// C ABI of libmoe.so: argument checks, the per-call plan (tiles, splits,
+// workspace layout) and the sequence of kernel launches.  See include/moe.h.
+#include <cudaTypedefs.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace moe {
+
+// Status word written by kernels whose bounded waits expire.
+__device__ int g_device_status = 0;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-side fault injection for tests of the error paths: MOE_FAULT_INJECT
+// set to "arg", "workspace" or "cuda" makes the next checked entry point fail
+// with that error before anything is enqueued.
+int injected_fault() {
+    const char *f = getenv("MOE_FAULT_INJECT");
+    if (f == nullptr || f[0] == '\0') return MOE_OK;
+    if (strcmp(f, "arg") == 0) return MOE_ERR_ARG;
+    if (strcmp(f, "workspace") == 0) return MOE_ERR_WORKSPACE;
+    if (strcmp(f, "cuda") == 0) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+int check_dims(int T, int d, int ffn, int E, int k, int dt) {
+    if (T < 0 || d <= 0 || ffn <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_ARG;
+    if (dt != MOE_F32 && dt != MOE_BF16) return MOE_ERR_ARG;
+    if (E > MOE_MAX_EXPERTS || k > 2) return MOE_ERR_UNSUPPORTED;
+    if (dt == MOE_BF16 && (d % 64 != 0 || ffn % 64 != 0)) return MOE_ERR_UNSUPPORTED;
+    if (dt == MOE_F32 && (d % 4 != 0 || ffn % 4 != 0)) return MOE_ERR_UNSUPPORTED;
+    // index arithmetic is 32-bit for rows and 64-bit for element offsets
+    if ((long long)T * k > (1ll << 30)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+int check_weights(const void *const *W, int E) {
+    if (W == nullptr) return MOE_ERR_ARG;
+    for (int e = 0; e < E; ++e) {
+        if (W[e] == nullptr) return MOE_ERR_ARG;
+        if (!aligned16(W[e])) return MOE_ERR_UNSUPPORTED;
+    }
+    return MOE_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+std::mutex g_dev_mutex;
+int g_sm_count[64];
+int *g_status_ptr[64];
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+    return dev;
+}
+
+}  // namespace
+
+int elem_size(int dt) { return dt == MOE_BF16 ? 2 : 4; }
+
+int device_sm_count() {
+    const int dev = current_device();
+    if (dev < 0) return kPlanSms;
+    std::lock_guard<std::mutex> g(g_dev_mutex);
+    if (g_sm_count[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            n <= 0)
+            n = kPlanSms;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+int *device_status_ptr() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> g(g_dev_mutex);
+    if (g_status_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+int encode_map_bf16_2d(CUtensorMap *map, const void *base, unsigned long long inner,
+                       unsigned long long outer, unsigned int box_inner, unsigned int box_outer) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (encode == nullptr) return MOE_ERR_CUDA;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Tile plan.  Rows per expert decide the tile family: with many rows per
+// expert (prefill) 256-wide tiles keep the tensor cores fed; with few
+// (decode) 128-wide tiles give enough units for every SM to stream weights.
+// An expert never has more than T rows (a token picks an expert at most
+// once), so for T <= 128 one row tile of round_up(T, 8) rows holds any expert.
+// The down projection's contraction is split so that about 8 units per SM
+// exist when few experts are busy; the partial sums are added in the combine.
+int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p) {
+    int rc = check_dims(T, d, ffn, E, k, dt);
+    if (rc != MOE_OK) return rc;
+    Plan q;
+    memset(&q, 0, sizeof q);
+    q.T = T;
+    q.d = d;
+    q.ffn = ffn;
+    q.E = E;
+    q.k = k;
+    q.dt = dt;
+    q.rows = T * k;
+    q.nchunks = (T + kChunk - 1) / kChunk;
+    q.splits = 1;
+    q.kps = (ffn + kBlockK - 1) / kBlockK;
+    if (dt == MOE_BF16) {
+        const long long rows_per_expert = (long long)q.rows / E;
+        q.wide = rows_per_expert >= 128 ? 1 : 0;
+        q.bm = T >= 128 ? 128 : ((T + 7) / 8) * 8;
+        if (q.bm < 8) q.bm = 8;
+        const int NB = q.wide ? 256 : 128;
+        const int kblocks = (ffn + kBlockK - 1) / kBlockK;
+        const long long busy = q.rows < E ? q.rows : E;
+        const long long mtiles = q.wide ? (q.rows + q.bm - 1) / q.bm : busy;
+        const long long ntiles = (d + NB - 1) / NB;
+        const long long base_units = mtiles * ntiles;
+        long long s = base_units > 0 ? (8LL * kPlanSms + base_units - 1) / base_units : 1;
+        const long long smax = kblocks / 8 > 0 ? kblocks / 8 : 1;
+        if (s > smax) s = smax;
+        if (s < 1) s = 1;
+        if (q.wide) s = 1;
+        q.kps = (kblocks + (int)s - 1) / (int)s;
+        q.splits = (kblocks + q.kps - 1) / q.kps;
+    }
+    const int elt = elem_size(dt);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes);
+        return o;
+    };
+    q.o_logits = take((size_t)T * E * 4);
+    q.o_idx = take((size_t)T * k * 4);
+    q.o_gates = take((size_t)T * k * 4);
+    q.o_ccount = take((size_t)q.nchunks * E * 4);
+    q.o_cbase = take((size_t)q.nchunks * E * 4);
+    q.o_counts = take((size_t)E * 4);
+    q.o_offsets = take((size_t)(E + 1) * 4);
+    q.o_perm = take((size_t)q.rows * 4);
+    q.o_inv = take((size_t)q.rows * 4);
+    q.o_xperm = take((size_t)q.rows * d * elt);
+    q.o_h = take((size_t)q.rows * ffn * elt);
+    q.o_y = take((size_t)q.splits * q.rows * d * 4);
+    q.bytes = off;
+    *p = q;
+    return MOE_OK;
+}
+
+namespace {
+
+template <typename T>
+T *ws_at(void *ws, size_t off) {
+    return reinterpret_cast<T *>(static_cast<uint8_t *>(ws) + off);
+}
+
+int run_forward(const Plan &P, const void *x, const void *W_g, const float *bias,
+                const void *const *W1, const void *const *W3, const void *const *W2, void *out,
+                void *ws, cudaStream_t s) {
+    float *logits = ws_at<float>(ws, P.o_logits);
+    int *idx = ws_at<int>(ws, P.o_idx);
+    float *gates = ws_at<float>(ws, P.o_gates);
+    int *cc = ws_at<int>(ws, P.o_ccount);
+    int *cb = ws_at<int>(ws, P.o_cbase);
+    int *counts = ws_at<int>(ws, P.o_counts);
+    int *offsets = ws_at<int>(ws, P.o_offsets);
+    int *perm = ws_at<int>(ws, P.o_perm);
+    int *inv = ws_at<int>(ws, P.o_inv);
+    void *x_perm = ws_at<uint8_t>(ws, P.o_xperm);
+    void *h = ws_at<uint8_t>(ws, P.o_h);
+    float *y = ws_at<float>(ws, P.o_y);
+    const int elt = elem_size(P.dt);
+    int rc;
+    if ((rc = cuda_rc(launch_router(x, W_g, bias, P.T, P.d, P.E, P.k, P.dt, logits, idx, gates,
+                                    cc, s))) != MOE_OK)
+        return rc;
+    if ((rc = cuda_rc(launch_chunk_scan(cc, P.nchunks, P.E, cb, counts, offsets, s))) != MOE_OK)
+        return rc;
+    if ((rc = cuda_rc(launch_group_tokens(idx, cb, offsets, x, P.T, P.d, P.E, P.k, elt, perm, inv,
+                                          x_perm, s))) != MOE_OK)
+        return rc;
+    if (P.dt == MOE_BF16) {
+        if ((rc = launch_swiglu_tc(x_perm, offsets, W1, W3, P.rows, P.d, P.ffn, P.E, P.bm, P.wide,
+                                   h, s)) != MOE_OK)
+            return rc;
+        if ((rc = launch_down_tc(h, offsets, W2, P.rows, P.d, P.ffn, P.E, P.bm, P.wide, P.splits,
+                                 P.kps, y, s)) != MOE_OK)
+            return rc;
+    } else {
+        if ((rc = cuda_rc(launch_swiglu_f32(static_cast<const float *>(x_perm), offsets, W1, W3,
+                                            P.rows, P.d, P.ffn, P.E, static_cast<float *>(h),
+                                            s))) != MOE_OK)
+            return rc;
+        if ((rc = cuda_rc(launch_down_f32(static_cast<const float *>(h), offsets, W2, P.rows, P.d,
+                                          P.ffn, P.E, y, s))) != MOE_OK)
+            return rc;
+    }
+    return cuda_rc(launch_combine(y, P.splits, P.rows, gates, inv, P.T, P.d, P.k, P.dt, out, s));
+}
+
+int check_forward_args(const void *x, const void *W_g, const void *const *W1,
+                       const void *const *W3, const void *const *W2, int T, int d, int ffn, int E,
+                       int k, int dt, const void *out, const void *ws, size_t ws_bytes,
+                       Plan *P) {
+    int rc = make_plan(T, d, ffn, E, k, dt, P);
+    if (rc != MOE_OK) return rc;
+    if ((rc = injected_fault()) != MOE_OK) return rc;
+    if (T == 0) return MOE_OK;
+    if (x == nullptr || W_g == nullptr || out == nullptr) return MOE_ERR_ARG;
+    if ((rc = check_weights(W1, E)) != MOE_OK) return rc;
+    if ((rc = check_weights(W3, E)) != MOE_OK) return rc;
+    if ((rc = check_weights(W2, E)) != MOE_OK) return rc;
+    if (!aligned16(x) || !aligned16(W_g) || !aligned16(out)) return MOE_ERR_UNSUPPORTED;
+    if (ws == nullptr || ws_bytes < P->bytes) return MOE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char *moe_strerror(int status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported shape, type or alignment";
+        case MOE_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+        case MOE_ERR_CUDA: return "CUDA runtime or launch error";
+        case MOE_ERR_DEVICE: return "a kernel's bounded wait expired";
+        default: return "unknown status";
+    }
+}
+
+int moe_version(void) { return 100; }
+
+int moe_workspace_bytes(int T, int d, int ffn, int E, int k, int dtype, size_t *bytes) {
+    if (bytes == nullptr) return MOE_ERR_ARG;
+    Plan P;
+    const int rc = make_plan(T, d, ffn, E, k, dtype, &P);
+    if (rc != MOE_OK) return rc;
+    *bytes = P.bytes;
+    return MOE_OK;
+}
+
+int moe_forward_launches(int T, int d, int ffn, int E, int k, int dtype, int *launches) {
+    if (launches == nullptr) return MOE_ERR_ARG;
+    Plan P;
+    const int rc = make_plan(T, d, ffn, E, k, dtype, &P);
+    if (rc != MOE_OK) return rc;
+    *launches = T == 0 ? 0 : 6;  // router, scan, group, gate/up, down, combine
+    return MOE_OK;
+}
+
+int moe_down_splits(int T, int d, int ffn, int E, int k, int dtype, int *splits) {
+    if (splits == nullptr) return MOE_ERR_ARG;
+    Plan P;
+    const int rc = make_plan(T, d, ffn, E, k, dtype, &P);
+    if (rc != MOE_OK) return rc;
+    *splits = P.splits;
+    return MOE_OK;
+}
+
+int moe_forward(const void *x, const void *W_g, const float *router_bias, const void *const *W1,
+                const void *const *W3, const void *const *W2, int T, int d, int ffn, int E, int k,
+                int dtype, void *out, void *workspace, size_t workspace_bytes, void *stream) {
+    Plan P;
+    int rc = check_forward_args(x, W_g, W1, W3, W2, T, d, ffn, E, k, dtype, out, workspace,
+                                workspace_bytes, &P);
+    if (rc != MOE_OK || T == 0) return rc;
+    return run_forward(P, x, W_g, router_bias, W1, W3, W2, out, workspace,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int moe_forward_host_io(const void *x_host, void *out_host, void *x_dev, void *out_dev,
+                        const void *W_g, const float *router_bias, const void *const *W1,
+                        const void *const *W3, const void *const *W2, int T, int d, int ffn,
+                        int E, int k, int dtype, void *workspace, size_t workspace_bytes,
+                        void *stream) {
+    Plan P;
+    int rc = check_forward_args(x_dev, W_g, W1, W3, W2, T, d, ffn, E, k, dtype, out_dev,
+                                workspace, workspace_bytes, &P);
+    if (rc != MOE_OK || T == 0) return rc;
+    if (x_host == nullptr || out_host == nullptr) return MOE_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t bytes = (size_t)T * d * elem_size(dtype);
+    if (cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if ((rc = run_forward(P, x_dev, W_g, router_bias, W1, W3, W2, out_dev, workspace, s)) != MOE_OK)
+        return rc;
+    if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+int moe_router(const void *x, const void *W_g, const float *router_bias, int T, int d, int E,
+               int k, int dtype, float *logits, int *idx, float *gates, void *stream) {
+    int rc = check_dims(T, d, 64, E, k, dtype);
+    if (rc != MOE_OK) return rc;
+    if ((rc = injected_fault()) != MOE_OK) return rc;
+    if (T == 0) return MOE_OK;
+    if (!x || !W_g || !logits || !idx || !gates) return MOE_ERR_ARG;
+    if (!aligned16(x) || !aligned16(W_g)) return MOE_ERR_UNSUPPORTED;
+    // this entry point returns no per-chunk counts: the kernel skips them
+    return cuda_rc(launch_router(x, W_g, router_bias, T, d, E, k, dtype, logits, idx, gates,
+                                 nullptr, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_route_workspace_bytes(int T, int E, int k, size_t *bytes) {
+    if (bytes == nullptr) return MOE_ERR_ARG;
+    int rc = check_dims(T, 64, 64, E, k, MOE_BF16);
+    if (rc != MOE_OK) return rc;
+    const size_t nchunks = (size_t)(T + kChunk - 1) / kChunk;
+    *bytes = 2 * align_up(nchunks * E * 4);
+    return MOE_OK;
+}
+
+int moe_route_from_logits(const float *logits, int T, int E, int k, int *idx, float *gates,
+                          int *counts, int *offsets, int *perm, int *inv, void *workspace,
+                          size_t workspace_bytes, void *stream) {
+    int rc = check_dims(T, 64, 64, E, k, MOE_BF16);
+    if (rc != MOE_OK) return rc;
+    if ((rc = injected_fault()) != MOE_OK) return rc;
+    if (!counts || !offsets) return MOE_ERR_ARG;
+    size_t need = 0;
+    moe_route_workspace_bytes(T, E, k, &need);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        // no rows: every count is zero and every offset is zero
+        if (cudaMemsetAsync(counts, 0, (size_t)E * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cudaMemsetAsync(offsets, 0, (size_t)(E + 1) * 4, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    if (!logits || !idx || !gates || !perm || !inv) return MOE_ERR_ARG;
+    if (workspace == nullptr || workspace_bytes < need) return MOE_ERR_WORKSPACE;
+    const int nchunks = (T + kChunk - 1) / kChunk;
+    int *cc = static_cast<int *>(workspace);
+    int *cb = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) +
+                                      align_up((size_t)nchunks * E * 4));
+    if ((rc = cuda_rc(launch_topk_from_logits(logits, T, E, k, idx, gates, cc, s))) != MOE_OK)
+        return rc;
+    if ((rc = cuda_rc(launch_chunk_scan(cc, nchunks, E, cb, counts, offsets, s))) != MOE_OK)
+        return rc;
+    return cuda_rc(launch_group_tokens(idx, cb, offsets, nullptr, T, 0, E, k, 0, perm, inv,
+                                       nullptr, s));
+}
+
+int moe_permute(const void *x, const int *perm, int T, int d, int k, int dtype, void *x_perm,
+                void *stream) {
+    int rc = check_dims(T, d, 64, k, k, dtype);
+    if (rc != MOE_OK) return rc;
+    if (T == 0) return MOE_OK;
+    if (!x || !perm || !x_perm) return MOE_ERR_ARG;
+    if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_UNSUPPORTED;
+    return cuda_rc(launch_permute(x, perm, T, d, k, elem_size(dtype), x_perm,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+int moe_expert_swiglu(const void *x_perm, const int *offsets, const void *const *W1,
+                      const void *const *W3, int rows, int d, int ffn, int E, int dtype, void *h,
+                      void *stream) {
+    int rc = check_dims(rows, d, ffn, E, 1, dtype);
+    if (rc != MOE_OK) return rc;
+    if ((rc = injected_fault()) != MOE_OK) return rc;
+    if (rows == 0) return MOE_OK;
+    if (!x_perm || !offsets || !h) return MOE_ERR_ARG;
+    if ((rc = check_weights(W1, E)) != MOE_OK) return rc;
+    if ((rc = check_weights(W3, E)) != MOE_OK) return rc;
+    if (!aligned16(x_perm) || !aligned16(h)) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == MOE_BF16) {
+        // plan as if the rows came from T = rows / 2 tokens with k = 2 when
+        // possible, else one token per row
+        Plan P;
+        const int k = (rows % 2 == 0 && E >= 2) ? 2 : 1;
+        if ((rc = make_plan(rows / k, d, ffn, E, k, dtype, &P)) != MOE_OK) return rc;
+        return launch_swiglu_tc(x_perm, offsets, W1, W3, rows, d, ffn, E, P.bm, P.wide, h, s);
+    }
+    return cuda_rc(launch_swiglu_f32(static_cast<const float *>(x_perm), offsets, W1, W3, rows, d,
+                                     ffn, E, static_cast<float *>(h), s));
+}
+
+int moe_expert_down(const void *h, const int *offsets, const void *const *W2, int T, int d,
+                    int ffn, int E, int k, int dtype, float *y_partial, void *stream) {
+    Plan P;
+    int rc = make_plan(T, d, ffn, E, k, dtype, &P);
+    if (rc != MOE_OK) return rc;
+    if ((rc = injected_fault()) != MOE_OK) return rc;
+    if (T == 0) return MOE_OK;
+    if (!h || !offsets || !y_partial) return MOE_ERR_ARG;
+    if ((rc = check_weights(W2, E)) != MOE_OK) return rc;
+    if (!aligned16(h) || !aligned16(y_partial)) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == MOE_BF16)
+        return launch_down_tc(h, offsets, W2, P.rows, d, ffn, E, P.bm, P.wide, P.splits, P.kps,
+                              y_partial, s);
+    return cuda_rc(launch_down_f32(static_cast<const float *>(h), offsets, W2, P.rows, d, ffn, E,
+                                   y_partial, s));
+}
+
+int moe_combine(const float *y_partial, int splits, const float *gates, const int *inv, int T,
+                int d, int k, int dtype, void *out, void *stream) {
+    int rc = check_dims(T, d, 64, k, k, dtype);
+    if (rc != MOE_OK) return rc;
+    if (splits < 1) return MOE_ERR_ARG;
+    if (T == 0) return MOE_OK;
+    if (!y_partial || !gates || !inv || !out) return MOE_ERR_ARG;
+    if (d % 4 != 0 || !aligned16(y_partial) || !aligned16(out)) return MOE_ERR_UNSUPPORTED;
+    return cuda_rc(launch_combine(y_partial, splits, T * k, gates, inv, T, d, k, dtype, out,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+int moe_add_rmsnorm(void *x, const void *add, void *xn, int T, int d, float eps, int dtype,
+                    void *stream) {
+    if (T < 0 || d <= 0 || (dtype != MOE_F32 && dtype != MOE_BF16) || !(eps >= 0.f))
+        return MOE_ERR_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !xn) return MOE_ERR_ARG;
+    return cuda_rc(launch_add_rmsnorm(x, add, xn, T, d, eps, dtype,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int moe_device_status(void *stream, int *status, int clear) {
+    if (status == nullptr) return MOE_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof v) != cudaSuccess) return MOE_ERR_CUDA;
+    *status = v;
+    if (clear && v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+int moe_selftest_wait_timeout(unsigned int limit_ns, void *stream) {
+    if (limit_ns < 1000u) limit_ns = 1000u;
+    if (limit_ns > 100000000u) limit_ns = 100000000u;
+    return cuda_rc(launch_wait_selftest(limit_ns, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,147 @@
+// Gated combine back to token order, plus the stacked-layer RMSNorm/residual
+// helper and the bounded-wait self-test kernel.
+//
+// Combine: out[t] = sum_j gates[t][j] * y_{row(t,j)}, the selected experts'
+// outputs weighted by the routing weights ("Mixtral & Sparse MoE (2024) > The
+// Solution", routing paragraph; "Mixtral" curriculum page, "weighted expert
+// outputs").  The down projection leaves fp32 partial sums per contraction
+// split; they are added here in split order, then gated in slot order, then
+// rounded once.  HBM-bound: one warp per token, 16-byte loads.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+template <typename T>
+__device__ __forceinline__ void store4(T *p, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(float *p, float4 v) {
+    *reinterpret_cast<float4 *>(p) = v;
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *p, float4 v) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t *>(&a);
+    u.y = *reinterpret_cast<const uint32_t *>(&b);
+    *reinterpret_cast<uint2 *>(p) = u;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ y, int splits,
+                                                      int rows, const float *__restrict__ gates,
+                                                      const int *__restrict__ inv, int Tn, int d,
+                                                      int k, T *out) {
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= Tn) return;
+    int rowj[2];
+    float gj[2];
+    for (int j = 0; j < k; ++j) {
+        rowj[j] = inv[(size_t)t * k + j];
+        gj[j] = gates[(size_t)t * k + j];
+    }
+    const int nv = d / 4;
+    const size_t split_stride = (size_t)rows * d;
+#pragma unroll 2
+    for (int v = lane; v < nv; v += 32) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const float4 *src = reinterpret_cast<const float4 *>(y + (size_t)rowj[j] * d) + v;
+            float4 s = __ldcs(src);
+            for (int q = 1; q < splits; ++q) {
+                const float4 p = __ldcs(src + q * split_stride / 4);
+                s.x += p.x;
+                s.y += p.y;
+                s.z += p.z;
+                s.w += p.w;
+            }
+            acc.x = fmaf(gj[j], s.x, acc.x);
+            acc.y = fmaf(gj[j], s.y, acc.y);
+            acc.z = fmaf(gj[j], s.z, acc.z);
+            acc.w = fmaf(gj[j], s.w, acc.w);
+        }
+        store4<T>(out + (size_t)t * d + 4 * v, acc);
+    }
+}
+
+// One block per row: optional residual add (rounded to the storage type),
+// then RMSNorm with gain 1.
+template <typename T>
+__global__ void __launch_bounds__(256) add_rmsnorm_kernel(T *x, const T *__restrict__ add, T *xn,
+                                                          int d, float eps) {
+    __shared__ float s_part[8];
+    const size_t o = (size_t)blockIdx.x * d;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) {
+        float v = to_f32(x[o + i]);
+        if (add != nullptr) {
+            const T r = from_f32<T>(v + to_f32(add[o + i]));
+            x[o + i] = r;
+            v = to_f32(r);
+        }
+        ss = fmaf(v, v, ss);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += s_part[w];
+    const float scale = 1.f / sqrtf(tot / static_cast<float>(d) + eps);
+    for (int i = threadIdx.x; i < d; i += blockDim.x)
+        xn[o + i] = from_f32<T>(to_f32(x[o + i]) * scale);
+}
+
+// Waits on a barrier nothing arrives at; the bounded wait gives up after
+// `limit_ns` and records kStatusSelftest.
+__global__ void wait_selftest_kernel(unsigned long long limit_ns, int *status) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar, 1);
+        ptx::fence_barrier_init();
+        ptx::mbar_wait_bounded(&bar, 0, nullptr, status, kStatusSelftest, limit_ns);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float *y, int splits, int rows, const float *gates,
+                           const int *inv, int T, int d, int k, int dt, void *out,
+                           cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const int grid = (T + 7) / 8;
+    if (dt == MOE_BF16)
+        combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(y, splits, rows, gates, inv, T, d, k,
+                                                           static_cast<__nv_bfloat16 *>(out));
+    else
+        combine_kernel<float><<<grid, 256, 0, s>>>(y, splits, rows, gates, inv, T, d, k,
+                                                   static_cast<float *>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_add_rmsnorm(void *x, const void *add, void *xn, int T, int d, float eps, int dt,
+                               cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    if (dt == MOE_BF16)
+        add_rmsnorm_kernel<__nv_bfloat16><<<T, 256, 0, s>>>(
+            static_cast<__nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(add),
+            static_cast<__nv_bfloat16 *>(xn), d, eps);
+    else
+        add_rmsnorm_kernel<float><<<T, 256, 0, s>>>(static_cast<float *>(x),
+                                                    static_cast<const float *>(add),
+                                                    static_cast<float *>(xn), d, eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(unsigned int limit_ns, cudaStream_t s) {
+    int *st = device_status_ptr();
+    if (st == nullptr) return cudaErrorUnknown;
+    wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns, st);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

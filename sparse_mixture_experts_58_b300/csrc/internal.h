@@ -1,0 +1,77 @@
+// Host-side declarations shared by the libmoe translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// SM count the tile planner sizes work for (a B300 has 148); grids use the
+// device's real count at launch.
+constexpr int kPlanSms = 148;
+
+// How one call is carved into kernels and scratch.
+struct Plan {
+    int T, d, ffn, E, k, dt;
+    int rows;      // T * k expert rows
+    int nchunks;   // router chunks of kChunk tokens
+    // grouped expert GEMMs (bf16 tensor-core path)
+    int wide;      // 1: 256-wide tiles (many rows per expert); 0: 128-wide
+    int bm;        // token rows per tile (<= 128)
+    int splits;    // split of the down projection's contraction
+    int kps;       // 64-wide contraction blocks per split
+    // workspace layout (byte offsets, 256-aligned)
+    size_t o_logits, o_idx, o_gates, o_ccount, o_cbase, o_counts, o_offsets, o_perm, o_inv;
+    size_t o_xperm, o_h, o_y, bytes;
+};
+
+int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p);
+
+int elem_size(int dt);
+int device_sm_count();
+// Device address of the status word for the current device (nullptr on error).
+int *device_status_ptr();
+
+// Kernel launchers (each returns the launch's cudaError_t).
+cudaError_t launch_router(const void *x, const void *Wg, const float *bias, int T, int d, int E,
+                          int k, int dt, float *logits, int *idx, float *gates, int *chunk_counts,
+                          cudaStream_t s);
+cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, int *idx,
+                                    float *gates, int *chunk_counts, cudaStream_t s);
+cudaError_t launch_chunk_scan(const int *chunk_counts, int nchunks, int E, int *chunk_base,
+                              int *counts, int *offsets, cudaStream_t s);
+cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int *offsets,
+                                const void *x, int T, int d, int E, int k, int elt, int *perm,
+                                int *inv, void *x_perm, cudaStream_t s);
+cudaError_t launch_permute(const void *x, const int *perm, int T, int d, int k, int elt,
+                           void *x_perm, cudaStream_t s);
+
+// Grouped expert GEMMs.  `rows` = total expert rows (T*k); `bm` rows per tile.
+int launch_swiglu_tc(const void *x_perm, const int *offsets, const void *const *W1,
+                     const void *const *W3, int rows, int d, int ffn, int E, int bm, int wide,
+                     void *h, cudaStream_t s);
+int launch_down_tc(const void *h, const int *offsets, const void *const *W2, int rows, int d,
+                   int ffn, int E, int bm, int wide, int splits, int kps, float *y,
+                   cudaStream_t s);
+cudaError_t launch_swiglu_f32(const float *x_perm, const int *offsets, const void *const *W1,
+                              const void *const *W3, int rows, int d, int ffn, int E, float *h,
+                              cudaStream_t s);
+cudaError_t launch_down_f32(const float *h, const int *offsets, const void *const *W2, int rows,
+                            int d, int ffn, int E, float *y, cudaStream_t s);
+
+cudaError_t launch_combine(const float *y, int splits, int rows, const float *gates,
+                           const int *inv, int T, int d, int k, int dt, void *out,
+                           cudaStream_t s);
+cudaError_t launch_add_rmsnorm(void *x, const void *add, void *xn, int T, int d, float eps,
+                               int dt, cudaStream_t s);
+cudaError_t launch_wait_selftest(unsigned int limit_ns, cudaStream_t s);
+
+// Tensor maps (TMA descriptors), encoded through the driver entry point.
+int encode_map_bf16_2d(CUtensorMap *map, const void *base, unsigned long long inner,
+                       unsigned long long outer, unsigned int box_inner,
+                       unsigned int box_outer);
+
+}  // namespace moe

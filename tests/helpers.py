@@ -1,0 +1,76 @@
+"""Shared helpers for the GPU parity tests: running the oracle on host copies
+of a workload and the parity measures."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from oracle import bf16_bits_to_f64
+from sparse_mixture_experts_58_b300 import inputs
+
+# Parity bounds: fp32 layers, max|gpu - ref| / max|ref|; bf16 layers,
+# max|gpu - ref| / RMS(ref).  Tokens whose kept/next logits are closer than
+# NEAR_TIE on the oracle's fp32 logits are left out of index and output
+# comparisons and counted.
+TOL_F32 = 1e-4
+TOL_BF16 = 2e-2
+NEAR_TIE = 1e-3
+
+
+def host_f64(a: np.ndarray) -> np.ndarray:
+    if a.dtype == np.uint16:
+        return bf16_bits_to_f64(a)
+    return a.astype(np.float64)
+
+
+def near_tie_mask(logits: np.ndarray, k: int) -> np.ndarray:
+    """True for tokens whose sorted top-(k+1) logits have an adjacent gap
+    below NEAR_TIE (a selection or slot order that rounding may flip)."""
+    s = -np.sort(-logits.astype(np.float64), axis=1)
+    m = min(k + 1, logits.shape[1])
+    if m < 2:
+        return np.zeros(logits.shape[0], bool)
+    gaps = s[:, :m - 1] - s[:, 1:m]
+    return (gaps < NEAR_TIE).any(1)
+
+
+def rel_error(gpu: np.ndarray, ref: np.ndarray, dtype: str) -> float:
+    g = host_f64(gpu)
+    r = host_f64(ref) if ref.dtype == np.uint16 else ref.astype(np.float64)
+    if g.size == 0:
+        return 0.0
+    diff = np.abs(g - r).max()
+    if dtype == "f32":
+        den = np.abs(r).max()
+    else:
+        den = np.sqrt((r ** 2).mean())
+    return float(diff / den) if den > 0 else float(diff)
+
+
+def tol(dtype: str) -> float:
+    return TOL_F32 if dtype == "f32" else TOL_BF16
+
+
+def oracle_on_rows(x: torch.Tensor, layer: inputs.Layer, k: int, rows=None, threads=0,
+                   host_layer=None):
+    """Run the oracle on the given token rows (all when rows is None).
+    Returns (out, logits, idx, gates) as host arrays for those rows."""
+    o = oracle.load()
+    xs = x if rows is None else x[torch.as_tensor(rows, device=x.device, dtype=torch.long)]
+    xh = inputs.to_host(xs)
+    Wg, W1, W3, W2, bias = host_layer if host_layer is not None else inputs.layer_to_host(layer)
+    return o.moe_forward(xh, Wg, W1, W3, W2, k, bias=bias, threads=threads)
+
+
+def sample_rows(T: int, n: int, seed: int, must=()) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    pick = set(int(v) for v in must)
+    n = min(n, T)
+    if len(pick) < n:
+        extra = rng.choice(T, size=min(T, n), replace=False)
+        for v in extra:
+            if len(pick) >= n:
+                break
+            pick.add(int(v))
+    return np.array(sorted(pick), dtype=np.int64)

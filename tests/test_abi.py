@@ -1,0 +1,130 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point the
+header declares, sizes workspaces, and rejects bad arguments before touching
+the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from sparse_mixture_experts_58_b300 import build
+    build.build()
+    from sparse_mixture_experts_58_b300 import moe as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    assert "moe_forward" in names and "moe_route_from_logits" in names
+    assert len(names) >= 15
+
+
+def test_library_exports_every_declared_symbol(moe):
+    lib = moe.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libmoe.so does not export {name}"
+    # the binding wraps every declared entry point
+    assert sorted(moe.EXPORTED) == declared_functions()
+
+
+def test_strerror_and_version(moe):
+    assert moe.strerror(0) == "ok"
+    for code in (-1, -2, -3, -4, -5):
+        assert moe.strerror(code) != "unknown status"
+    assert moe.lib().moe_version() >= 100
+
+
+def test_workspace_sizes(moe):
+    # Mixtral decode/prefill shapes: scratch holds the grouped rows, the hidden
+    # activations and the fp32 partial outputs
+    for T in (1, 16, 4096, 8192, 16384):
+        n = moe.workspace_bytes(T, 4096, 14336, 8, 2, moe.BF16)
+        S = moe.down_splits(T, 4096, 14336, 8, 2, moe.BF16)
+        rows = 2 * T
+        assert n >= rows * 4096 * 2 + rows * 14336 * 2 + S * rows * 4096 * 4
+        assert n % 256 == 0
+        assert 1 <= S <= 14336 // 64
+    assert moe.workspace_bytes(0, 4096, 14336, 8, 2, moe.BF16) >= 0
+    assert moe.down_splits(4096, 4096, 14336, 8, 2, moe.BF16) == 1
+    assert moe.down_splits(16, 4096, 14336, 8, 2, moe.BF16) > 1
+    assert moe.forward_launches(16, 4096, 14336, 8, 2, moe.BF16) == 6
+    assert moe.forward_launches(0, 4096, 14336, 8, 2, moe.BF16) == 0
+
+
+@pytest.mark.parametrize("args,code", [
+    ((16, 4096, 14336, 8, 3, 1), -2),      # only k in {1, 2}
+    ((16, 4096, 14336, 2, 3, 1), -1),      # k > E
+    ((-1, 4096, 14336, 8, 2, 1), -1),      # negative T
+    ((16, 4096, 14336, 33, 2, 1), -2),     # too many experts
+    ((16, 4000, 14336, 8, 2, 1), -2),      # bf16 needs d % 64 == 0
+    ((16, 4096, 14300, 8, 2, 1), -2),      # bf16 needs ffn % 64 == 0
+    ((16, 130, 448, 8, 2, 0), -2),         # fp32 needs d % 4 == 0
+    ((16, 4096, 14336, 8, 2, 7), -1),      # unknown dtype
+])
+def test_workspace_rejects_bad_shapes(moe, args, code):
+    n = ctypes.c_size_t()
+    assert moe.lib().moe_workspace_bytes(*args, ctypes.byref(n)) == code
+
+
+def _forward_call(moe, **over):
+    E = over.get("E", 8)
+    arr = ctypes.c_void_p * E
+    fake = ctypes.c_void_p(0x10000)   # never dereferenced: validation fails first
+    w = arr(*([0x10000] * E))
+    a = dict(x=fake, Wg=fake, bias=None, W1=w, W3=w, W2=w, T=16, d=256, ffn=512, E=E, k=2,
+             dt=moe.BF16, out=fake, ws=None, ws_bytes=0, stream=None)
+    a.update(over)
+    return moe.lib().moe_forward(a["x"], a["Wg"], a["bias"], a["W1"], a["W3"], a["W2"], a["T"],
+                                 a["d"], a["ffn"], a["E"], a["k"], a["dt"], a["out"], a["ws"],
+                                 a["ws_bytes"], a["stream"])
+
+
+def test_forward_validates_before_launch(moe):
+    assert _forward_call(moe, k=3) == -2
+    assert _forward_call(moe, x=None) == -1
+    assert _forward_call(moe, W1=None) == -1
+    assert _forward_call(moe, ws=None) == -3                       # no workspace
+    assert _forward_call(moe, ws=ctypes.c_void_p(0x10000), ws_bytes=16) == -3
+    assert _forward_call(moe, x=ctypes.c_void_p(0x10008)) == -2    # misaligned tensor
+    assert _forward_call(moe, T=0) == 0                            # empty batch: no-op
+
+
+def test_fault_injection_fails_before_launch(moe, monkeypatch):
+    monkeypatch.setenv("MOE_FAULT_INJECT", "workspace")
+    assert _forward_call(moe) == -3
+    monkeypatch.setenv("MOE_FAULT_INJECT", "cuda")
+    assert _forward_call(moe) == -4
+    monkeypatch.setenv("MOE_FAULT_INJECT", "arg")
+    assert _forward_call(moe) == -1
+    monkeypatch.delenv("MOE_FAULT_INJECT")
+
+
+def test_binding_module_requires_library(tmp_path):
+    """Importing the binding without the built library raises (no fallback)."""
+    import subprocess
+    import sys
+    import shutil
+    pkg = os.path.join(ROOT, "sparse_mixture_experts_58_b300")
+    dst = tmp_path / "sparse_mixture_experts_58_b300"
+    dst.mkdir()
+    for f in ("__init__.py", "moe.py", "inputs.py"):
+        shutil.copy(os.path.join(pkg, f), dst / f)
+    code = ("import sys; sys.path.insert(0, %r)\n"
+            "try:\n    import sparse_mixture_experts_58_b300.moe\n"
+            "except ImportError as e:\n    print('raised', e); sys.exit(0)\n"
+            "sys.exit(1)\n") % str(tmp_path)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "not built" in r.stdout

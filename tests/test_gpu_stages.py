@@ -1,0 +1,165 @@
+"""Stage-by-stage parity of the CUDA path through the C ABI (needs a GPU).
+
+Router and grouping against the oracle; the grouped expert GEMMs against a
+plain torch fp32 evaluation of the same rows (a debugging aid: the layer
+tests compare everything against the oracle)."""
+import numpy as np
+import pytest
+import torch
+
+import helpers
+import oracle
+from sparse_mixture_experts_58_b300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from sparse_mixture_experts_58_b300 import moe as m
+    return m
+
+
+@pytest.fixture(autouse=True)
+def _status_clean(moe):
+    moe.device_status(clear=True)
+    yield
+    assert moe.device_status(clear=True) == 0, "a kernel's bounded wait expired"
+
+
+def _logits_with_ties(T, E, seed):
+    rng = np.random.default_rng(seed)
+    l = rng.standard_normal((T, E)).astype(np.float32)
+    l[::3] = (np.round(l[::3] * 2) / 2).astype(np.float32)   # many exact ties
+    l[5::7, :] = 0.0                                           # all-equal rows
+    return l
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 8, 2), (16, 8, 2), (17, 8, 2), (300, 8, 2), (4096, 8, 2),
+                                   (1000, 3, 1), (257, 32, 2), (64, 2, 2), (50, 1, 1),
+                                   (16384, 8, 2)])
+def test_route_from_logits_bit_exact(moe, T, E, k):
+    l = _logits_with_ties(T, E, seed=T * 31 + E)
+    idx, gates, counts, offsets, perm, inv = moe.route_from_logits(torch.from_numpy(l).cuda(), k)
+    torch.cuda.synchronize()
+    o = oracle.load()
+    ridx, rg, rcounts, roffsets, rperm, rinv = o.route(l, k)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    assert np.array_equal(counts.cpu().numpy(), rcounts)
+    assert np.array_equal(offsets.cpu().numpy(), roffsets)
+    assert np.array_equal(perm.cpu().numpy(), rperm)
+    assert np.array_equal(inv.cpu().numpy(), rinv)
+    assert np.allclose(gates.cpu().numpy(), rg, rtol=0, atol=2e-7)
+
+
+def test_route_empty(moe):
+    idx, gates, counts, offsets, perm, inv = moe.route_from_logits(
+        torch.zeros(0, 8, device="cuda"), 2)
+    torch.cuda.synchronize()
+    assert counts.sum().item() == 0 and offsets.abs().sum().item() == 0
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 64), ("decode", 16), ("prefill", 512)])
+def test_router_matches_oracle(moe, name, T):
+    x, layer = inputs.make_named(name, device="cuda", T=T)
+    k = layer.meta["k"]
+    logits, idx, gates = moe.router(x, layer.Wg, k, layer.bias)
+    torch.cuda.synchronize()
+    o = oracle.load()
+    rl, ridx, rg = o.router(inputs.to_host(x), inputs.to_host(layer.Wg), k)
+    assert np.allclose(logits.cpu().numpy(), rl, rtol=1e-5, atol=1e-5)
+    keep = ~helpers.near_tie_mask(rl, k)
+    assert np.array_equal(idx.cpu().numpy()[keep], ridx[keep])
+    assert np.allclose(gates.cpu().numpy()[keep], rg[keep], atol=2e-5)
+
+
+def test_router_skew_bias(moe):
+    x, layer = inputs.make_named("skewed", device="cuda", T=1024)
+    logits, idx, gates = moe.router(x, layer.Wg, 2, layer.bias)
+    torch.cuda.synchronize()
+    o = oracle.load()
+    rl, ridx, rg = o.router(inputs.to_host(x), inputs.to_host(layer.Wg), 2,
+                            bias=layer.bias.cpu().numpy())
+    keep = ~helpers.near_tie_mask(rl, 2)
+    assert np.array_equal(idx.cpu().numpy()[keep], ridx[keep])
+    share = np.bincount(ridx.ravel(), minlength=8) / ridx.size
+    assert share[0] > 0.3 and share[7] < 0.01      # experts 0-1 get most rows
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 4096), ("f32", 128), ("bf16", 64)])
+def test_permute_exact(moe, dtype, d):
+    T, k = 37, 2
+    g = torch.Generator(device="cuda").manual_seed(3)
+    x = torch.randn(T, d, device="cuda", generator=g).to(inputs.TORCH_DTYPE[dtype])
+    perm = torch.randperm(T * k, device="cuda", generator=g).to(torch.int32)
+    xp = moe.permute(x, perm, k)
+    torch.cuda.synchronize()
+    ref = x[(perm.long() // k)]
+    assert torch.equal(xp.view(torch.int16 if dtype == "bf16" else torch.int32),
+                       ref.view(torch.int16 if dtype == "bf16" else torch.int32))
+
+
+def _grouped_case(T, d, ffn, E, dtype, seed, skew=False):
+    x, layer = inputs.make_workload(T, d, ffn, E, 2, dtype, seed, "cuda",
+                                    bias=(inputs.SKEW_BIAS if skew else None))
+    return x, layer
+
+
+def _torch_swiglu_rows(x_perm, offsets, W1, W3):
+    xp = x_perm.float()
+    h = torch.empty(xp.shape[0], W1.shape[1], device=xp.device)
+    off = offsets.cpu().tolist()
+    for e in range(W1.shape[0]):
+        a, b = off[e], off[e + 1]
+        if b > a:
+            u = xp[a:b] @ W1[e].float().T
+            v = xp[a:b] @ W3[e].float().T
+            h[a:b] = torch.nn.functional.silu(u) * v
+    return h
+
+
+@pytest.mark.parametrize("T,d,ffn,E,skew", [
+    (16, 256, 448, 8, False),      # narrow tiles, ragged last column tile
+    (200, 128, 256, 4, False),     # 100 rows per expert: narrow, several row tiles
+    (700, 192, 384, 8, False),     # wide tiles (175 rows/expert), ragged rows
+    (1024, 256, 512, 8, True),     # skewed: one expert with many row tiles
+    (5, 64, 64, 8, False),         # several experts empty
+])
+def test_grouped_gemms_against_torch(moe, T, d, ffn, E, skew):
+    x, layer = _grouped_case(T, d, ffn, E, "bf16", seed=T, skew=skew)
+    logits, idx, gates = moe.router(x, layer.Wg, 2, layer.bias)
+    idx2, gates2, counts, offsets, perm, inv = moe.route_from_logits(logits, 2)
+    xp = moe.permute(x, perm, 2)
+    h = moe.expert_swiglu(xp, offsets, layer.W1, layer.W3)
+    y = moe.expert_down(h, offsets, layer.W2, T, 2)
+    out = moe.combine(y, gates2, inv, T, 2, torch.bfloat16)
+    torch.cuda.synchronize()
+    href = _torch_swiglu_rows(xp, offsets, layer.W1, layer.W3)
+    scale = href.pow(2).mean().sqrt().item()
+    assert (h.float() - href).abs().max().item() <= 2e-2 * scale + 1e-6
+    # down projection from the GPU's own h
+    yref = torch.empty(h.shape[0], d, device="cuda")
+    off = offsets.cpu().tolist()
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if b > a:
+            yref[a:b] = h[a:b].float() @ layer.W2[e].float().T
+    ysum = y.sum(0)
+    yscale = yref.pow(2).mean().sqrt().item()
+    assert (ysum - yref).abs().max().item() <= 1e-3 * yscale + 1e-6
+    oref = torch.zeros(T, d, device="cuda")
+    for j in range(2):
+        oref += gates2[:, j:j + 1] * ysum[inv.view(T, 2)[:, j].long()]
+    assert (out.float() - oref).abs().max().item() <= 1e-2 * oref.pow(2).mean().sqrt().item()
+
+
+def test_wait_timeout_selftest(moe):
+    """A bounded wait that nothing satisfies gives up, reports, and leaves the
+    context usable."""
+    moe.selftest_wait_timeout(2_000_000)
+    assert moe.device_status(clear=True) == 5
+    a = torch.ones(1024, device="cuda")
+    assert a.sum().item() == 1024.0
+    assert moe.device_status(clear=True) == 0
