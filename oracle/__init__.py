@@ -47,7 +47,7 @@ def _declare(lib):
     lib.oracle_moe_forward.argtypes = [
         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
         c_int, c_int, c_int, c_int, c_int, c_int,
-        c_void_p, c_void_p, c_void_p, c_void_p, c_int]
+        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int]
     lib.oracle_moe_forward.restype = c_int
     lib.oracle_router.argtypes = [c_void_p, c_void_p, c_void_p, c_int, c_int,
                                   c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]
@@ -105,18 +105,20 @@ class Oracle:
     def max_threads(self) -> int:
         return self.lib.oracle_max_threads()
 
-    def moe_forward(self, x, Wg, W1, W3, W2, k, bias=None, threads=0):
+    def moe_forward(self, x, Wg, W1, W3, W2, k, bias=None, threads=0, exact=False):
         """Whole layer.  Returns (out, logits fp32 [T,E], idx int32 [T,k],
-        gates float64 [T,k]); ``out`` has x's element type."""
+        gates float64 [T,k]); ``out`` has x's element type.  With
+        ``exact=True`` a fifth item is the float64 result before rounding."""
         x = np.ascontiguousarray(x)
         dt = _dt_code(x)
         T, d = x.shape
         E = Wg.shape[0]
-        ffn = W1.shape[1]
         Wg = np.ascontiguousarray(Wg)
         W1 = [np.ascontiguousarray(w) for w in W1]
         W3 = [np.ascontiguousarray(w) for w in W3]
         W2 = [np.ascontiguousarray(w) for w in W2]
+        ffn = W1[0].shape[0]
+        assert len(W1) == len(W3) == len(W2) == E
         for w in (Wg, *W1, *W3, *W2):
             assert w.dtype == x.dtype
         assert Wg.shape == (E, d)
@@ -131,11 +133,14 @@ class Oracle:
         logits = np.empty((T, E), np.float32)
         idx = np.empty((T, k), np.int32)
         gates = np.empty((T, k), np.float64)
+        ex = np.empty((T, d), np.float64) if exact else None
         rc = self.lib.oracle_moe_forward(
             _ptr(x), _ptr(Wg), _ptr(b), p1, p3, p2, T, d, ffn, E, k, dt,
-            _ptr(out), _ptr(logits), _ptr(idx), _ptr(gates), int(threads))
+            _ptr(out), _ptr(logits), _ptr(idx), _ptr(gates), _ptr(ex), int(threads))
         if rc != 0:
             raise RuntimeError(f"oracle_moe_forward failed: {rc}")
+        if exact:
+            return out, logits, idx, gates, ex
         return out, logits, idx, gates
 
     def router(self, x, Wg, k, bias=None):

@@ -178,13 +178,14 @@ static int all_finite_f32(const float *p, size_t n)
  * out[t] = sum_j g[t][j] * W2[e_j] ( silu(W1[e_j] x_t) * (W3[e_j] x_t) )
  * with e_j and g the router's selection and gates for token t.
  * Optional outputs (pass NULL to skip): logits [T][E] fp32, idx [T][k],
- * gates [T][k] in double.
+ * gates [T][k] in double, and out_exact [T][d]: the weighted sum in double
+ * before the one rounding to the element type.
  */
 int oracle_moe_forward(const void *x, const void *Wg, const float *bias,
                        const void *const *W1, const void *const *W3,
                        const void *const *W2, int T, int d, int ffn, int E, int k,
                        int dt, void *out, float *logits_out, int *idx_out,
-                       double *gates_out, int nthreads)
+                       double *gates_out, double *out_exact, int nthreads)
 {
     if (T < 0 || d < 1 || ffn < 1 || E < 1 || k < 1 || k > E ||
         (dt != ORACLE_F32 && dt != ORACLE_BF16))
@@ -249,6 +250,9 @@ int oracle_moe_forward(const void *x, const void *Wg, const float *bias,
             }
             for (int n = 0; n < d; ++n)
                 store_elem(out, xo + (size_t)n, dt, acc[n]);
+            if (out_exact)
+                for (int n = 0; n < d; ++n)
+                    out_exact[xo + (size_t)n] = acc[n];
             if (logits_out)
                 for (int e = 0; e < E; ++e)
                     logits_out[(size_t)t * E + e] = l[e];

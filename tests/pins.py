@@ -319,6 +319,20 @@ def pin_token_independence(o):
     assert np.array_equal(outp, out[p])
 
 
+def pin_exact_output_rounds_to_out(o):
+    """The unrounded result the oracle exposes is the value its output rounds
+    from: one nearest-even rounding per element, in both storage types."""
+    rng = _rng(16)
+    x, Wg, W1, W3, W2 = _rand_layer(rng, 12, 16, 24, 4)
+    out, _, _, _, ex = o.moe_forward(x, Wg, W1, W3, W2, 2, exact=True)
+    assert np.array_equal(out, ex.astype(np.float32))
+    to = lambda a: torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    outb, _, _, _, exb = o.moe_forward(to(x), to(Wg), to(W1), to(W3), to(W2), 2, exact=True)
+    assert np.array_equal(outb, np.array([o.to_bf16(v) for v in exb.ravel()],
+                                         np.uint16).reshape(outb.shape))
+    assert np.all(np.abs(bf16_bits_to_f64(outb) - exb) <= np.abs(exb) * 2.0 ** -8)
+
+
 def pin_down_projection_linear(o):
     """Doubling W2 doubles the output exactly (a power-of-two scale commutes
     with every rounding)."""

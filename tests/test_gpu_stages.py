@@ -138,7 +138,10 @@ def test_grouped_gemms_against_torch(moe, T, d, ffn, E, skew):
     torch.cuda.synchronize()
     href = _torch_swiglu_rows(xp, offsets, layer.W1, layer.W3)
     scale = href.pow(2).mean().sqrt().item()
-    assert (h.float() - href).abs().max().item() <= 2e-2 * scale + 1e-6
+    # h is stored in bf16: each element is within half a bf16 ulp (2^-9
+    # relative) of its fp32 value, plus accumulation-order differences
+    bound = href.abs() * 2.0 ** -8 + 1e-3 * scale
+    assert ((h.float() - href).abs() <= bound).all(), (h.float() - href).abs().max().item()
     # down projection from the GPU's own h
     yref = torch.empty(h.shape[0], d, device="cuda")
     off = offsets.cpu().tolist()
@@ -152,7 +155,8 @@ def test_grouped_gemms_against_torch(moe, T, d, ffn, E, skew):
     oref = torch.zeros(T, d, device="cuda")
     for j in range(2):
         oref += gates2[:, j:j + 1] * ysum[inv.view(T, 2)[:, j].long()]
-    assert (out.float() - oref).abs().max().item() <= 1e-2 * oref.pow(2).mean().sqrt().item()
+    obound = oref.abs() * 2.0 ** -8 + 1e-4 * oref.pow(2).mean().sqrt().item()
+    assert ((out.float() - oref).abs() <= obound).all()
 
 
 def test_wait_timeout_selftest(moe):
