@@ -198,6 +198,35 @@ int moe_selftest_wait_timeout(unsigned int limit_ns, void *stream);
 /* Number of kernels moe_forward launches for this shape (for launch counts). */
 int moe_forward_launches(int T, int d, int ffn, int E, int k, int dtype, int *launches);
 
+/*
+ * The pages have no counterpart to this entry point: it is a convenience for
+ * callers that cannot allocate device memory where they run the layer (an
+ * inference-engine plugin handed fixed buffers, a serving process whose
+ * memory budget was reserved at start-up, code running while a stream is
+ * captured into a CUDA graph, where cudaMalloc is refused).
+ *
+ * Same result as moe_forward, but the scratch is a fixed array of
+ * MOE_STATIC_SCRATCH_BYTES inside the library on each device, held until the
+ * process exits, so no workspace is passed and nothing is allocated.  The
+ * caller still passes x, the weights and out.
+ *   - Shapes whose moe_workspace_bytes(...) exceeds MOE_STATIC_SCRATCH_BYTES
+ *     are rejected with MOE_ERR_WORKSPACE before anything is enqueued (at the
+ *     Mixtral shape, d = 4096 and ffn = 14336 with 8 experts and top-2,
+ *     this covers batches of up to 70 tokens).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins.
+ *   - Every call on a device shares the one array: calls whose GPU work can
+ *     overlap (other streams, other host threads) race and must be
+ *     serialised by the caller.  Contents left by a previous call are never
+ *     read; nothing needs clearing.
+ */
+#define MOE_STATIC_SCRATCH_BYTES (16u << 20)
+int moe_forward_static_scratch(const void *x, const void *W_g, const float *router_bias,
+                               const void *const *W1, const void *const *W3,
+                               const void *const *W2, int T, int d, int ffn, int E, int k,
+                               int dtype, void *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -58,12 +58,16 @@ _sig("moe_add_rmsnorm", _i, _vp, _vp, _vp, _i, _i, ctypes.c_float, _i, _vp)
 _sig("moe_device_status", _i, _vp, _P(_i), _i)
 _sig("moe_selftest_wait_timeout", _i, ctypes.c_uint, _vp)
 _sig("moe_forward_launches", _i, _i, _i, _i, _i, _i, _i, _P(_i))
+_sig("moe_forward_static_scratch", _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
+     _vp, _vp)
+STATIC_SCRATCH_BYTES = 16 << 20
 
 EXPORTED = [
     "moe_strerror", "moe_version", "moe_workspace_bytes", "moe_forward", "moe_forward_host_io",
     "moe_router", "moe_route_workspace_bytes", "moe_route_from_logits", "moe_permute",
     "moe_expert_swiglu", "moe_down_splits", "moe_expert_down", "moe_combine",
     "moe_add_rmsnorm", "moe_device_status", "moe_selftest_wait_timeout", "moe_forward_launches",
+    "moe_forward_static_scratch",
 ]
 
 
@@ -285,3 +289,16 @@ def device_status(clear=True, stream=None) -> int:
 
 def selftest_wait_timeout(limit_ns=1_000_000, stream=None):
     _check(_lib.moe_selftest_wait_timeout(int(limit_ns), _stream(stream)), "moe_selftest_wait_timeout")
+
+
+def forward_static_scratch(x, Wg, W1, W3, W2, k=2, bias=None, out=None, stream=None):
+    """out = MoE(x) through moe_forward_static_scratch: no workspace, the
+    library's fixed per-device scratch instead (see include/moe.h)."""
+    T, d, ffn, E = _shape(x, Wg, W1)
+    if out is None:
+        out = torch.empty_like(x)
+    p1, p3, p2 = _expert_ptrs(W1, E), _expert_ptrs(W3, E), _expert_ptrs(W2, E)
+    _check(_lib.moe_forward_static_scratch(_ptr(x), _ptr(Wg), _ptr(bias), p1, p3, p2, T, d, ffn,
+                                           E, k, _dt(x), _ptr(out), _stream(stream)),
+           "moe_forward_static_scratch")
+    return out
