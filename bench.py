@@ -81,9 +81,41 @@ def load_peaks():
     return dict(PEAKS_FALLBACK), "fallback"
 
 
+class _Nvml:
+    """Read-only NVML queries through the driver's libnvidia-ml (ctypes):
+    SM clock, its maximum, and the active clock-event reasons."""
+
+    def __init__(self, index):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sm_mhz(self):
+        v = self.ct.c_uint()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, self.ct.byref(v))   # 1 = SM clock
+        return v.value
+
+    def sm_max_mhz(self):
+        v = self.ct.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, self.ct.byref(v))
+        return v.value
+
+    def reasons(self):
+        v = self.ct.c_ulonglong()
+        self.reasons_fn(self.h, self.ct.byref(v))
+        return v.value
+
+
 class ClockSampler:
     """NVML samples (SM clock, max clock, clock-event reasons) every few ms
-    while running; read-only."""
+    while running; read-only.  Uses the driver's NVML library directly."""
 
     REASONS = {
         "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4,
@@ -92,17 +124,14 @@ class ClockSampler:
         "display_clock_setting": 0x100,
     }
 
-    def __init__(self, index: int, period_s: float = 0.005):
+    def __init__(self, index: int, period_s: float = 0.002):
         self.samples = []
         self.period = period_s
         self.ok = False
         self.max_mhz = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.nv = _Nvml(index)
+            self.max_mhz = self.nv.sm_max_mhz()
             self.ok = True
         except Exception as e:  # no NVML: report that instead of clocks
             self.err = repr(e)
@@ -110,12 +139,9 @@ class ClockSampler:
         self._t = None
 
     def _run(self):
-        nv = self.nv
         while not self._stop.is_set():
             try:
-                mhz = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
-                rs = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                self.samples.append((mhz, rs))
+                self.samples.append((self.nv.sm_mhz(), self.nv.reasons()))
             except Exception:
                 pass
             time.sleep(self.period)
@@ -279,33 +305,52 @@ def measure(args, rank, world, local):
         step()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    clocks = ClockSampler(local)
 
-    barrier(world)
-    torch.cuda.synchronize()
+    # The timed step is the forward captured once into a CUDA graph (the same
+    # C-ABI call and kernels; replays cost one graph launch of host time).
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+    run = graph.replay if graph is not None else step
+
+    def timed(fn, n):
+        barrier(world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return reduce_max(e0.elapsed_time(e1) / 1e3, world, dev)
+
+    clocks = ClockSampler(local)
     clocks.start()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    elapsed_max = timed(run, args.steps)
     clocks.stop()
-    barrier(world)
-    elapsed = ev0.elapsed_time(ev1) / 1e3
-    elapsed_max = reduce_max(elapsed, world, dev)
     status = moe.device_status(clear=True)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
+    # the same forward called directly (host launch overhead included)
+    direct_elapsed = timed(step, args.steps)
 
     # -- per-stage breakdown through the stage entry points (same kernels),
-    #    events on the launching stream between stages
+    #    events on the launching stream between stages; a sleep kernel first
+    #    lets the host queue the whole sequence so the events see GPU time
     stage_names = ["router", "route", "permute", "gate_up_swiglu", "down", "combine"]
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(stage_names) + 1)]
     acc = [0.0] * len(stage_names)
     n_rep = max(3, min(args.steps, 50))
     for rep in range(n_rep + 2):
+        torch.cuda._sleep(2_000_000)
         evs[0].record(stream)
         logits, _, _ = moe.router(x, layer.Wg, k, bias)
         evs[1].record(stream)
@@ -338,17 +383,7 @@ def measure(args, rank, world, local):
 
     for _ in range(2):
         e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_elapsed = reduce_max(e0.elapsed_time(e1) / 1e3, world, dev)
+    e2e_elapsed = timed(e2e_step, args.steps)
 
     if rank != 0:
         return 0
@@ -403,7 +438,12 @@ def measure(args, rank, world, local):
         },
         "stages_us": {n: s * 1e6 for n, s in zip(stage_names, stage_s)},
         "e2e": {"value": T * world * args.steps / e2e_elapsed, "unit": "tokens/s",
-                "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2},
+                "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2,
+                "how": "moe_forward_host_io called per step: pinned x -> device, layer, "
+                       "out -> pinned host, all on one stream"},
+        "timed_as": "CUDA graph replay of one moe_forward call per step" if graph is not None
+                    else "moe_forward called per step",
+        "direct_call_tokens_per_s": T * world * args.steps / direct_elapsed,
         "gpu_launches": moe.forward_launches(T, d, ffn, E, k, moe.BF16) * args.steps,
         "clocks": clocks.summary(),
     }
@@ -421,6 +461,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", choices=sorted(WORKLOAD_NAMES), default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time direct moe_forward calls instead of a captured CUDA graph")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

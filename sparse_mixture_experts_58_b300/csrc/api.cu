@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <unordered_map>
 
 #include "internal.h"
 
@@ -95,8 +96,65 @@ int *device_status_ptr() {
     return g_status_ptr[dev];
 }
 
+namespace {
+
+// Encoded tensor maps, keyed by everything that goes into one.  A map depends
+// only on these values, so a cached entry is always valid; the cache is
+// emptied when it grows past kMapCacheMax entries.
+struct MapKey {
+    const void *base;
+    unsigned long long inner, outer;
+    unsigned int box_inner, box_outer;
+    bool operator==(const MapKey &o) const {
+        return base == o.base && inner == o.inner && outer == o.outer &&
+               box_inner == o.box_inner && box_outer == o.box_outer;
+    }
+};
+
+struct MapKeyHash {
+    size_t operator()(const MapKey &k) const {
+        size_t h = std::hash<const void *>()(k.base);
+        h ^= std::hash<unsigned long long>()(k.inner * 1000003ull + k.outer) + 0x9e3779b97f4a7c15ull +
+             (h << 6) + (h >> 2);
+        h ^= std::hash<unsigned long long>()(((unsigned long long)k.box_inner << 32) | k.box_outer) +
+             0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+        return h;
+    }
+};
+
+constexpr size_t kMapCacheMax = 8192;
+std::mutex g_map_mutex;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_map_cache;
+
+int encode_uncached(CUtensorMap *map, const void *base, unsigned long long inner,
+                    unsigned long long outer, unsigned int box_inner, unsigned int box_outer);
+
+}  // namespace
+
 int encode_map_bf16_2d(CUtensorMap *map, const void *base, unsigned long long inner,
                        unsigned long long outer, unsigned int box_inner, unsigned int box_outer) {
+    const MapKey key{base, inner, outer, box_inner, box_outer};
+    {
+        std::lock_guard<std::mutex> g(g_map_mutex);
+        auto it = g_map_cache.find(key);
+        if (it != g_map_cache.end()) {
+            *map = it->second;
+            return MOE_OK;
+        }
+    }
+    const int rc = encode_uncached(map, base, inner, outer, box_inner, box_outer);
+    if (rc == MOE_OK) {
+        std::lock_guard<std::mutex> g(g_map_mutex);
+        if (g_map_cache.size() >= kMapCacheMax) g_map_cache.clear();
+        g_map_cache.emplace(key, *map);
+    }
+    return rc;
+}
+
+namespace {
+
+int encode_uncached(CUtensorMap *map, const void *base, unsigned long long inner,
+                    unsigned long long outer, unsigned int box_inner, unsigned int box_outer) {
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -118,6 +176,8 @@ int encode_map_bf16_2d(CUtensorMap *map, const void *base, unsigned long long in
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
+
+}  // namespace
 
 // Tile plan.  Rows per expert decide the tile family: with many rows per
 // expert (prefill) 256-wide tiles keep the tensor cores fed; with few
@@ -209,9 +269,10 @@ int run_forward(const Plan &P, const void *x, const void *W_g, const float *bias
     const int elt = elem_size(P.dt);
     int rc;
     if ((rc = cuda_rc(launch_router(x, W_g, bias, P.T, P.d, P.E, P.k, P.dt, logits, idx, gates,
-                                    cc, s))) != MOE_OK)
+                                    s))) != MOE_OK)
         return rc;
-    if ((rc = cuda_rc(launch_chunk_scan(cc, P.nchunks, P.E, cb, counts, offsets, s))) != MOE_OK)
+    if ((rc = cuda_rc(launch_chunk_scan(idx, P.T, P.k, P.E, cc, cb, counts, offsets, s))) !=
+        MOE_OK)
         return rc;
     if ((rc = cuda_rc(launch_group_tokens(idx, cb, offsets, x, P.T, P.d, P.E, P.k, elt, perm, inv,
                                           x_perm, s))) != MOE_OK)
@@ -341,9 +402,8 @@ int moe_router(const void *x, const void *W_g, const float *router_bias, int T, 
     if (T == 0) return MOE_OK;
     if (!x || !W_g || !logits || !idx || !gates) return MOE_ERR_ARG;
     if (!aligned16(x) || !aligned16(W_g)) return MOE_ERR_UNSUPPORTED;
-    // this entry point returns no per-chunk counts: the kernel skips them
     return cuda_rc(launch_router(x, W_g, router_bias, T, d, E, k, dtype, logits, idx, gates,
-                                 nullptr, static_cast<cudaStream_t>(stream)));
+                                 static_cast<cudaStream_t>(stream)));
 }
 
 int moe_route_workspace_bytes(int T, int E, int k, size_t *bytes) {
@@ -378,9 +438,9 @@ int moe_route_from_logits(const float *logits, int T, int E, int k, int *idx, fl
     int *cc = static_cast<int *>(workspace);
     int *cb = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) +
                                       align_up((size_t)nchunks * E * 4));
-    if ((rc = cuda_rc(launch_topk_from_logits(logits, T, E, k, idx, gates, cc, s))) != MOE_OK)
+    if ((rc = cuda_rc(launch_topk_from_logits(logits, T, E, k, idx, gates, s))) != MOE_OK)
         return rc;
-    if ((rc = cuda_rc(launch_chunk_scan(cc, nchunks, E, cb, counts, offsets, s))) != MOE_OK)
+    if ((rc = cuda_rc(launch_chunk_scan(idx, T, k, E, cc, cb, counts, offsets, s))) != MOE_OK)
         return rc;
     return cuda_rc(launch_group_tokens(idx, cb, offsets, nullptr, T, 0, E, k, 0, perm, inv,
                                        nullptr, s));

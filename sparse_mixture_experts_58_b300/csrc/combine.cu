@@ -29,42 +29,73 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *p, float4 v
     *reinterpret_cast<uint2 *>(p) = u;
 }
 
+__device__ __forceinline__ void add4(float4 &s, const float4 &p) {
+    s.x += p.x;
+    s.y += p.y;
+    s.z += p.z;
+    s.w += p.w;
+}
+
+// Block (t, c): token t, columns [1024 c, 1024 c + 1024); one thread per four
+// columns.  Up to kSplitBatch partial sums per slot are loaded together, then
+// added in split order, so a thread waits for one round trip per batch.
+constexpr int kSplitBatch = 8;
+
 template <typename T>
 __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ y, int splits,
                                                       int rows, const float *__restrict__ gates,
                                                       const int *__restrict__ inv, int Tn, int d,
                                                       int k, T *out) {
-    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (t >= Tn) return;
-    int rowj[2];
-    float gj[2];
-    for (int j = 0; j < k; ++j) {
-        rowj[j] = inv[(size_t)t * k + j];
-        gj[j] = gates[(size_t)t * k + j];
-    }
-    const int nv = d / 4;
-    const size_t split_stride = (size_t)rows * d;
-#pragma unroll 2
-    for (int v = lane; v < nv; v += 32) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < k; ++j) {
-            const float4 *src = reinterpret_cast<const float4 *>(y + (size_t)rowj[j] * d) + v;
-            float4 s = __ldcs(src);
-            for (int q = 1; q < splits; ++q) {
-                const float4 p = __ldcs(src + q * split_stride / 4);
-                s.x += p.x;
-                s.y += p.y;
-                s.z += p.z;
-                s.w += p.w;
-            }
-            acc.x = fmaf(gj[j], s.x, acc.x);
-            acc.y = fmaf(gj[j], s.y, acc.y);
-            acc.z = fmaf(gj[j], s.z, acc.z);
-            acc.w = fmaf(gj[j], s.w, acc.w);
+    const int t = blockIdx.x;
+    const int v = blockIdx.y * 256 + threadIdx.x;  // float4 column group
+    if (v >= d / 4) return;
+    const size_t stride4 = (size_t)rows * d / 4;   // one split, in float4
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    int rowj[2] = {0, 0};
+    float gj[2] = {0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        if (j < k) {
+            rowj[j] = inv[(size_t)t * k + j];
+            gj[j] = gates[(size_t)t * k + j];
         }
-        store4<T>(out + (size_t)t * d + 4 * v, acc);
     }
+    float4 s[2] = {zero, zero};
+    for (int q0 = 0; q0 < splits; q0 += kSplitBatch) {
+        float4 p[2][kSplitBatch];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float4 *src = reinterpret_cast<const float4 *>(y) + (size_t)rowj[j] * (d / 4) + v;
+#pragma unroll
+            for (int i = 0; i < kSplitBatch; ++i)
+                p[j][i] = (j < k && q0 + i < splits) ? __ldcs(src + (size_t)(q0 + i) * stride4)
+                                                     : zero;
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            if (q0 == 0) {
+                s[j] = p[j][0];
+#pragma unroll
+                for (int i = 1; i < kSplitBatch; ++i)
+                    if (q0 + i < splits) add4(s[j], p[j][i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < kSplitBatch; ++i)
+                    if (q0 + i < splits) add4(s[j], p[j][i]);
+            }
+        }
+    }
+    float4 acc = zero;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        if (j < k) {
+            acc.x = fmaf(gj[j], s[j].x, acc.x);
+            acc.y = fmaf(gj[j], s[j].y, acc.y);
+            acc.z = fmaf(gj[j], s[j].z, acc.z);
+            acc.w = fmaf(gj[j], s[j].w, acc.w);
+        }
+    }
+    store4<T>(out + (size_t)t * d + 4 * v, acc);
 }
 
 // One block per row: optional residual add (rounded to the storage type),
@@ -113,7 +144,7 @@ cudaError_t launch_combine(const float *y, int splits, int rows, const float *ga
                            const int *inv, int T, int d, int k, int dt, void *out,
                            cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    const int grid = (T + 7) / 8;
+    const dim3 grid(T, (d / 4 + 255) / 256);
     if (dt == MOE_BF16)
         combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(y, splits, rows, gates, inv, T, d, k,
                                                            static_cast<__nv_bfloat16 *>(out));

@@ -332,10 +332,17 @@ int run_tc(TcArgs &args, int units_bound, cudaStream_t s) {
     using L = SmemLayout<NB, STAGES>;
     auto kernel = grouped_gemm_tc<NB, STAGES, SWIGLU>;
     {
+        // once per device, so later launches (and stream capture) only enqueue
+        static bool attr_set[64];
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
         std::lock_guard<std::mutex> g(g_attr_mutex);
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(L::kTotal)) != cudaSuccess)
-            return MOE_ERR_CUDA;
+        if (!attr_set[dev]) {
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(L::kTotal)) != cudaSuccess)
+                return MOE_ERR_CUDA;
+            attr_set[dev] = true;
+        }
     }
     const int grid = units_bound < device_sm_count() ? units_bound : device_sm_count();
     if (grid <= 0) return MOE_OK;

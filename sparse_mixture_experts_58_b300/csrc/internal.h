@@ -37,12 +37,13 @@ int *device_status_ptr();
 
 // Kernel launchers (each returns the launch's cudaError_t).
 cudaError_t launch_router(const void *x, const void *Wg, const float *bias, int T, int d, int E,
-                          int k, int dt, float *logits, int *idx, float *gates, int *chunk_counts,
-                          cudaStream_t s);
+                          int k, int dt, float *logits, int *idx, float *gates, cudaStream_t s);
 cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, int *idx,
-                                    float *gates, int *chunk_counts, cudaStream_t s);
-cudaError_t launch_chunk_scan(const int *chunk_counts, int nchunks, int E, int *chunk_base,
-                              int *counts, int *offsets, cudaStream_t s);
+                                    float *gates, cudaStream_t s);
+// Per-chunk expert counts from idx (into chunk_counts), then their per-expert
+// exclusive scan: chunk_base, counts, offsets.
+cudaError_t launch_chunk_scan(const int *idx, int T, int k, int E, int *chunk_counts,
+                              int *chunk_base, int *counts, int *offsets, cudaStream_t s);
 cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int *offsets,
                                 const void *x, int T, int d, int E, int k, int elt, int *perm,
                                 int *inv, void *x_perm, cudaStream_t s);

@@ -14,12 +14,29 @@
 namespace moe {
 namespace {
 
-// One block of 1024 threads; warp e scans expert e's column of chunk counts.
-__global__ void __launch_bounds__(1024) chunk_scan_kernel(const int *__restrict__ cc, int nchunks,
-                                                          int E, int *chunk_base, int *counts,
-                                                          int *offsets) {
+// One block of 1024 threads.  First each warp counts, for its chunks of
+// kChunk tokens, how many of the chunk's kChunk*k (<= 32) selections hit each
+// expert (one ballot per expert); then warp e scans expert e's column of
+// those counts.  The counts go through global memory (cc); __syncthreads()
+// orders the block's writes before its reads.
+__global__ void __launch_bounds__(1024) chunk_scan_kernel(const int *__restrict__ idx, int Tn,
+                                                          int k, int E, int *cc, int *chunk_base,
+                                                          int *counts, int *offsets) {
     __shared__ int s_tot[MOE_MAX_EXPERTS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nchunks = (Tn + kChunk - 1) / kChunk;
+    for (int c = warp; c < nchunks; c += 32) {
+        const int first = c * kChunk;
+        const int nsel = min(kChunk, Tn - first) * k;
+        const int sel = lane < nsel ? idx[(size_t)first * k + lane] : -1;
+        int mine = 0;
+        for (int e = 0; e < E; ++e) {
+            const int n = __popc(__ballot_sync(0xffffffffu, sel == e));
+            if (lane == e) mine = n;
+        }
+        if (lane < E) cc[(size_t)c * E + lane] = mine;
+    }
+    __syncthreads();
     if (warp < E) {
         int carry = 0;
         for (int base = 0; base < nchunks; base += 32) {
@@ -48,14 +65,26 @@ __global__ void __launch_bounds__(1024) chunk_scan_kernel(const int *__restrict_
     }
 }
 
-// Copy one row (rowvec 16-byte vectors) from src to k destinations.
+// Copy one row (rowvec 16-byte vectors) from src to one or two destinations,
+// one warp; four loads per lane are issued before their stores.
 __device__ __forceinline__ void copy_row(const uint4 *__restrict__ src, uint4 *dst0, uint4 *dst1,
                                          int rowvec, int lane) {
-#pragma unroll 4
-    for (int v = lane; v < rowvec; v += 32) {
-        const uint4 val = __ldcs(src + v);
-        dst0[v] = val;
-        if (dst1 != nullptr) dst1[v] = val;
+    constexpr int U = 4;
+    for (int v0 = lane; v0 < rowvec; v0 += 32 * U) {
+        uint4 val[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + 32 * u;
+            val[u] = __ldcs(src + (v < rowvec ? v : 0));
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + 32 * u;
+            if (v < rowvec) {
+                dst0[v] = val[u];
+                if (dst1 != nullptr) dst1[v] = val[u];
+            }
+        }
     }
 }
 
@@ -80,21 +109,46 @@ __global__ void __launch_bounds__(256) group_tokens_kernel(
             for (int i2 = 0; i2 < i; ++i2)
                 for (int j2 = 0; j2 < k; ++j2) rank += (s_idx[i2 * k + j2] == e);
             const int r = offsets[e] + chunk_base[(size_t)c * E + e] + rank;
-            perm[r] = t * k + j;
-            inv[(size_t)t * k + j] = r;
+            if (blockIdx.y == 0) {
+                perm[r] = t * k + j;
+                inv[(size_t)t * k + j] = r;
+            }
             s_row[i * k + j] = r;
         }
     }
     if (x == nullptr) return;
     __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rowvec = static_cast<int>(row_bytes / 16);
-    for (int i = warp * 2; i < warp * 2 + 2 && i < ntok; ++i) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(first + i) * row_bytes);
-        uint4 *d0 = reinterpret_cast<uint4 *>(x_perm + (size_t)s_row[i * k] * row_bytes);
-        uint4 *d1 = k > 1 ? reinterpret_cast<uint4 *>(x_perm + (size_t)s_row[i * k + 1] * row_bytes)
-                          : nullptr;
-        copy_row(src, d0, d1, rowvec, lane);
+    // This block's slice of the chunk's rows (blockIdx.y of gridDim.y parts),
+    // flattened to (token, 16-byte vector) pairs over all threads; each thread
+    // issues U loads, then writes each value to the token's k grouped rows.
+    constexpr int U = 8;
+    const int rowvec_all = static_cast<int>(row_bytes / 16);
+    const int vbeg = (int)((long long)rowvec_all * blockIdx.y / gridDim.y);
+    const int vend = (int)((long long)rowvec_all * (blockIdx.y + 1) / gridDim.y);
+    const int rowvec = vend - vbeg;
+    const int total = ntok * rowvec;
+    const uint4 *xs = reinterpret_cast<const uint4 *>(x + (size_t)first * row_bytes);
+    for (int i0 = threadIdx.x; i0 < total; i0 += blockDim.x * U) {
+        uint4 val[U];
+        int tok[U], vec[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + blockDim.x * u;
+            const int ii = i < total ? i : 0;
+            tok[u] = ii / rowvec;
+            vec[u] = vbeg + (ii - tok[u] * rowvec);
+            val[u] = __ldcs(xs + (size_t)tok[u] * rowvec_all + vec[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (i0 + (int)blockDim.x * u < total) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    if (j < k)
+                        reinterpret_cast<uint4 *>(x_perm + (size_t)s_row[tok[u] * k + j] *
+                                                               row_bytes)[vec[u]] = val[u];
+            }
+        }
     }
 }
 
@@ -112,9 +166,10 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint8_t *__restrict_
 
 }  // namespace
 
-cudaError_t launch_chunk_scan(const int *chunk_counts, int nchunks, int E, int *chunk_base,
-                              int *counts, int *offsets, cudaStream_t s) {
-    chunk_scan_kernel<<<1, 1024, 0, s>>>(chunk_counts, nchunks, E, chunk_base, counts, offsets);
+cudaError_t launch_chunk_scan(const int *idx, int T, int k, int E, int *chunk_counts,
+                              int *chunk_base, int *counts, int *offsets, cudaStream_t s) {
+    chunk_scan_kernel<<<1, 1024, 0, s>>>(idx, T, k, E, chunk_counts, chunk_base, counts,
+                                         offsets);
     return cudaGetLastError();
 }
 
@@ -123,7 +178,17 @@ cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int
                                 int *inv, void *x_perm, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const int nchunks = (T + kChunk - 1) / kChunk;
-    group_tokens_kernel<<<nchunks, 256, 0, s>>>(
+    // few chunks (small batches): split each chunk's row copy over several
+    // blocks so enough loads are in flight
+    int parts = 1;
+    if (x != nullptr) {
+        const int rowvec = (int)((size_t)d * elt / 16);
+        parts = (2 * kPlanSms + nchunks - 1) / nchunks;
+        if (parts > 8) parts = 8;
+        if (parts > rowvec) parts = rowvec > 0 ? rowvec : 1;
+        if (parts < 1) parts = 1;
+    }
+    group_tokens_kernel<<<dim3(nchunks, parts), 256, 0, s>>>(
         idx, chunk_base, offsets, static_cast<const uint8_t *>(x), T, E, k, (size_t)d * elt, perm,
         inv, static_cast<uint8_t *>(x_perm));
     return cudaGetLastError();

@@ -1,11 +1,13 @@
 // Router: logits = x . W_g (fp32 accumulation), top-k selection (k <= 2,
 // ties to the lower expert index) and the softmax over the kept logits
-// ("Mixtral of Experts" (azimuth.plus), router paragraph).  Also counts, per
-// chunk of kChunk tokens, how many rows each expert receives; the grouping
-// pass turns those counts into row positions.
+// ("Mixtral of Experts" (azimuth.plus), router paragraph).
 //
-// HBM-bound: it reads x once (T*d elements) and W_g from L1/L2.  One warp
-// handles two tokens at a time so each W_g vector fetched is used twice.
+// One block handles two tokens.  Its 256 threads split the hidden dimension:
+// each thread takes 16-byte slices of both token rows and the same slices of
+// every expert's router row, issues all of those loads before any arithmetic
+// (one memory round trip when d <= 256 slices per thread pass), then the block
+// reduces the per-thread partial sums in a fixed order.  HBM traffic is x
+// once; the 64 KB router matrix is served from L1/L2.
 #include "internal.h"
 
 namespace moe {
@@ -37,16 +39,17 @@ template <> struct Vec<float> {
     __device__ static void unpack(const uint4 &v, float (&f)[4]) { unpack4f(v, f); }
 };
 
-// Finish one token: bias, top-k, gates, outputs, chunk count.
+constexpr int kRouterThreads = 256;
+constexpr int kRouterTokens = 2;
+
+// Bias, selection, gates and outputs for one token, from its E logits.
 template <int EMAX>
-__device__ __forceinline__ void finish_token(const float (&acc)[EMAX], const float *bias, int t,
-                                             int E, int k, float *logits, int *idx, float *gates,
-                                             int *s_cnt) {
-    float l[EMAX];
+__device__ __forceinline__ void finish_token(float (&l)[EMAX], const float *bias, int t, int E,
+                                             int k, float *logits, int *idx, float *gates) {
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) {
         if (e < E) {
-            l[e] = acc[e] + (bias != nullptr ? bias[e] : 0.f);
+            l[e] += (bias != nullptr ? bias[e] : 0.f);
             logits[(size_t)t * E + e] = l[e];
         }
     }
@@ -56,54 +59,65 @@ __device__ __forceinline__ void finish_token(const float (&acc)[EMAX], const flo
     for (int j = 0; j < k; ++j) {
         idx[(size_t)t * k + j] = sel[j];
         gates[(size_t)t * k + j] = g[j];
-        atomicAdd(&s_cnt[sel[j]], 1);
     }
 }
 
-// One block = one chunk of kChunk tokens: 8 warps x 2 tokens.
-template <typename T, int EMAX>
-__global__ void __launch_bounds__(256) router_kernel(const T *__restrict__ x,
-                                                     const T *__restrict__ Wg,
-                                                     const float *__restrict__ bias, int Tn,
-                                                     int d, int E, int k, float *logits, int *idx,
-                                                     float *gates, int *chunk_counts) {
+// V: 16-byte slices per thread per pass (all loads of a pass are in flight
+// together).  Rows of experts >= E are clamped to a valid row and their sums
+// ignored, which keeps the loads free of branches.
+template <typename T, int EMAX, int V>
+__global__ void __launch_bounds__(kRouterThreads) router_kernel(
+    const T *__restrict__ x, const T *__restrict__ Wg, const float *__restrict__ bias, int Tn,
+    int d, int E, int k, float *logits, int *idx, float *gates) {
     constexpr int VN = Vec<T>::n;
-    __shared__ int s_cnt[EMAX];
-    if (threadIdx.x < EMAX) s_cnt[threadIdx.x] = 0;
-    __syncthreads();
+    constexpr int NW = kRouterThreads / 32;
+    __shared__ float s_part[NW][kRouterTokens][EMAX];
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t0 = blockIdx.x * kChunk + warp * 2;
-    const bool has0 = t0 < Tn, has1 = t0 + 1 < Tn;
+    const int t0 = blockIdx.x * kRouterTokens;
+    const bool has1 = t0 + 1 < Tn;
+    const int nvec = d / VN;
+    const uint4 *xr0 = reinterpret_cast<const uint4 *>(x + (size_t)t0 * d);
+    const uint4 *xr1 = reinterpret_cast<const uint4 *>(x + (size_t)(has1 ? t0 + 1 : t0) * d);
+    const uint4 *wr[EMAX];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e)
+        wr[e] = reinterpret_cast<const uint4 *>(Wg + (size_t)(e < E ? e : E - 1) * d);
+
     float acc0[EMAX], acc1[EMAX];
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) acc0[e] = acc1[e] = 0.f;
-
-    const int nvec = d / VN;
-    const uint4 *xr0 = reinterpret_cast<const uint4 *>(x + (size_t)t0 * d);
-    const uint4 *xr1 = reinterpret_cast<const uint4 *>(x + (size_t)(t0 + 1) * d);
     const uint4 zero = make_uint4(0, 0, 0, 0);
-    if (has0) {
-#pragma unroll 2
-        for (int v = lane; v < nvec; v += 32) {
+    for (int v0 = threadIdx.x; v0 < nvec; v0 += kRouterThreads * V) {
+        uint4 xa[V], xb[V], w[V][EMAX];
+#pragma unroll
+        for (int u = 0; u < V; ++u) {
+            const int v = v0 + kRouterThreads * u;
+            const int vv = v < nvec ? v : 0;
+            xa[u] = __ldcs(xr0 + vv);
+            xb[u] = __ldcs(xr1 + vv);
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e) w[u][e] = __ldg(wr[e] + vv);
+            if (v >= nvec) xa[u] = xb[u] = zero;
+        }
+#pragma unroll
+        for (int u = 0; u < V; ++u) {
             float a[VN], b[VN];
-            Vec<T>::unpack(__ldcs(xr0 + v), a);
-            Vec<T>::unpack(has1 ? __ldcs(xr1 + v) : zero, b);
+            Vec<T>::unpack(xa[u], a);
+            Vec<T>::unpack(xb[u], b);
 #pragma unroll
             for (int e = 0; e < EMAX; ++e) {
-                if (e < E) {
-                    float w[VN];
-                    Vec<T>::unpack(__ldg(reinterpret_cast<const uint4 *>(Wg + (size_t)e * d) + v),
-                                   w);
+                float wf[VN];
+                Vec<T>::unpack(w[u][e], wf);
 #pragma unroll
-                    for (int i = 0; i < VN; ++i) {
-                        acc0[e] = fmaf(a[i], w[i], acc0[e]);
-                        acc1[e] = fmaf(b[i], w[i], acc1[e]);
-                    }
+                for (int i = 0; i < VN; ++i) {
+                    acc0[e] = fmaf(a[i], wf[i], acc0[e]);
+                    acc1[e] = fmaf(b[i], wf[i], acc1[e]);
                 }
             }
         }
     }
+    // block reduction: butterfly within each warp, then warps in order
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) {
 #pragma unroll
@@ -112,84 +126,85 @@ __global__ void __launch_bounds__(256) router_kernel(const T *__restrict__ x,
             acc1[e] += __shfl_xor_sync(0xffffffffu, acc1[e], off);
         }
     }
-    if (lane == 0 && has0) finish_token<EMAX>(acc0, bias, t0, E, k, logits, idx, gates, s_cnt);
-    if (lane == 1 && has1) finish_token<EMAX>(acc1, bias, t0 + 1, E, k, logits, idx, gates, s_cnt);
-    __syncthreads();
-    if (chunk_counts != nullptr && threadIdx.x < E)
-        chunk_counts[(size_t)blockIdx.x * E + threadIdx.x] = s_cnt[threadIdx.x];
-}
-
-// Selection from given logits: one thread per token, 128 tokens (8 chunks)
-// per block.
-template <int EMAX>
-__global__ void __launch_bounds__(128) topk_kernel(const float *__restrict__ logits, int Tn, int E,
-                                                   int k, int *idx, float *gates,
-                                                   int *chunk_counts, int nchunks) {
-    constexpr int CPB = 128 / kChunk;
-    __shared__ int s_cnt[CPB][EMAX];
-    for (int i = threadIdx.x; i < CPB * EMAX; i += blockDim.x) (&s_cnt[0][0])[i] = 0;
-    __syncthreads();
-    const int t = blockIdx.x * 128 + threadIdx.x;
-    if (t < Tn) {
-        float l[EMAX];
+    if (lane == 0) {
 #pragma unroll
-        for (int e = 0; e < EMAX; ++e)
-            if (e < E) l[e] = logits[(size_t)t * E + e];
-        int sel[2];
-        float g[2];
-        top2_gates(l, E, k, sel, g);
-        for (int j = 0; j < k; ++j) {
-            idx[(size_t)t * k + j] = sel[j];
-            gates[(size_t)t * k + j] = g[j];
-            atomicAdd(&s_cnt[threadIdx.x / kChunk][sel[j]], 1);
+        for (int e = 0; e < EMAX; ++e) {
+            s_part[warp][0][e] = acc0[e];
+            s_part[warp][1][e] = acc1[e];
         }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < CPB * E; i += blockDim.x) {
-        const int c = blockIdx.x * CPB + i / E;
-        if (c < nchunks) chunk_counts[(size_t)c * E + i % E] = s_cnt[i / E][i % E];
+    if (threadIdx.x < kRouterTokens && (threadIdx.x == 0 || has1)) {
+        const int j = threadIdx.x;
+        float l[EMAX];
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+            float s = s_part[0][j][e];
+#pragma unroll
+            for (int w2 = 1; w2 < NW; ++w2) s += s_part[w2][j][e];
+            l[e] = s;
+        }
+        finish_token<EMAX>(l, bias, t0 + j, E, k, logits, idx, gates);
+    }
+}
+
+// Selection from given logits: one thread per token.
+template <int EMAX>
+__global__ void __launch_bounds__(128) topk_kernel(const float *__restrict__ logits, int Tn, int E,
+                                                   int k, int *idx, float *gates) {
+    const int t = blockIdx.x * 128 + threadIdx.x;
+    if (t >= Tn) return;
+    float l[EMAX];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) l[e] = e < E ? logits[(size_t)t * E + e] : 0.f;
+    int sel[2];
+    float g[2];
+    top2_gates(l, E, k, sel, g);
+    for (int j = 0; j < k; ++j) {
+        idx[(size_t)t * k + j] = sel[j];
+        gates[(size_t)t * k + j] = g[j];
     }
 }
 
 template <typename T>
 cudaError_t router_dispatch(const void *x, const void *Wg, const float *bias, int T_, int d,
-                            int E, int k, float *logits, int *idx, float *gates, int *cc,
-                            cudaStream_t s) {
-    const int nchunks = (T_ + kChunk - 1) / kChunk;
+                            int E, int k, float *logits, int *idx, float *gates, cudaStream_t s) {
+    const int grid = (T_ + kRouterTokens - 1) / kRouterTokens;
     const T *xp = static_cast<const T *>(x);
     const T *wp = static_cast<const T *>(Wg);
+    // 16-byte loads in flight per thread per pass: V * (2 + EMAX)
     if (E <= 8)
-        router_kernel<T, 8><<<nchunks, 256, 0, s>>>(xp, wp, bias, T_, d, E, k, logits, idx, gates, cc);
+        router_kernel<T, 8, 2><<<grid, kRouterThreads, 0, s>>>(xp, wp, bias, T_, d, E, k, logits,
+                                                               idx, gates);
     else if (E <= 16)
-        router_kernel<T, 16><<<nchunks, 256, 0, s>>>(xp, wp, bias, T_, d, E, k, logits, idx, gates, cc);
+        router_kernel<T, 16, 1><<<grid, kRouterThreads, 0, s>>>(xp, wp, bias, T_, d, E, k,
+                                                                logits, idx, gates);
     else
-        router_kernel<T, 32><<<nchunks, 256, 0, s>>>(xp, wp, bias, T_, d, E, k, logits, idx, gates, cc);
+        router_kernel<T, 32, 1><<<grid, kRouterThreads, 0, s>>>(xp, wp, bias, T_, d, E, k,
+                                                                logits, idx, gates);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_router(const void *x, const void *Wg, const float *bias, int T, int d, int E,
-                          int k, int dt, float *logits, int *idx, float *gates, int *chunk_counts,
-                          cudaStream_t s) {
+                          int k, int dt, float *logits, int *idx, float *gates, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (dt == MOE_BF16)
-        return router_dispatch<__nv_bfloat16>(x, Wg, bias, T, d, E, k, logits, idx, gates,
-                                              chunk_counts, s);
-    return router_dispatch<float>(x, Wg, bias, T, d, E, k, logits, idx, gates, chunk_counts, s);
+        return router_dispatch<__nv_bfloat16>(x, Wg, bias, T, d, E, k, logits, idx, gates, s);
+    return router_dispatch<float>(x, Wg, bias, T, d, E, k, logits, idx, gates, s);
 }
 
 cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, int *idx,
-                                    float *gates, int *chunk_counts, cudaStream_t s) {
+                                    float *gates, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    const int nchunks = (T + kChunk - 1) / kChunk;
     const int grid = (T + 127) / 128;
     if (E <= 8)
-        topk_kernel<8><<<grid, 128, 0, s>>>(logits, T, E, k, idx, gates, chunk_counts, nchunks);
+        topk_kernel<8><<<grid, 128, 0, s>>>(logits, T, E, k, idx, gates);
     else if (E <= 16)
-        topk_kernel<16><<<grid, 128, 0, s>>>(logits, T, E, k, idx, gates, chunk_counts, nchunks);
+        topk_kernel<16><<<grid, 128, 0, s>>>(logits, T, E, k, idx, gates);
     else
-        topk_kernel<32><<<grid, 128, 0, s>>>(logits, T, E, k, idx, gates, chunk_counts, nchunks);
+        topk_kernel<32><<<grid, 128, 0, s>>>(logits, T, E, k, idx, gates);
     return cudaGetLastError();
 }
 
