@@ -72,6 +72,37 @@ def rank_token_seed(base_seed: int, rank: int) -> int:
 
 # ---------------------------------------------------------------- peaks, clocks
 
+GEMM_SOURCES = ("sparse_mixture_experts_58_b300/csrc/gemm_tc.cu",
+                "sparse_mixture_experts_58_b300/csrc/ptx.cuh",
+                "sparse_mixture_experts_58_b300/csrc/common.cuh")
+
+
+def gemm_source_hash() -> str:
+    """Hash of the tensor-core GEMM's device sources (ties recorded ncu
+    counters to the kernel they were taken on)."""
+    import hashlib
+    h = hashlib.sha256()
+    for p in GEMM_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(key: str):
+    """DRAM bytes (read + write) per launch from the committed ncu summary,
+    or None when absent or taken on a different kernel source."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = d.get(key)
+    if not ent or ent.get("source_hash") != gemm_source_hash():
+        return None
+    return ent.get("bytes_per_launch")
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -147,7 +178,9 @@ class ClockSampler:
             time.sleep(self.period)
 
     def start(self):
+        """Start (or resume) sampling; samples accumulate across start/stop."""
         if self.ok:
+            self._stop.clear()
             self._t = threading.Thread(target=self._run, daemon=True)
             self._t.start()
 
@@ -155,6 +188,7 @@ class ClockSampler:
         if self._t is not None:
             self._stop.set()
             self._t.join()
+            self._t = None
 
     def summary(self):
         if not self.ok:
@@ -278,7 +312,12 @@ def measure(args, rank, world, local):
     dev = torch.device("cuda", local)
     dist_init(world, "nccl")
     cfg = dict(inputs.WORKLOADS[args.config])
+    if args.T:
+        cfg["T"] = args.T
     T, d, ffn, E, k = cfg["T"], cfg["d"], cfg["ffn"], cfg["E"], cfg["k"]
+    workload = WORKLOAD_NAMES[args.config]
+    if args.T:
+        workload = f"{workload} (T overridden to {T})"
 
     # weights shared by every rank; tokens per rank
     gen = inputs.generator(cfg["seed"], dev)
@@ -416,7 +455,7 @@ def measure(args, rank, world, local):
         "dtype": "bf16",
         "data": "synthetic: seeded x~N(0,1), weights~N(0,1/fan_in), random init",
         "config": {
-            "workload": WORKLOAD_NAMES[args.config], "T": T, "d": d, "ffn": ffn, "E": E, "k": k,
+            "workload": workload, "T": T, "d": d, "ffn": ffn, "E": E, "k": k,
             "tokens_per_gpu": T, "parallelism": f"replicas x{world} (no data-path collective)",
             "l2": "no flush: each step streams the touched experts' weights "
                   f"({n_touched * 3 * d * ffn * 2 / 1e9:.2f} GB) > 126 MB L2",
@@ -426,7 +465,10 @@ def measure(args, rank, world, local):
             "kernel": "grouped gate/up GEMM + SwiGLU (tcgen05)",
             "bound": g_bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "peak_source": f"{peak_src} (burst)",
-            "traffic": None,
+            "traffic": recorded_traffic(f"gate_up_{args.config}"),
+            "traffic_source": "profiles/ncu_traffic.json (dram__bytes_read.sum + "
+                              "dram__bytes_write.sum, one ncu capture; null if the kernel "
+                              "source changed since)",
             "algorithmic_per_launch": {"bytes": g_bytes, "flops": g_flops},
             "launch_us": t_g * 1e6,
         },
@@ -453,13 +495,122 @@ def measure(args, rank, world, local):
     return 0
 
 
+def measure_sweep(args, rank, world, local):
+    """Token-count sweep: for each T, the 32-layer chain
+    x <- x + MoE_l(RMSNorm(x)) with independent layer weights (90 GB resident),
+    captured as one CUDA graph and replayed; reports per-T chain time, per-layer
+    time and the fraction of the per-layer roofline."""
+    import torch
+
+    from sparse_mixture_experts_58_b300 import inputs, moe
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    cfg = inputs.WORKLOADS["sweep"]
+    d, ffn, E, k, L = cfg["d"], cfg["ffn"], cfg["E"], cfg["k"], cfg["layers"]
+    Ts = [int(t) for t in args.sweep_T.split(",")] if args.sweep_T else list(cfg["Ts"])
+    layers = [inputs.sweep_layer(l, d, ffn, E, device=dev, seed0=cfg["layer_seed0"])
+              for l in range(L)]
+    peaks, peak_src = load_peaks()
+    ws = moe.Workspace(dev)
+    stream = torch.cuda.current_stream()
+    results = []
+    clocks = ClockSampler(local)
+    tot_tokens, tot_time = 0, 0.0
+    for T in Ts:
+        x0 = inputs.sweep_tokens(T, d, device=dev, seed=rank_token_seed(cfg["seed"], rank))
+        x, xn, out = x0.clone(), torch.empty_like(x0), torch.empty_like(x0)
+        ws.get(moe.workspace_bytes(T, d, ffn, E, k, moe.BF16))
+
+        def chain():
+            x.copy_(x0)
+            moe.add_rmsnorm(x, None, xn)
+            for layer in layers:
+                moe.forward(xn, layer.Wg, layer.W1, layer.W3, layer.W2, k, out=out, workspace=ws)
+                moe.add_rmsnorm(x, out, xn)
+
+        # experts touched per layer on this batch (for the byte roofline)
+        chain()
+        torch.cuda.synchronize()
+        x.copy_(x0)
+        moe.add_rmsnorm(x, None, xn)
+        touched = []
+        for layer in layers:
+            _, idx, _ = moe.router(xn, layer.Wg, k)
+            touched.append(int((torch.bincount(idx.flatten().long(), minlength=E) > 0).sum()))
+            moe.forward(xn, layer.Wg, layer.W1, layer.W3, layer.W2, k, out=out, workspace=ws)
+            moe.add_rmsnorm(x, out, xn)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            chain()
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        g.replay()
+        torch.cuda.synchronize()
+        est = time.perf_counter() - t0
+        reps = max(3, min(args.steps, int(0.5 / max(est, 1e-6))))
+        barrier(world)
+        clocks.start()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        clocks.stop()
+        barrier(world)
+        t_chain = reduce_max(e0.elapsed_time(e1) / 1e3 / reps, world, dev)
+        if moe.device_status(clear=True) != 0:
+            raise RuntimeError("device status set during the sweep")
+        roof = 0.0
+        for n in touched:
+            f, b = algorithmic(T, d, ffn, E, k, n)
+            b += 3 * T * d * 2                 # RMSNorm/residual pass per layer
+            roof += max(b / (peaks["hbm_gbs"] * 1e9), f / (peaks["bf16_tflops"] * 1e12))
+        results.append({"T": T, "chain_ms": t_chain * 1e3, "layer_us": t_chain / L * 1e6,
+                        "tokens_per_s_32_layers": T * world / t_chain,
+                        "roofline_chain_ms": roof * 1e3, "frac": roof / t_chain,
+                        "experts_touched_min": min(touched), "reps": reps})
+        tot_tokens += T * world
+        tot_time += t_chain
+        del g
+    if rank != 0:
+        return 0
+    last = results[-1]
+    line = {
+        "metric": METRIC + " [32-layer token-count sweep]",
+        "value": last["tokens_per_s_32_layers"], "unit": "tokens/s (32-layer chain)",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": last["chain_ms"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded x~N(0,1), weights~N(0,1/fan_in), random init",
+        "config": {"workload": "token-count sweep: T in " + ",".join(map(str, Ts)) +
+                   ", 32 layers with independent weights, x <- x + MoE(RMSNorm(x)), "
+                   "d=4096, ffn=14336, E=8, top-2, bf16",
+                   "l2": "no flush: 90 GB of layer weights stream per chain"},
+        "sweep": results,
+        "peaks": {"source": peak_src, **peaks},
+        "gpu_launches": (2 + L * (moe.forward_launches(16, d, ffn, E, k, moe.BF16) + 1)),
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=sorted(WORKLOAD_NAMES), default="decode")
+    ap.add_argument("--config", choices=sorted(WORKLOAD_NAMES) + ["sweep"], default="decode")
+    ap.add_argument("--sweep-T", default="", help="comma-separated token counts for --config sweep")
+    ap.add_argument("--T", type=int, default=0, help="override the workload's token count")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="time direct moe_forward calls instead of a captured CUDA graph")
@@ -468,7 +619,11 @@ def main(argv=None):
         args.warmup = 3
     rank, world, local = dist_env()
     if args.impl == "reference":
+        if args.config == "sweep":
+            args.config = "decode"
         return run_reference(args, rank, world)
+    if args.config == "sweep":
+        return measure_sweep(args, rank, world, local)
     return measure(args, rank, world, local)
 
 

@@ -217,6 +217,10 @@ int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p) {
         if (s > smax) s = smax;
         if (s < 1) s = 1;
         if (q.wide) s = 1;
+        // tuning overrides (measurement only): MOE_PLAN_WIDE=0|1, MOE_PLAN_SPLITS=n
+        if (const char *w = getenv("MOE_PLAN_WIDE")) q.wide = atoi(w) != 0;
+        if (const char *sp = getenv("MOE_PLAN_SPLITS")) s = atoi(sp) > 0 ? atoi(sp) : s;
+        if (s > kblocks) s = kblocks;
         q.kps = (kblocks + (int)s - 1) / (int)s;
         q.splits = (kblocks + q.kps - 1) / q.kps;
     }

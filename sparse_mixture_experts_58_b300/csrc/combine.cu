@@ -36,20 +36,19 @@ __device__ __forceinline__ void add4(float4 &s, const float4 &p) {
     s.w += p.w;
 }
 
-// Block (t, c): token t, columns [1024 c, 1024 c + 1024); one thread per four
-// columns.  Up to kSplitBatch partial sums per slot are loaded together, then
-// added in split order, so a thread waits for one round trip per batch.
-constexpr int kSplitBatch = 8;
-
-template <typename T>
+// Block (t, c): token t, columns [4 * C * 256 c, ...): each thread owns C
+// groups of four columns, 256 groups apart.  For each slot, up to SB split
+// partials of all C groups are loaded together, then added in split order, so
+// a thread has 2 * C * SB loads in flight per round trip.
+template <typename T, int C, int SB>
 __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ y, int splits,
                                                       int rows, const float *__restrict__ gates,
                                                       const int *__restrict__ inv, int Tn, int d,
                                                       int k, T *out) {
     const int t = blockIdx.x;
-    const int v = blockIdx.y * 256 + threadIdx.x;  // float4 column group
-    if (v >= d / 4) return;
-    const size_t stride4 = (size_t)rows * d / 4;   // one split, in float4
+    const int nv = d / 4;
+    const int v0 = blockIdx.y * 256 * C + threadIdx.x;  // first float4 column group
+    const size_t stride4 = (size_t)rows * nv;            // one split, in float4
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
     int rowj[2] = {0, 0};
     float gj[2] = {0.f, 0.f};
@@ -60,42 +59,58 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
             gj[j] = gates[(size_t)t * k + j];
         }
     }
-    float4 s[2] = {zero, zero};
-    for (int q0 = 0; q0 < splits; q0 += kSplitBatch) {
-        float4 p[2][kSplitBatch];
+    float4 s[2][C];
+    for (int q0 = 0; q0 < splits; q0 += SB) {
+        float4 p[2][C][SB];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const float4 *src = reinterpret_cast<const float4 *>(y) + (size_t)rowj[j] * (d / 4) + v;
+            const float4 *src = reinterpret_cast<const float4 *>(y) + (size_t)rowj[j] * nv;
 #pragma unroll
-            for (int i = 0; i < kSplitBatch; ++i)
-                p[j][i] = (j < k && q0 + i < splits) ? __ldcs(src + (size_t)(q0 + i) * stride4)
-                                                     : zero;
+            for (int c = 0; c < C; ++c) {
+                const int v = v0 + 256 * c;
+#pragma unroll
+                for (int i = 0; i < SB; ++i)
+                    p[j][c][i] = (j < k && v < nv && q0 + i < splits)
+                                     ? __ldcs(src + (size_t)(q0 + i) * stride4 + v)
+                                     : zero;
+            }
         }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            if (q0 == 0) {
-                s[j] = p[j][0];
 #pragma unroll
-                for (int i = 1; i < kSplitBatch; ++i)
-                    if (q0 + i < splits) add4(s[j], p[j][i]);
-            } else {
+            for (int c = 0; c < C; ++c) {
+                if (q0 == 0) s[j][c] = p[j][c][0];
+                else add4(s[j][c], p[j][c][0]);
 #pragma unroll
-                for (int i = 0; i < kSplitBatch; ++i)
-                    if (q0 + i < splits) add4(s[j], p[j][i]);
+                for (int i = 1; i < SB; ++i)
+                    if (q0 + i < splits) add4(s[j][c], p[j][c][i]);
             }
         }
     }
-    float4 acc = zero;
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        if (j < k) {
-            acc.x = fmaf(gj[j], s[j].x, acc.x);
-            acc.y = fmaf(gj[j], s[j].y, acc.y);
-            acc.z = fmaf(gj[j], s[j].z, acc.z);
-            acc.w = fmaf(gj[j], s[j].w, acc.w);
+    for (int c = 0; c < C; ++c) {
+        const int v = v0 + 256 * c;
+        if (v >= nv) continue;
+        float4 acc = zero;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            if (j < k) {
+                acc.x = fmaf(gj[j], s[j][c].x, acc.x);
+                acc.y = fmaf(gj[j], s[j][c].y, acc.y);
+                acc.z = fmaf(gj[j], s[j][c].z, acc.z);
+                acc.w = fmaf(gj[j], s[j][c].w, acc.w);
+            }
         }
+        store4<T>(out + (size_t)t * d + 4 * v, acc);
     }
-    store4<T>(out + (size_t)t * d + 4 * v, acc);
+}
+
+template <typename T, int C, int SB>
+void launch_combine_t(const float *y, int splits, int rows, const float *gates, const int *inv,
+                      int T_, int d, int k, void *out, cudaStream_t s) {
+    const dim3 grid(T_, (d / 4 + 256 * C - 1) / (256 * C));
+    combine_kernel<T, C, SB><<<grid, 256, 0, s>>>(y, splits, rows, gates, inv, T_, d, k,
+                                                  static_cast<T *>(out));
 }
 
 // One block per row: optional residual add (rounded to the storage type),
@@ -144,13 +159,19 @@ cudaError_t launch_combine(const float *y, int splits, int rows, const float *ga
                            const int *inv, int T, int d, int k, int dt, void *out,
                            cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    const dim3 grid(T, (d / 4 + 255) / 256);
-    if (dt == MOE_BF16)
-        combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(y, splits, rows, gates, inv, T, d, k,
-                                                           static_cast<__nv_bfloat16 *>(out));
-    else
-        combine_kernel<float><<<grid, 256, 0, s>>>(y, splits, rows, gates, inv, T, d, k,
-                                                   static_cast<float *>(out));
+    // unsplit partials (large batches): 4 column groups per thread, one load
+    // per slot each; split partials (small batches): 1 group, 8 splits a batch
+    if (dt == MOE_BF16) {
+        if (splits == 1)
+            launch_combine_t<__nv_bfloat16, 4, 1>(y, splits, rows, gates, inv, T, d, k, out, s);
+        else
+            launch_combine_t<__nv_bfloat16, 1, 8>(y, splits, rows, gates, inv, T, d, k, out, s);
+    } else {
+        if (splits == 1)
+            launch_combine_t<float, 4, 1>(y, splits, rows, gates, inv, T, d, k, out, s);
+        else
+            launch_combine_t<float, 1, 8>(y, splits, rows, gates, inv, T, d, k, out, s);
+    }
     return cudaGetLastError();
 }
 
