@@ -49,11 +49,16 @@ def _declare(lib):
         c_int, c_int, c_int, c_int, c_int, c_int,
         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int]
     lib.oracle_moe_forward.restype = c_int
+    lib.oracle_moe_forward_ex.argtypes = [
+        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+        c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int]
+    lib.oracle_moe_forward_ex.restype = c_int
     lib.oracle_router.argtypes = [c_void_p, c_void_p, c_void_p, c_int, c_int,
-                                  c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]
+                                  c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]
     lib.oracle_router.restype = c_int
-    lib.oracle_route.argtypes = [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p,
-                                 c_void_p, c_void_p, c_void_p, c_void_p]
+    lib.oracle_route.argtypes = [c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p,
+                                 c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
     lib.oracle_route.restype = c_int
     lib.oracle_rmsnorm.argtypes = [c_void_p, c_int, c_int, ctypes.c_double, c_int, c_void_p]
     lib.oracle_rmsnorm.restype = c_int
@@ -105,10 +110,15 @@ class Oracle:
     def max_threads(self) -> int:
         return self.lib.oracle_max_threads()
 
-    def moe_forward(self, x, Wg, W1, W3, W2, k, bias=None, threads=0, exact=False):
+    def moe_forward(self, x, Wg, W1, W3, W2, k, bias=None, threads=0, exact=False,
+                    gating=0, capacity=0, drop_renorm=0):
         """Whole layer.  Returns (out, logits fp32 [T,E], idx int32 [T,k],
-        gates float64 [T,k]); ``out`` has x's element type.  With
-        ``exact=True`` a fifth item is the float64 result before rounding."""
+        gates float64 [T,k] before any drop); ``out`` has x's element type.
+        With ``exact=True`` a fifth item is the float64 result before
+        rounding.  gating 0: softmax over the kept logits; 1: softmax over all
+        logits, kept ones not renormalised.  capacity: selections each expert
+        keeps, in token order (0: all); drop_renorm: dropped slots' gate mass
+        lost (0) or spread over the token's kept slots (1)."""
         x = np.ascontiguousarray(x)
         dt = _dt_code(x)
         T, d = x.shape
@@ -134,16 +144,17 @@ class Oracle:
         idx = np.empty((T, k), np.int32)
         gates = np.empty((T, k), np.float64)
         ex = np.empty((T, d), np.float64) if exact else None
-        rc = self.lib.oracle_moe_forward(
-            _ptr(x), _ptr(Wg), _ptr(b), p1, p3, p2, T, d, ffn, E, k, dt,
-            _ptr(out), _ptr(logits), _ptr(idx), _ptr(gates), _ptr(ex), int(threads))
+        rc = self.lib.oracle_moe_forward_ex(
+            _ptr(x), _ptr(Wg), _ptr(b), p1, p3, p2, T, d, ffn, E, k, dt, int(gating),
+            int(capacity), int(drop_renorm), _ptr(out), _ptr(logits), _ptr(idx), _ptr(gates),
+            _ptr(ex), int(threads))
         if rc != 0:
             raise RuntimeError(f"oracle_moe_forward failed: {rc}")
         if exact:
             return out, logits, idx, gates, ex
         return out, logits, idx, gates
 
-    def router(self, x, Wg, k, bias=None):
+    def router(self, x, Wg, k, bias=None, gating=0):
         x = np.ascontiguousarray(x)
         dt = _dt_code(x)
         T, d = x.shape
@@ -154,27 +165,30 @@ class Oracle:
         logits = np.empty((T, E), np.float32)
         idx = np.empty((T, k), np.int32)
         gates = np.empty((T, k), np.float64)
-        rc = self.lib.oracle_router(_ptr(x), _ptr(Wg), _ptr(b), T, d, E, k, dt,
+        rc = self.lib.oracle_router(_ptr(x), _ptr(Wg), _ptr(b), T, d, E, k, dt, int(gating),
                                     _ptr(logits), _ptr(idx), _ptr(gates))
         if rc != 0:
             raise RuntimeError(f"oracle_router failed: {rc}")
         return logits, idx, gates
 
-    def route(self, logits, k):
-        """Grouping from given fp32 logits: (idx, gates, counts, offsets, perm, inv)."""
+    def route(self, logits, k, gating=0, capacity=0):
+        """Grouping from given fp32 logits: (idx, gates, counts, offsets, perm,
+        inv); with a capacity, only kept selections get rows (perm holds
+        offsets[E] valid entries, inv is -1 for dropped ones)."""
         logits = np.ascontiguousarray(logits, dtype=np.float32)
         T, E = logits.shape
         idx = np.empty((T, k), np.int32)
         gates = np.empty((T, k), np.float64)
         counts = np.empty(E, np.int32)
         offsets = np.empty(E + 1, np.int32)
-        perm = np.empty(T * k, np.int32)
+        perm = np.full(T * k, -1, np.int32)
         inv = np.empty(T * k, np.int32)
-        rc = self.lib.oracle_route(_ptr(logits), T, E, k, _ptr(idx), _ptr(gates),
-                                   _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv))
+        rc = self.lib.oracle_route(_ptr(logits), T, E, k, int(gating), int(capacity), _ptr(idx),
+                                   _ptr(gates), _ptr(counts), _ptr(offsets), _ptr(perm),
+                                   _ptr(inv))
         if rc != 0:
             raise RuntimeError(f"oracle_route failed: {rc}")
-        return idx, gates, counts, offsets, perm, inv
+        return idx, gates, counts, offsets, perm[:int(offsets[-1])], inv
 
     def rmsnorm(self, x, eps=1e-5):
         x = np.ascontiguousarray(x)

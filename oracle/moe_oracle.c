@@ -34,7 +34,11 @@
  *     construct added to the logits before selection;
  *   - router logits are stored as fp32 (one rounding of the exact sum);
  *   - the layer output is rounded once, to nearest-even, after the weighted sum;
- *   - RMSNorm (for the stacked-layer harness) uses gain 1.
+ *   - RMSNorm (for the stacked-layer harness) uses gain 1;
+ *   - variants: gating 1 = softmax over all experts then top-k without
+ *     renormalising; a per-expert capacity keeps each expert's first
+ *     `capacity` selections in token order, and a dropped slot's gate mass is
+ *     either lost or spread proportionally over the token's kept slots.
  *
  * Layouts (row-major, the same as the library's):
  *   x    [T][d]        W_g  [E][d]
@@ -152,16 +156,30 @@ static void select_top_k(const float *l, int E, int k, int *chosen)
     }
 }
 
-/* Softmax over the kept logits only (every other score is -inf, so it
- * contributes exp(-inf) = 0).  The largest kept logit is subtracted first. */
-static void gates_of(const float *l, const int *chosen, int k, double *g)
+/* Gating modes.
+ *   0: keep the top k scores, set the others to -inf, softmax over what
+ *      survives ("Mixtral of Experts" (azimuth.plus), router paragraph);
+ *   1: softmax over all E scores, then keep the top k, without renormalising
+ *      the kept probabilities (a reading of "Mixtral & Sparse MoE (2024) > The
+ *      Solution", routing paragraph: scores normalised by a softmax, top-2
+ *      selected, outputs combined by their routing scores).
+ * The largest logit (chosen[0]) is subtracted before exponentiating. */
+static void gates_of(const float *l, const int *chosen, int E, int k, int gating, double *g)
 {
     double l0 = (double)l[chosen[0]];
-    double z = 0.0;
-    for (int j = 0; j < k; ++j)
-        z += exp((double)l[chosen[j]] - l0);
-    for (int j = 0; j < k; ++j)
-        g[j] = exp((double)l[chosen[j]] - l0) / z;
+    if (gating == 0) {
+        double z = 0.0;
+        for (int j = 0; j < k; ++j)
+            z += exp((double)l[chosen[j]] - l0);
+        for (int j = 0; j < k; ++j)
+            g[j] = exp((double)l[chosen[j]] - l0) / z;
+    } else {
+        double zall = 0.0;
+        for (int e = 0; e < E; ++e)
+            zall += exp((double)l[e] - l0);
+        for (int j = 0; j < k; ++j)
+            g[j] = exp((double)l[chosen[j]] - l0) / zall;
+    }
 }
 
 static int all_finite_f32(const float *p, size_t n)
@@ -172,23 +190,65 @@ static int all_finite_f32(const float *p, size_t n)
     return 1;
 }
 
+/* Capacity ("Mixtral & Sparse MoE (2024) > The Solution", load-balancing
+ * paragraph: a limit on how many tokens each expert takes).  Reading: an
+ * expert keeps its first `capacity` (token, slot) selections in token order
+ * and drops the rest; capacity <= 0 keeps everything. */
+static void keep_flags(const int *idx, int T, int E, int k, int capacity, unsigned char *kept)
+{
+    int *taken = (int *)calloc((size_t)E, sizeof(int));
+    for (int t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            int e = idx[(size_t)t * k + j];
+            kept[(size_t)t * k + j] = (unsigned char)(capacity <= 0 || taken[e] < capacity);
+            taken[e] += 1;
+        }
+    free(taken);
+}
+
+/* Gate actually applied to each slot.  A dropped slot contributes nothing.
+ * drop_renorm = 0: its gate mass is lost; 1: the token's kept gates are
+ * scaled so they sum to the token's total gate mass (all slots dropped:
+ * every gate is 0). */
+static void applied_gates(const double *g0, const unsigned char *kept, int k, int drop_renorm,
+                          double *g)
+{
+    double total = 0.0, kept_total = 0.0;
+    for (int j = 0; j < k; ++j) {
+        total += g0[j];
+        if (kept[j])
+            kept_total += g0[j];
+    }
+    for (int j = 0; j < k; ++j) {
+        if (!kept[j])
+            g[j] = 0.0;
+        else if (drop_renorm)
+            g[j] = kept_total > 0.0 ? g0[j] * total / kept_total : 0.0;
+        else
+            g[j] = g0[j];
+    }
+}
+
 /* ---- whole layer ------------------------------------------------------- */
 
 /*
- * out[t] = sum_j g[t][j] * W2[e_j] ( silu(W1[e_j] x_t) * (W3[e_j] x_t) )
- * with e_j and g the router's selection and gates for token t.
+ * out[t] = sum over kept slots j of g[t][j] * W2[e_j] ( silu(W1[e_j] x_t) * (W3[e_j] x_t) )
+ * with e_j the router's selection for token t and g the applied gates.
+ *   gating: 0 or 1 (see gates_of); capacity: rows kept per expert (<= 0: all);
+ *   drop_renorm: policy for dropped slots (see applied_gates).
  * Optional outputs (pass NULL to skip): logits [T][E] fp32, idx [T][k],
- * gates [T][k] in double, and out_exact [T][d]: the weighted sum in double
- * before the one rounding to the element type.
+ * gates [T][k] in double (before any drop), and out_exact [T][d]: the
+ * weighted sum in double before the one rounding to the element type.
  */
-int oracle_moe_forward(const void *x, const void *Wg, const float *bias,
-                       const void *const *W1, const void *const *W3,
-                       const void *const *W2, int T, int d, int ffn, int E, int k,
-                       int dt, void *out, float *logits_out, int *idx_out,
-                       double *gates_out, double *out_exact, int nthreads)
+int oracle_moe_forward_ex(const void *x, const void *Wg, const float *bias,
+                          const void *const *W1, const void *const *W3,
+                          const void *const *W2, int T, int d, int ffn, int E, int k,
+                          int dt, int gating, int capacity, int drop_renorm, void *out,
+                          float *logits_out, int *idx_out, double *gates_out,
+                          double *out_exact, int nthreads)
 {
     if (T < 0 || d < 1 || ffn < 1 || E < 1 || k < 1 || k > E ||
-        (dt != ORACLE_F32 && dt != ORACLE_BF16))
+        (dt != ORACLE_F32 && dt != ORACLE_BF16) || (gating != 0 && gating != 1))
         return ORACLE_BAD_ARG;
     if (T == 0)
         return ORACLE_OK;
@@ -203,30 +263,51 @@ int oracle_moe_forward(const void *x, const void *Wg, const float *bias,
 #else
     (void)nthreads;
 #endif
+    float *L = (float *)malloc(sizeof(float) * (size_t)T * E);
+    int *IDX = (int *)malloc(sizeof(int) * (size_t)T * k);
+    double *G = (double *)malloc(sizeof(double) * (size_t)T * k);
+    unsigned char *KEPT = (unsigned char *)malloc((size_t)T * k);
+    if (!L || !IDX || !G || !KEPT) {
+        free(L);
+        free(IDX);
+        free(G);
+        free(KEPT);
+        return ORACLE_NO_MEM;
+    }
     int status = ORACLE_OK;
+    /* router, per token */
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        float *l = L + (size_t)t * E;
+        for (int e = 0; e < E; ++e)
+            l[e] = router_logit(x, (size_t)t * d, Wg, bias, d, e, dt);
+        if (!all_finite_f32(l, (size_t)E)) {
+#pragma omp atomic write
+            status = ORACLE_NONFINITE;
+        }
+        select_top_k(l, E, k, IDX + (size_t)t * k);
+        gates_of(l, IDX + (size_t)t * k, E, k, gating, G + (size_t)t * k);
+    }
+    /* capacity: which selections each expert keeps, in token order */
+    keep_flags(IDX, T, E, k, capacity, KEPT);
+    /* experts and the weighted sum, per token */
 #pragma omp parallel for schedule(dynamic, 1)
     for (int t = 0; t < T; ++t) {
-        float *l = (float *)malloc(sizeof(float) * (size_t)E);
-        int *chosen = (int *)malloc(sizeof(int) * (size_t)k);
         double *g = (double *)malloc(sizeof(double) * (size_t)k);
         double *h = (double *)malloc(sizeof(double) * (size_t)ffn);
         double *acc = (double *)malloc(sizeof(double) * (size_t)d);
-        if (!l || !chosen || !g || !h || !acc) {
+        if (!g || !h || !acc) {
 #pragma omp atomic write
             status = ORACLE_NO_MEM;
         } else {
             size_t xo = (size_t)t * d;
-            for (int e = 0; e < E; ++e)
-                l[e] = router_logit(x, xo, Wg, bias, d, e, dt);
-            if (!all_finite_f32(l, (size_t)E)) {
-#pragma omp atomic write
-                status = ORACLE_NONFINITE;
-            }
-            select_top_k(l, E, k, chosen);
-            gates_of(l, chosen, k, g);
+            const int *chosen = IDX + (size_t)t * k;
+            applied_gates(G + (size_t)t * k, KEPT + (size_t)t * k, k, drop_renorm, g);
             for (int n = 0; n < d; ++n)
                 acc[n] = 0.0;
             for (int j = 0; j < k; ++j) {
+                if (!KEPT[(size_t)t * k + j])
+                    continue;
                 int e = chosen[j];
                 /* gate and up projections, then the SwiGLU product */
                 for (int c = 0; c < ffn; ++c) {
@@ -253,31 +334,43 @@ int oracle_moe_forward(const void *x, const void *Wg, const float *bias,
             if (out_exact)
                 for (int n = 0; n < d; ++n)
                     out_exact[xo + (size_t)n] = acc[n];
-            if (logits_out)
-                for (int e = 0; e < E; ++e)
-                    logits_out[(size_t)t * E + e] = l[e];
-            for (int j = 0; j < k; ++j) {
-                if (idx_out)
-                    idx_out[(size_t)t * k + j] = chosen[j];
-                if (gates_out)
-                    gates_out[(size_t)t * k + j] = g[j];
-            }
         }
-        free(l);
-        free(chosen);
         free(g);
         free(h);
         free(acc);
     }
+    if (logits_out)
+        memcpy(logits_out, L, sizeof(float) * (size_t)T * E);
+    if (idx_out)
+        memcpy(idx_out, IDX, sizeof(int) * (size_t)T * k);
+    if (gates_out)
+        memcpy(gates_out, G, sizeof(double) * (size_t)T * k);
+    free(L);
+    free(IDX);
+    free(G);
+    free(KEPT);
     return status;
+}
+
+/* The layer as the azimuth.plus router paragraph states it: gating 0, no
+ * capacity limit. */
+int oracle_moe_forward(const void *x, const void *Wg, const float *bias,
+                       const void *const *W1, const void *const *W3,
+                       const void *const *W2, int T, int d, int ffn, int E, int k,
+                       int dt, void *out, float *logits_out, int *idx_out,
+                       double *gates_out, double *out_exact, int nthreads)
+{
+    return oracle_moe_forward_ex(x, Wg, bias, W1, W3, W2, T, d, ffn, E, k, dt, 0, 0, 0, out,
+                                 logits_out, idx_out, gates_out, out_exact, nthreads);
 }
 
 /* Router alone: logits (fp32), selection and gates, for every token. */
 int oracle_router(const void *x, const void *Wg, const float *bias, int T, int d,
-                  int E, int k, int dt, float *logits_out, int *idx_out,
+                  int E, int k, int dt, int gating, float *logits_out, int *idx_out,
                   double *gates_out)
 {
-    if (T < 0 || d < 1 || E < 1 || k < 1 || k > E || !logits_out || !idx_out || !gates_out)
+    if (T < 0 || d < 1 || E < 1 || k < 1 || k > E || !logits_out || !idx_out || !gates_out ||
+        (gating != 0 && gating != 1))
         return ORACLE_BAD_ARG;
     int status = ORACLE_OK;
 #pragma omp parallel for schedule(static)
@@ -290,36 +383,42 @@ int oracle_router(const void *x, const void *Wg, const float *bias, int T, int d
             status = ORACLE_NONFINITE;
         }
         select_top_k(l, E, k, idx_out + (size_t)t * k);
-        gates_of(l, idx_out + (size_t)t * k, k, gates_out + (size_t)t * k);
+        gates_of(l, idx_out + (size_t)t * k, E, k, gating, gates_out + (size_t)t * k);
     }
     return status;
 }
 
 /*
  * Grouping tokens by expert, from given fp32 logits.  Selection and gates as
- * in the router; then
- *   counts[e]  = number of (token, slot) pairs routed to e,
- *   offsets    = exclusive prefix sum of counts, offsets[E] = T*k,
+ * in the router; capacity as in keep_flags; then, over kept selections only,
+ *   counts[e]  = number of (token, slot) pairs expert e keeps,
+ *   offsets    = exclusive prefix sum of counts, offsets[E] = sum of counts,
  *   rows ordered by (expert, token) ascending: row r holds perm[r] = t*k + j,
- *   inv[t*k + j] = r.
+ *   inv[t*k + j] = r, or -1 for a dropped selection.
  */
-int oracle_route(const float *logits, int T, int E, int k, int *idx_out,
-                 double *gates_out, int *counts, int *offsets, int *perm, int *inv)
+int oracle_route(const float *logits, int T, int E, int k, int gating, int capacity,
+                 int *idx_out, double *gates_out, int *counts, int *offsets, int *perm,
+                 int *inv)
 {
     if (T < 0 || E < 1 || k < 1 || k > E || !idx_out || !gates_out || !counts ||
-        !offsets || !perm || !inv)
+        !offsets || !perm || !inv || (gating != 0 && gating != 1))
         return ORACLE_BAD_ARG;
     if (!all_finite_f32(logits, (size_t)T * E))
         return ORACLE_NONFINITE;
     for (int t = 0; t < T; ++t) {
         select_top_k(logits + (size_t)t * E, E, k, idx_out + (size_t)t * k);
-        gates_of(logits + (size_t)t * E, idx_out + (size_t)t * k, k,
+        gates_of(logits + (size_t)t * E, idx_out + (size_t)t * k, E, k, gating,
                  gates_out + (size_t)t * k);
     }
+    unsigned char *kept = (unsigned char *)malloc((size_t)T * k + 1);
+    if (!kept)
+        return ORACLE_NO_MEM;
+    keep_flags(idx_out, T, E, k, capacity, kept);
     for (int e = 0; e < E; ++e)
         counts[e] = 0;
     for (size_t s = 0; s < (size_t)T * k; ++s)
-        counts[idx_out[s]] += 1;
+        if (kept[s])
+            counts[idx_out[s]] += 1;
     offsets[0] = 0;
     for (int e = 0; e < E; ++e)
         offsets[e + 1] = offsets[e] + counts[e];
@@ -328,10 +427,15 @@ int oracle_route(const float *logits, int T, int E, int k, int *idx_out,
         for (int t = 0; t < T; ++t)
             for (int j = 0; j < k; ++j)
                 if (idx_out[(size_t)t * k + j] == e) {
+                    if (!kept[(size_t)t * k + j]) {
+                        inv[(size_t)t * k + j] = -1;
+                        continue;
+                    }
                     perm[r] = t * k + j;
                     inv[(size_t)t * k + j] = r;
                     ++r;
                 }
+    free(kept);
     return ORACLE_OK;
 }
 

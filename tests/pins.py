@@ -408,7 +408,149 @@ def pin_add(o):
 
 
 # ---------------------------------------------------------------------------
-# 6. The pages' printed numbers for the Mixtral shape.
+# 6. Router variant: softmax over all experts, then top-k, no renormalisation.
+# ---------------------------------------------------------------------------
+
+def pin_hand_example_softmax_then_topk(o):
+    """The worked example with gating 1.  t0 logits (a,0,0), a = ln 3: the
+    full softmax is (3/5, 1/5, 1/5), experts 0 and 1 kept with gates 3/5 and
+    1/5: out = 3/5 (2s1, 2s1) + 1/5 (s1, 0) = (1.4 s1, 1.2 s1).
+    t1 logits (a,2a,0): softmax (3, 9, 1)/13, experts 1 then 0, gates 9/13,
+    3/13: out = 9/13 (s1, 6s2) + 3/13 (2s1, 2s1+14s2)."""
+    h = hand_example()
+    out, _, idx, gates = o.moe_forward(h["x"], h["Wg"], h["W1"], h["W3"], h["W2"], 2, gating=1)
+    s1, s2 = silu(1.0), silu(2.0)
+    assert np.array_equal(idx, h["idx"])
+    assert np.allclose(gates[0], [0.6, 0.2], atol=1e-7)
+    assert np.allclose(gates[1], [9 / 13, 3 / 13], atol=1e-7)
+    assert np.allclose(out[0], [1.4 * s1, 1.2 * s1], rtol=1e-6)
+    want1 = [9 / 13 * s1 + 3 / 13 * 2 * s1, 9 / 13 * 6 * s2 + 3 / 13 * (2 * s1 + 14 * s2)]
+    assert np.allclose(out[1], want1, rtol=1e-6)
+
+
+def pin_softmax_then_topk_gates(o):
+    """Gating 1: each gate is the full softmax probability of its expert
+    (library softmax), the gates sum to at most 1 (exactly 1 when k = E), and
+    the layer output is the gating-0 output scaled per token by that sum."""
+    from scipy.special import softmax
+    rng = _rng(20)
+    for E, k in ((8, 2), (5, 5), (16, 4), (64, 8)):
+        logits = (rng.standard_normal((100, E)) * 2).astype(np.float32)
+        idx, g, *_ = o.route(logits, k, gating=1)
+        p = softmax(logits.astype(np.float64), axis=1)
+        assert np.allclose(g, np.take_along_axis(p, idx.astype(np.int64), 1), rtol=1e-13)
+        assert np.all(g.sum(1) <= 1 + 1e-15)
+        if k == E:
+            assert np.allclose(g.sum(1), 1.0, atol=1e-15)
+    x, Wg, W1, W3, W2 = _rand_layer(rng, 9, 8, 12, 6)
+    _, l0, i0, g0, ex0 = o.moe_forward(x, Wg, W1, W3, W2, 2, exact=True)
+    _, l1, i1, g1, ex1 = o.moe_forward(x, Wg, W1, W3, W2, 2, exact=True, gating=1)
+    assert np.array_equal(i0, i1)
+    assert np.allclose(ex1, ex0 * g1.sum(1, keepdims=True), rtol=1e-12, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# 7. Capacity-limited routing.
+# ---------------------------------------------------------------------------
+
+def pin_capacity_hand_example(o):
+    """Capacity 1 on the worked example: expert 0's selections in token order
+    are (t0,slot0), (t1,slot1), (t2,slot1); expert 1's (t0,slot1), (t1,slot0);
+    expert 2's (t2,slot0).  Kept: t0 both slots, t1 none, t2 slot 0 only.
+    Lost mass: out[t1] = 0, out[t2] = 3/4 y2 = 3/4 (-s1-m1, -m1);
+    renormalised: out[t2] = y2."""
+    h = hand_example()
+    s1, m1 = silu(1.0), silu(-1.0)
+    y2 = np.array([-s1 - m1, -m1])
+    for renorm, scale in ((0, 0.75), (1, 1.0)):
+        out, *_ = o.moe_forward(h["x"], h["Wg"], h["W1"], h["W3"], h["W2"], 2, capacity=1,
+                                drop_renorm=renorm)
+        assert np.allclose(out[0], h["out"][0], rtol=1e-6)
+        assert np.all(out[1] == 0)
+        assert np.allclose(out[2], scale * y2, rtol=1e-6)
+    idx, g, counts, offsets, perm, inv = o.route(
+        o.moe_forward(h["x"], h["Wg"], h["W1"], h["W3"], h["W2"], 2)[1], 2, capacity=1)
+    assert list(counts) == [1, 1, 1] and list(offsets) == [0, 1, 2, 3]
+    assert list(perm) == [0, 1, 4] and list(inv) == [0, 1, -1, -1, 2, -1]
+
+
+def pin_capacity_route_bruteforce(o):
+    """Kept selections = each expert's first C selections in token order
+    (built here with a stable sort); rows as in the dropless grouping."""
+    rng = _rng(21)
+    for T, E, k, C in ((200, 8, 2, 30), (64, 4, 2, 1), (100, 16, 4, 20), (50, 8, 2, 1000),
+                       (80, 64, 8, 9)):
+        logits = rng.standard_normal((T, E)).astype(np.float32)
+        logits[:, 0] += 2.0                       # make expert 0 overflow
+        idx, g, counts, offsets, perm, inv = o.route(logits, k, capacity=C)
+        flat = idx.ravel()
+        order = np.argsort(flat, kind="stable")   # by expert, then (token, slot)
+        kept = np.zeros(T * k, bool)
+        for e in range(E):
+            sel = order[flat[order] == e]
+            kept[sel[:C]] = True
+        assert np.array_equal(counts, np.minimum(np.bincount(flat, minlength=E), C))
+        assert np.array_equal(inv < 0, ~kept)
+        assert np.array_equal(np.sort(perm), np.flatnonzero(kept))
+        assert np.array_equal(inv[perm], np.arange(offsets[-1]))
+        for e in range(E):
+            rows = perm[offsets[e]:offsets[e + 1]]
+            assert np.all(flat[rows] == e) and np.all(np.diff(rows // k) > 0)
+
+
+def pin_capacity_gate_policies(o):
+    """Lost mass: kept slots keep their gates.  Renormalised: each token's kept
+    gates sum to its full gate mass (1 in gating 0, the kept softmax mass in
+    gating 1).  A capacity that drops nothing changes nothing."""
+    rng = _rng(22)
+    x, Wg, W1, W3, W2 = _rand_layer(rng, 40, 8, 12, 4)
+    Wg[0] *= 0.0
+    Wg[0, 0] = 5.0                                 # expert 0 popular
+    base = o.moe_forward(x, Wg, W1, W3, W2, 2, exact=True)
+    same = o.moe_forward(x, Wg, W1, W3, W2, 2, exact=True, capacity=40)
+    assert np.array_equal(base[4], same[4])
+    for gating in (0, 1):
+        _, _, idx, g, ex_lost = o.moe_forward(x, Wg, W1, W3, W2, 2, exact=True, gating=gating,
+                                              capacity=6)
+        _, _, _, _, ex_ren = o.moe_forward(x, Wg, W1, W3, W2, 2, exact=True, gating=gating,
+                                           capacity=6, drop_renorm=1)
+        _, _, _, _, ex_full = o.moe_forward(x, Wg, W1, W3, W2, 2, exact=True, gating=gating)
+        _, _, _, _, _, inv = o.route(base[1], 2, gating=gating, capacity=6)
+        kept = (inv >= 0).reshape(-1, 2)
+        # per-expert contributions from single-expert layers (k = 1 on a copy)
+        for t in range(40):
+            if kept[t].all():
+                assert np.allclose(ex_lost[t], ex_full[t], rtol=1e-12, atol=1e-15)
+                assert np.allclose(ex_ren[t], ex_full[t], rtol=1e-12, atol=1e-15)
+            elif not kept[t].any():
+                assert np.all(ex_lost[t] == 0) and np.all(ex_ren[t] == 0)
+            else:
+                j = int(np.flatnonzero(kept[t])[0])
+                # renormalised = lost-mass output scaled by total / kept gate
+                scale = g[t].sum() / g[t, j]
+                assert np.allclose(ex_ren[t], ex_lost[t] * scale, rtol=1e-12, atol=1e-15)
+
+
+def pin_large_E_and_k(o):
+    """64 experts and k up to 8 (k = E too): the dense brute force."""
+    rng = _rng(23)
+    for T, d, ffn, E, k in ((6, 8, 8, 64, 8), (5, 6, 4, 4, 4), (7, 8, 6, 16, 3)):
+        x, Wg, W1, W3, W2 = _rand_layer(rng, T, d, ffn, E)
+        out, logits, idx, _ = o.moe_forward(x, Wg, W1, W3, W2, k)
+        l = logits.astype(np.float64)
+        order = np.argsort(-l, axis=1, kind="stable")[:, :k]
+        assert np.array_equal(idx, order)
+        mask = np.zeros_like(l, dtype=bool)
+        np.put_along_axis(mask, order, True, 1)
+        p = np.where(mask, np.exp(l - l.max(1, keepdims=True)), 0.0)
+        w = p / p.sum(1, keepdims=True)
+        ys = np.stack([_dense_swiglu(x, W1[e], W3[e], W2[e]) for e in range(E)], 1)
+        ref = (w[:, :, None] * ys).sum(1)
+        assert np.allclose(out, ref, rtol=2e-6, atol=2e-7)
+
+
+# ---------------------------------------------------------------------------
+# 8. The pages' printed numbers for the Mixtral shape.
 # ---------------------------------------------------------------------------
 
 def pin_page_shape_numbers(o=None):

@@ -36,6 +36,14 @@ MUTANTS = [
     ("rmsnorm_sum_not_mean", "double scale = 1.0 / sqrt(ss / d + eps);", "double scale = 1.0 / sqrt(ss + eps);"),
     ("counts_off_by_one", "offsets[e + 1] = offsets[e] + counts[e];", "offsets[e + 1] = offsets[e] + counts[e] + (e == 0);"),
     ("second_slot_same_as_first", "if (taken)\n                continue;", "if (taken && j == 0)\n                continue;"),
+    ("full_softmax_unnormalised", "g[j] = exp((double)l[chosen[j]] - l0) / zall;",
+     "g[j] = exp((double)l[chosen[j]] - l0);"),
+    ("full_softmax_over_kept", "zall += exp((double)l[e] - l0);", "zall += exp((double)l[e] - l0) * (e < 2);"),
+    ("capacity_off_by_one", "taken[e] < capacity", "taken[e] <= capacity"),
+    ("capacity_per_slot", "int e = idx[(size_t)t * k + j];\n            kept",
+     "int e = j;\n            kept"),
+    ("renorm_ignores_total", "g0[j] * total / kept_total", "g0[j] / kept_total"),
+    ("dropped_row_kept_in_grouping", "if (!kept[(size_t)t * k + j]) {", "if (0) {"),
 ]
 
 RUNNER = r"""
