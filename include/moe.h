@@ -49,7 +49,9 @@
  *   - The library allocates no device memory: scratch comes from the caller's
  *     `workspace` (size from moe_workspace_bytes, 256-byte aligned).  Calls on
  *     different streams need different workspaces.
- *   - Limits: 1 <= E <= 32, k in {1, 2}, T >= 0 (T = 0 is a no-op).  bf16 needs
+ *   - Limits: 1 <= E <= 64, 1 <= k <= min(E, 8), T >= 0 (T = 0 is a no-op).
+ *     ("Mixtral > Architecture Overview" weighs 4 or 64 experts against 8;
+ *     Mixtral itself uses E = 8, k = 2.)  bf16 needs
  *     d and ffn multiples of 64 and 16-byte aligned tensors; fp32 needs d a
  *     multiple of 4.
  */
@@ -67,13 +69,40 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_ARG = -1,         /* null pointer, negative size, k > E, ...       */
-    MOE_ERR_UNSUPPORTED = -2, /* E > 32, k > 2, alignment or shape limits      */
+    MOE_ERR_UNSUPPORTED = -2, /* E > 64, k > 8, alignment or shape limits      */
     MOE_ERR_WORKSPACE = -3,   /* workspace missing, too small or misaligned    */
     MOE_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed          */
     MOE_ERR_DEVICE = -5       /* a kernel's bounded wait expired (status word) */
 } moe_status;
 
-#define MOE_MAX_EXPERTS 32
+#define MOE_MAX_EXPERTS 64
+#define MOE_MAX_TOPK 8
+
+/*
+ * Routing options (moe_forward_ex, moe_route_from_logits_ex).  A NULL
+ * options pointer, or all fields zero, is the layer as "Mixtral of Experts"
+ * (azimuth.plus, router paragraph) states it.
+ *   gating: MOE_GATING_TOPK_SOFTMAX -- keep the top k logits, softmax over
+ *     them (the gates sum to 1); MOE_GATING_SOFTMAX_TOPK -- softmax over all E
+ *     logits, keep the k largest probabilities as they are, not renormalised
+ *     (a reading of "Mixtral & Sparse MoE (2024) > The Solution", routing
+ *     paragraph).
+ *   capacity: the most (token, slot) selections each expert keeps; an expert
+ *     keeps its first `capacity` selections in token order and drops the rest
+ *     ("The Solution", load-balancing paragraph: capacity constraints).
+ *     <= 0: no limit.  moe_capacity() gives ceil(factor * T * k / E).
+ *   drop_policy: what a dropped selection's gate does.  MOE_DROP_LOSE -- its
+ *     mass is lost (the token's output is the kept slots' weighted sum);
+ *     MOE_DROP_RENORMALIZE -- the token's kept gates are scaled to sum to its
+ *     full gate mass (a token with every slot dropped gets zero output).
+ */
+typedef enum { MOE_GATING_TOPK_SOFTMAX = 0, MOE_GATING_SOFTMAX_TOPK = 1 } moe_gating;
+typedef enum { MOE_DROP_LOSE = 0, MOE_DROP_RENORMALIZE = 1 } moe_drop_policy;
+typedef struct {
+    int gating;      /* moe_gating      */
+    int capacity;    /* rows per expert */
+    int drop_policy; /* moe_drop_policy */
+} moe_options;
 
 /* Text for a status code (static storage). */
 const char *moe_strerror(int status);
@@ -95,6 +124,20 @@ int moe_forward(const void *x, const void *W_g, const float *router_bias,
                 const void *const *W1, const void *const *W3, const void *const *W2,
                 int T, int d, int ffn, int E, int k, int dtype, void *out,
                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * moe_forward with routing options (see moe_options; NULL = moe_forward).
+ * The expert GEMMs only see the kept rows, so a capacity limit also removes
+ * the dropped rows' work.
+ */
+int moe_forward_ex(const void *x, const void *W_g, const float *router_bias,
+                   const void *const *W1, const void *const *W3, const void *const *W2,
+                   int T, int d, int ffn, int E, int k, int dtype, const moe_options *options,
+                   void *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Capacity for a capacity factor: ceil(factor * T * k / E), written to
+ * *capacity (factor <= 0 gives 0, i.e. no limit). */
+int moe_capacity(double capacity_factor, int T, int k, int E, int *capacity);
 
 /*
  * Same as moe_forward, with the tokens and the result in HOST memory: copies
@@ -135,6 +178,17 @@ int moe_route_from_logits(const float *logits, int T, int E, int k, int *idx,
                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * moe_route_from_logits with routing options: gates follow options->gating;
+ * with a capacity only kept selections get rows -- counts are the kept
+ * counts, perm holds offsets[E] entries and inv[t*k + j] is -1 for a dropped
+ * selection.  gates are the routing gates before any drop.
+ */
+int moe_route_from_logits_ex(const float *logits, int T, int E, int k,
+                             const moe_options *options, int *idx, float *gates, int *counts,
+                             int *offsets, int *perm, int *inv, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/*
  * Gather: x_perm[r] = x[perm[r] / k] for r < T*k (exact copies).
  */
 int moe_permute(const void *x, const int *perm, int T, int d, int k, int dtype,
@@ -166,7 +220,9 @@ int moe_expert_down(const void *h, const int *offsets, const void *const *W2, in
 
 /*
  * Gated combine: out[t][n] = sum_j gates[t][j] * (sum_s y[s][inv[t*k+j]][n]),
- * fp32 sums in fixed order, one rounding to dtype.
+ * fp32 sums in fixed order, one rounding to dtype.  Slots with inv < 0 (dropped
+ * by a capacity limit) are skipped; moe_forward_ex's renormalising drop policy
+ * is applied inside moe_forward_ex, not by this entry point.
  */
 int moe_combine(const float *y_partial, int splits, const float *gates, const int *inv,
                 int T, int d, int k, int dtype, void *out, void *stream);

@@ -37,7 +37,7 @@ int injected_fault() {
 int check_dims(int T, int d, int ffn, int E, int k, int dt) {
     if (T < 0 || d <= 0 || ffn <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_ARG;
     if (dt != MOE_F32 && dt != MOE_BF16) return MOE_ERR_ARG;
-    if (E > MOE_MAX_EXPERTS || k > 2) return MOE_ERR_UNSUPPORTED;
+    if (E > MOE_MAX_EXPERTS || k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED;
     if (dt == MOE_BF16 && (d % 64 != 0 || ffn % 64 != 0)) return MOE_ERR_UNSUPPORTED;
     if (dt == MOE_F32 && (d % 4 != 0 || ffn % 4 != 0)) return MOE_ERR_UNSUPPORTED;
     // index arithmetic is 32-bit for rows and 64-bit for element offsets
@@ -255,9 +255,31 @@ T *ws_at(void *ws, size_t off) {
     return reinterpret_cast<T *>(static_cast<uint8_t *>(ws) + off);
 }
 
-int run_forward(const Plan &P, const void *x, const void *W_g, const float *bias,
-                const void *const *W1, const void *const *W3, const void *const *W2, void *out,
-                void *ws, cudaStream_t s) {
+// Routing options with defaults filled in and checked.
+struct Options {
+    int gating = MOE_GATING_TOPK_SOFTMAX;
+    int capacity = 0;
+    int renorm = 0;
+};
+
+int read_options(const moe_options *o, Options *out) {
+    Options r;
+    if (o != nullptr) {
+        if (o->gating != MOE_GATING_TOPK_SOFTMAX && o->gating != MOE_GATING_SOFTMAX_TOPK)
+            return MOE_ERR_ARG;
+        if (o->drop_policy != MOE_DROP_LOSE && o->drop_policy != MOE_DROP_RENORMALIZE)
+            return MOE_ERR_ARG;
+        r.gating = o->gating;
+        r.capacity = o->capacity > 0 ? o->capacity : 0;
+        r.renorm = o->drop_policy == MOE_DROP_RENORMALIZE && r.capacity > 0;
+    }
+    *out = r;
+    return MOE_OK;
+}
+
+int run_forward(const Plan &P, const Options &O, const void *x, const void *W_g,
+                const float *bias, const void *const *W1, const void *const *W3,
+                const void *const *W2, void *out, void *ws, cudaStream_t s) {
     float *logits = ws_at<float>(ws, P.o_logits);
     int *idx = ws_at<int>(ws, P.o_idx);
     float *gates = ws_at<float>(ws, P.o_gates);
@@ -272,14 +294,14 @@ int run_forward(const Plan &P, const void *x, const void *W_g, const float *bias
     float *y = ws_at<float>(ws, P.o_y);
     const int elt = elem_size(P.dt);
     int rc;
-    if ((rc = cuda_rc(launch_router(x, W_g, bias, P.T, P.d, P.E, P.k, P.dt, logits, idx, gates,
-                                    s))) != MOE_OK)
+    if ((rc = cuda_rc(launch_router(x, W_g, bias, P.T, P.d, P.E, P.k, P.dt, O.gating, logits, idx,
+                                    gates, s))) != MOE_OK)
         return rc;
-    if ((rc = cuda_rc(launch_chunk_scan(idx, P.T, P.k, P.E, cc, cb, counts, offsets, s))) !=
-        MOE_OK)
+    if ((rc = cuda_rc(launch_chunk_scan(idx, P.T, P.k, P.E, O.capacity, cc, cb, counts, offsets,
+                                        s))) != MOE_OK)
         return rc;
-    if ((rc = cuda_rc(launch_group_tokens(idx, cb, offsets, x, P.T, P.d, P.E, P.k, elt, perm, inv,
-                                          x_perm, s))) != MOE_OK)
+    if ((rc = cuda_rc(launch_group_tokens(idx, cb, offsets, x, P.T, P.d, P.E, P.k, O.capacity, elt,
+                                          perm, inv, x_perm, s))) != MOE_OK)
         return rc;
     if (P.dt == MOE_BF16) {
         if ((rc = launch_swiglu_tc(x_perm, offsets, W1, W3, P.rows, P.d, P.ffn, P.E, P.bm, P.wide,
@@ -297,7 +319,8 @@ int run_forward(const Plan &P, const void *x, const void *W_g, const float *bias
                                           P.ffn, P.E, y, s))) != MOE_OK)
             return rc;
     }
-    return cuda_rc(launch_combine(y, P.splits, P.rows, gates, inv, P.T, P.d, P.k, P.dt, out, s));
+    return cuda_rc(
+        launch_combine(y, P.splits, P.rows, gates, inv, P.T, P.d, P.k, O.renorm, P.dt, out, s));
 }
 
 int check_forward_args(const void *x, const void *W_g, const void *const *W1,
@@ -373,8 +396,35 @@ int moe_forward(const void *x, const void *W_g, const float *router_bias, const 
     int rc = check_forward_args(x, W_g, W1, W3, W2, T, d, ffn, E, k, dtype, out, workspace,
                                 workspace_bytes, &P);
     if (rc != MOE_OK || T == 0) return rc;
-    return run_forward(P, x, W_g, router_bias, W1, W3, W2, out, workspace,
+    return run_forward(P, Options(), x, W_g, router_bias, W1, W3, W2, out, workspace,
                        static_cast<cudaStream_t>(stream));
+}
+
+int moe_forward_ex(const void *x, const void *W_g, const float *router_bias,
+                   const void *const *W1, const void *const *W3, const void *const *W2, int T,
+                   int d, int ffn, int E, int k, int dtype, const moe_options *options, void *out,
+                   void *workspace, size_t workspace_bytes, void *stream) {
+    Options O;
+    int rc = read_options(options, &O);
+    if (rc != MOE_OK) return rc;
+    Plan P;
+    rc = check_forward_args(x, W_g, W1, W3, W2, T, d, ffn, E, k, dtype, out, workspace,
+                            workspace_bytes, &P);
+    if (rc != MOE_OK || T == 0) return rc;
+    return run_forward(P, O, x, W_g, router_bias, W1, W3, W2, out, workspace,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int moe_capacity(double capacity_factor, int T, int k, int E, int *capacity) {
+    if (capacity == nullptr || T < 0 || k < 1 || E < 1) return MOE_ERR_ARG;
+    if (!(capacity_factor > 0.0)) {
+        *capacity = 0;
+        return MOE_OK;
+    }
+    const double c = ceil(capacity_factor * (double)T * (double)k / (double)E);
+    if (c > 2147483647.0) return MOE_ERR_ARG;
+    *capacity = (int)c;
+    return MOE_OK;
 }
 
 int moe_forward_host_io(const void *x_host, void *out_host, void *x_dev, void *out_dev,
@@ -391,7 +441,8 @@ int moe_forward_host_io(const void *x_host, void *out_host, void *x_dev, void *o
     const size_t bytes = (size_t)T * d * elem_size(dtype);
     if (cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return MOE_ERR_CUDA;
-    if ((rc = run_forward(P, x_dev, W_g, router_bias, W1, W3, W2, out_dev, workspace, s)) != MOE_OK)
+    if ((rc = run_forward(P, Options(), x_dev, W_g, router_bias, W1, W3, W2, out_dev, workspace,
+                          s)) != MOE_OK)
         return rc;
     if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return MOE_ERR_CUDA;
@@ -406,8 +457,8 @@ int moe_router(const void *x, const void *W_g, const float *router_bias, int T, 
     if (T == 0) return MOE_OK;
     if (!x || !W_g || !logits || !idx || !gates) return MOE_ERR_ARG;
     if (!aligned16(x) || !aligned16(W_g)) return MOE_ERR_UNSUPPORTED;
-    return cuda_rc(launch_router(x, W_g, router_bias, T, d, E, k, dtype, logits, idx, gates,
-                                 static_cast<cudaStream_t>(stream)));
+    return cuda_rc(launch_router(x, W_g, router_bias, T, d, E, k, dtype, MOE_GATING_TOPK_SOFTMAX,
+                                 logits, idx, gates, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_route_workspace_bytes(int T, int E, int k, size_t *bytes) {
@@ -422,7 +473,18 @@ int moe_route_workspace_bytes(int T, int E, int k, size_t *bytes) {
 int moe_route_from_logits(const float *logits, int T, int E, int k, int *idx, float *gates,
                           int *counts, int *offsets, int *perm, int *inv, void *workspace,
                           size_t workspace_bytes, void *stream) {
-    int rc = check_dims(T, 64, 64, E, k, MOE_BF16);
+    return moe_route_from_logits_ex(logits, T, E, k, nullptr, idx, gates, counts, offsets, perm,
+                                    inv, workspace, workspace_bytes, stream);
+}
+
+int moe_route_from_logits_ex(const float *logits, int T, int E, int k,
+                             const moe_options *options, int *idx, float *gates, int *counts,
+                             int *offsets, int *perm, int *inv, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    Options O;
+    int rc = read_options(options, &O);
+    if (rc != MOE_OK) return rc;
+    rc = check_dims(T, 64, 64, E, k, MOE_BF16);
     if (rc != MOE_OK) return rc;
     if ((rc = injected_fault()) != MOE_OK) return rc;
     if (!counts || !offsets) return MOE_ERR_ARG;
@@ -442,12 +504,14 @@ int moe_route_from_logits(const float *logits, int T, int E, int k, int *idx, fl
     int *cc = static_cast<int *>(workspace);
     int *cb = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) +
                                       align_up((size_t)nchunks * E * 4));
-    if ((rc = cuda_rc(launch_topk_from_logits(logits, T, E, k, idx, gates, s))) != MOE_OK)
+    if ((rc = cuda_rc(launch_topk_from_logits(logits, T, E, k, O.gating, idx, gates, s))) !=
+        MOE_OK)
         return rc;
-    if ((rc = cuda_rc(launch_chunk_scan(idx, T, k, E, cc, cb, counts, offsets, s))) != MOE_OK)
+    if ((rc = cuda_rc(launch_chunk_scan(idx, T, k, E, O.capacity, cc, cb, counts, offsets, s))) !=
+        MOE_OK)
         return rc;
-    return cuda_rc(launch_group_tokens(idx, cb, offsets, nullptr, T, 0, E, k, 0, perm, inv,
-                                       nullptr, s));
+    return cuda_rc(launch_group_tokens(idx, cb, offsets, nullptr, T, 0, E, k, O.capacity, 0, perm,
+                                       inv, nullptr, s));
 }
 
 int moe_permute(const void *x, const int *perm, int T, int d, int k, int dtype, void *x_perm,
@@ -511,7 +575,7 @@ int moe_combine(const float *y_partial, int splits, const float *gates, const in
     if (T == 0) return MOE_OK;
     if (!y_partial || !gates || !inv || !out) return MOE_ERR_ARG;
     if (d % 4 != 0 || !aligned16(y_partial) || !aligned16(out)) return MOE_ERR_UNSUPPORTED;
-    return cuda_rc(launch_combine(y_partial, splits, T * k, gates, inv, T, d, k, dtype, out,
+    return cuda_rc(launch_combine(y_partial, splits, T * k, gates, inv, T, d, k, 0, dtype, out,
                                   static_cast<cudaStream_t>(stream)));
 }
 

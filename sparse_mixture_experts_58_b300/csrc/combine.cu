@@ -37,46 +37,65 @@ __device__ __forceinline__ void add4(float4 &s, const float4 &p) {
 }
 
 // Block (t, c): token t, columns [4 * C * 256 c, ...): each thread owns C
-// groups of four columns, 256 groups apart.  For each slot, up to SB split
-// partials of all C groups are loaded together, then added in split order, so
-// a thread has 2 * C * SB loads in flight per round trip.
-template <typename T, int C, int SB>
+// groups of four columns, 256 groups apart.  For each of the token's k <= K
+// slots, up to SB split partials of all C groups are loaded together, then
+// added in split order, so a thread has K * C * SB loads in flight per round
+// trip.  A slot with inv < 0 was dropped by a capacity limit and contributes
+// nothing; with `renorm` the kept gates are scaled by (sum of all the token's
+// gates) / (sum of its kept gates), and a token with no kept slot gets 0.
+template <typename T, int K, int C, int SB>
 __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ y, int splits,
                                                       int rows, const float *__restrict__ gates,
                                                       const int *__restrict__ inv, int Tn, int d,
-                                                      int k, T *out) {
+                                                      int k, int renorm, T *out) {
     const int t = blockIdx.x;
     const int nv = d / 4;
     const int v0 = blockIdx.y * 256 * C + threadIdx.x;  // first float4 column group
     const size_t stride4 = (size_t)rows * nv;            // one split, in float4
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-    int rowj[2] = {0, 0};
-    float gj[2] = {0.f, 0.f};
+    int rowj[K];
+    float gj[K];
+    bool use[K];
+    float total = 0.f, kept_total = 0.f;
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < K; ++j) {
+        rowj[j] = 0;
+        gj[j] = 0.f;
+        use[j] = false;
         if (j < k) {
-            rowj[j] = inv[(size_t)t * k + j];
+            const int r = inv[(size_t)t * k + j];
             gj[j] = gates[(size_t)t * k + j];
+            total += gj[j];
+            use[j] = r >= 0;
+            if (use[j]) {
+                rowj[j] = r;
+                kept_total += gj[j];
+            }
         }
     }
-    float4 s[2][C];
-    for (int q0 = 0; q0 < splits; q0 += SB) {
-        float4 p[2][C][SB];
+    if (renorm) {
+        const float f = kept_total > 0.f ? total / kept_total : 0.f;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < K; ++j) gj[j] *= f;
+    }
+    float4 s[K][C];
+    for (int q0 = 0; q0 < splits; q0 += SB) {
+        float4 p[K][C][SB];
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
             const float4 *src = reinterpret_cast<const float4 *>(y) + (size_t)rowj[j] * nv;
 #pragma unroll
             for (int c = 0; c < C; ++c) {
                 const int v = v0 + 256 * c;
 #pragma unroll
                 for (int i = 0; i < SB; ++i)
-                    p[j][c][i] = (j < k && v < nv && q0 + i < splits)
+                    p[j][c][i] = (use[j] && v < nv && q0 + i < splits)
                                      ? __ldcs(src + (size_t)(q0 + i) * stride4 + v)
                                      : zero;
             }
         }
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < K; ++j) {
 #pragma unroll
             for (int c = 0; c < C; ++c) {
                 if (q0 == 0) s[j][c] = p[j][c][0];
@@ -93,8 +112,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
         if (v >= nv) continue;
         float4 acc = zero;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            if (j < k) {
+        for (int j = 0; j < K; ++j) {
+            if (use[j]) {
                 acc.x = fmaf(gj[j], s[j][c].x, acc.x);
                 acc.y = fmaf(gj[j], s[j][c].y, acc.y);
                 acc.z = fmaf(gj[j], s[j][c].z, acc.z);
@@ -105,12 +124,33 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
     }
 }
 
-template <typename T, int C, int SB>
+template <typename T, int K, int C, int SB>
 void launch_combine_t(const float *y, int splits, int rows, const float *gates, const int *inv,
-                      int T_, int d, int k, void *out, cudaStream_t s) {
+                      int T_, int d, int k, int renorm, void *out, cudaStream_t s) {
     const dim3 grid(T_, (d / 4 + 256 * C - 1) / (256 * C));
-    combine_kernel<T, C, SB><<<grid, 256, 0, s>>>(y, splits, rows, gates, inv, T_, d, k,
-                                                  static_cast<T *>(out));
+    combine_kernel<T, K, C, SB><<<grid, 256, 0, s>>>(y, splits, rows, gates, inv, T_, d, k, renorm,
+                                                     static_cast<T *>(out));
+}
+
+// Kernel shape by slot count and split count: unsplit partials (large
+// batches) take 4 column groups per thread; split partials (small batches)
+// one group and several splits per batch.
+template <typename T>
+void launch_combine_dt(const float *y, int splits, int rows, const float *gates, const int *inv,
+                       int T_, int d, int k, int renorm, void *out, cudaStream_t s) {
+    if (k <= 2) {
+        if (splits == 1)
+            launch_combine_t<T, 2, 4, 1>(y, splits, rows, gates, inv, T_, d, k, renorm, out, s);
+        else
+            launch_combine_t<T, 2, 1, 8>(y, splits, rows, gates, inv, T_, d, k, renorm, out, s);
+    } else {
+        if (splits == 1)
+            launch_combine_t<T, MOE_MAX_TOPK, 1, 1>(y, splits, rows, gates, inv, T_, d, k, renorm,
+                                                    out, s);
+        else
+            launch_combine_t<T, MOE_MAX_TOPK, 1, 2>(y, splits, rows, gates, inv, T_, d, k, renorm,
+                                                    out, s);
+    }
 }
 
 // One block per row: optional residual add (rounded to the storage type),
@@ -156,22 +196,13 @@ __global__ void wait_selftest_kernel(unsigned long long limit_ns, int *status) {
 }  // namespace
 
 cudaError_t launch_combine(const float *y, int splits, int rows, const float *gates,
-                           const int *inv, int T, int d, int k, int dt, void *out,
+                           const int *inv, int T, int d, int k, int renorm, int dt, void *out,
                            cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    // unsplit partials (large batches): 4 column groups per thread, one load
-    // per slot each; split partials (small batches): 1 group, 8 splits a batch
-    if (dt == MOE_BF16) {
-        if (splits == 1)
-            launch_combine_t<__nv_bfloat16, 4, 1>(y, splits, rows, gates, inv, T, d, k, out, s);
-        else
-            launch_combine_t<__nv_bfloat16, 1, 8>(y, splits, rows, gates, inv, T, d, k, out, s);
-    } else {
-        if (splits == 1)
-            launch_combine_t<float, 4, 1>(y, splits, rows, gates, inv, T, d, k, out, s);
-        else
-            launch_combine_t<float, 1, 8>(y, splits, rows, gates, inv, T, d, k, out, s);
-    }
+    if (dt == MOE_BF16)
+        launch_combine_dt<__nv_bfloat16>(y, splits, rows, gates, inv, T, d, k, renorm, out, s);
+    else
+        launch_combine_dt<float>(y, splits, rows, gates, inv, T, d, k, renorm, out, s);
     return cudaGetLastError();
 }
 

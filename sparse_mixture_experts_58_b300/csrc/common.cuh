@@ -54,33 +54,42 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
     return __float2bfloat16_rn(v);
 }
 
-// Selection of the k (<= 2) largest of E logits: slot 0 gets the largest,
-// equal values go to the lower index.  Gates: softmax over the kept logits,
-// computed relative to the largest so the exponent is <= 0.
-__device__ __forceinline__ void top2_gates(const float *l, int E, int k, int *sel, float *g) {
-    int i0 = 0;
-    float b0 = l[0];
-    int i1 = -1;
-    float b1 = 0.f;
-    for (int e = 1; e < E; ++e) {
-        float v = l[e];
-        if (v > b0) {
-            i1 = i0; b1 = b0;
-            i0 = e;  b0 = v;
-        } else if (i1 < 0 || v > b1) {
-            i1 = e;  b1 = v;
+// Selection of the k (<= MOE_MAX_TOPK) largest of E logits by insertion into
+// a descending list: slot 0 gets the largest; a value only moves ahead of a
+// strictly smaller one, so equal values keep ascending expert order.
+// Gates, relative to the largest logit l0 so every exponent is <= 0:
+//   gating 0: z_j = exp(l_j - l0), g_j = z_j / sum_j' z_j' (softmax over kept);
+//   gating 1: g_j = exp(l_j - l0) / sum_e exp(l_e - l0) (full softmax, kept
+//             entries not renormalised).
+__device__ __forceinline__ void topk_gates(const float *l, int E, int k, int gating, int *sel,
+                                           float *g) {
+    float val[MOE_MAX_TOPK];
+    int n = 0;
+    for (int e = 0; e < E; ++e) {
+        const float v = l[e];
+        if (n < k || v > val[n - 1]) {
+            int p = n < k ? n : k - 1;
+            while (p > 0 && v > val[p - 1]) {
+                val[p] = val[p - 1];
+                sel[p] = sel[p - 1];
+                --p;
+            }
+            val[p] = v;
+            sel[p] = e;
+            if (n < k) ++n;
         }
     }
-    sel[0] = i0;
-    if (k == 1) {
-        g[0] = 1.f;
-        return;
+    float z[MOE_MAX_TOPK];
+    float s = 0.f;
+    for (int j = 0; j < k; ++j) {
+        z[j] = expf(val[j] - val[0]);
+        s += z[j];
     }
-    sel[1] = i1;
-    float z = expf(b1 - b0);
-    float s = 1.f + z;
-    g[0] = 1.f / s;
-    g[1] = z / s;
+    if (gating == MOE_GATING_SOFTMAX_TOPK) {
+        s = 0.f;
+        for (int e = 0; e < E; ++e) s += expf(l[e] - val[0]);
+    }
+    for (int j = 0; j < k; ++j) g[j] = z[j] / s;
 }
 
 }  // namespace moe

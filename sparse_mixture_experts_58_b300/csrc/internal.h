@@ -37,16 +37,18 @@ int *device_status_ptr();
 
 // Kernel launchers (each returns the launch's cudaError_t).
 cudaError_t launch_router(const void *x, const void *Wg, const float *bias, int T, int d, int E,
-                          int k, int dt, float *logits, int *idx, float *gates, cudaStream_t s);
-cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, int *idx,
-                                    float *gates, cudaStream_t s);
+                          int k, int dt, int gating, float *logits, int *idx, float *gates,
+                          cudaStream_t s);
+cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, int gating,
+                                    int *idx, float *gates, cudaStream_t s);
 // Per-chunk expert counts from idx (into chunk_counts), then their per-expert
-// exclusive scan: chunk_base, counts, offsets.
-cudaError_t launch_chunk_scan(const int *idx, int T, int k, int E, int *chunk_counts,
+// exclusive scan: chunk_base; counts and offsets of the kept rows (capacity
+// <= 0: all rows).
+cudaError_t launch_chunk_scan(const int *idx, int T, int k, int E, int capacity, int *chunk_counts,
                               int *chunk_base, int *counts, int *offsets, cudaStream_t s);
 cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int *offsets,
-                                const void *x, int T, int d, int E, int k, int elt, int *perm,
-                                int *inv, void *x_perm, cudaStream_t s);
+                                const void *x, int T, int d, int E, int k, int capacity, int elt,
+                                int *perm, int *inv, void *x_perm, cudaStream_t s);
 cudaError_t launch_permute(const void *x, const int *perm, int T, int d, int k, int elt,
                            void *x_perm, cudaStream_t s);
 
@@ -64,7 +66,7 @@ cudaError_t launch_down_f32(const float *h, const int *offsets, const void *cons
                             int d, int ffn, int E, float *y, cudaStream_t s);
 
 cudaError_t launch_combine(const float *y, int splits, int rows, const float *gates,
-                           const int *inv, int T, int d, int k, int dt, void *out,
+                           const int *inv, int T, int d, int k, int renorm, int dt, void *out,
                            cudaStream_t s);
 cudaError_t launch_add_rmsnorm(void *x, const void *add, void *xn, int T, int d, float eps,
                                int dt, cudaStream_t s);

@@ -3,55 +3,63 @@
 // contiguous block of rows ("Mixtral" curriculum page: run only the chosen
 // MLPs; batching tokens per expert is the routing work of MoE serving).
 //
-//   chunk_scan:   per-expert exclusive scan over the router's per-chunk counts
-//                 -> counts[E], offsets[E+1], chunk_base[chunk][E]
-//   group_tokens: row of (t, j) = offsets[e] + chunk_base[chunk][e] + rank of
-//                 t among the chunk's tokens routed to e; writes perm / inv and
-//                 copies x[t] to each of its rows (16-byte vectors).
+//   chunk_scan:   per chunk of kChunk tokens, how many selections hit each
+//                 expert; per expert, the exclusive scan of those counts over
+//                 chunks (a selection's rank among its expert's selections in
+//                 token order = chunk base + rank inside the chunk); counts and
+//                 offsets of the rows each expert keeps (all of them, or the
+//                 first `capacity` in token order).
+//   group_tokens: row of (t, j) = offsets[e] + rank, or dropped when rank >=
+//                 capacity; writes perm / inv and copies x[t] to each of its
+//                 rows (16-byte vectors).
 // No atomics decide any position, so the result is deterministic.
 #include "internal.h"
 
 namespace moe {
 namespace {
 
-// One block of 1024 threads.  First each warp counts, for its chunks of
-// kChunk tokens, how many of the chunk's kChunk*k (<= 32) selections hit each
-// expert (one ballot per expert); then warp e scans expert e's column of
-// those counts.  The counts go through global memory (cc); __syncthreads()
-// orders the block's writes before its reads.
+// One block of 1024 threads.  First each warp counts, for its chunks, how many
+// of the chunk's kChunk*k selections hit each expert (ballots over 32-lane
+// segments of idx); lane e%32 keeps expert e's count.  The counts go through
+// global memory (cc); __syncthreads() orders the block's writes before its
+// reads.  Then warp w scans the columns of experts w and w + 32.
 __global__ void __launch_bounds__(1024) chunk_scan_kernel(const int *__restrict__ idx, int Tn,
-                                                          int k, int E, int *cc, int *chunk_base,
-                                                          int *counts, int *offsets) {
+                                                          int k, int E, int capacity, int *cc,
+                                                          int *chunk_base, int *counts,
+                                                          int *offsets) {
     __shared__ int s_tot[MOE_MAX_EXPERTS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nchunks = (Tn + kChunk - 1) / kChunk;
     for (int c = warp; c < nchunks; c += 32) {
         const int first = c * kChunk;
         const int nsel = min(kChunk, Tn - first) * k;
-        const int sel = lane < nsel ? idx[(size_t)first * k + lane] : -1;
-        int mine = 0;
-        for (int e = 0; e < E; ++e) {
-            const int n = __popc(__ballot_sync(0xffffffffu, sel == e));
-            if (lane == e) mine = n;
+        int mine[2] = {0, 0};
+        for (int s0 = 0; s0 < nsel; s0 += 32) {
+            const int sel = s0 + lane < nsel ? idx[(size_t)first * k + s0 + lane] : -1;
+            for (int e = 0; e < E; ++e) {
+                const int n = __popc(__ballot_sync(0xffffffffu, sel == e));
+                if (lane == (e & 31)) mine[e >> 5] += n;
+            }
         }
-        if (lane < E) cc[(size_t)c * E + lane] = mine;
+        if (lane < E) cc[(size_t)c * E + lane] = mine[0];
+        if (lane + 32 < E) cc[(size_t)c * E + lane + 32] = mine[1];
     }
     __syncthreads();
-    if (warp < E) {
+    for (int e = warp; e < E; e += 32) {
         int carry = 0;
         for (int base = 0; base < nchunks; base += 32) {
             const int c = base + lane;
-            const int v = c < nchunks ? cc[(size_t)c * E + warp] : 0;
+            const int v = c < nchunks ? cc[(size_t)c * E + e] : 0;
             int s = v;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const int n = __shfl_up_sync(0xffffffffu, s, off);
                 if (lane >= off) s += n;
             }
-            if (c < nchunks) chunk_base[(size_t)c * E + warp] = carry + s - v;
+            if (c < nchunks) chunk_base[(size_t)c * E + e] = carry + s - v;
             carry += __shfl_sync(0xffffffffu, s, 31);
         }
-        if (lane == 0) s_tot[warp] = carry;
+        if (lane == 0) s_tot[e] = capacity > 0 ? min(carry, capacity) : carry;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -65,10 +73,10 @@ __global__ void __launch_bounds__(1024) chunk_scan_kernel(const int *__restrict_
     }
 }
 
-// Copy one row (rowvec 16-byte vectors) from src to one or two destinations,
-// one warp; four loads per lane are issued before their stores.
-__device__ __forceinline__ void copy_row(const uint4 *__restrict__ src, uint4 *dst0, uint4 *dst1,
-                                         int rowvec, int lane) {
+// Copy one row (rowvec 16-byte vectors) from src to one destination, one
+// warp; four loads per lane are issued before their stores.
+__device__ __forceinline__ void copy_row(const uint4 *__restrict__ src, uint4 *dst, int rowvec,
+                                         int lane) {
     constexpr int U = 4;
     for (int v0 = lane; v0 < rowvec; v0 += 32 * U) {
         uint4 val[U];
@@ -80,25 +88,25 @@ __device__ __forceinline__ void copy_row(const uint4 *__restrict__ src, uint4 *d
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int v = v0 + 32 * u;
-            if (v < rowvec) {
-                dst0[v] = val[u];
-                if (dst1 != nullptr) dst1[v] = val[u];
-            }
+            if (v < rowvec) dst[v] = val[u];
         }
     }
 }
 
-// One block = one chunk of kChunk tokens (8 warps x 2 tokens for the copy).
+// One block = one chunk of kChunk tokens (x up to 8 row slices for small
+// batches, blockIdx.y).  Thread i < kChunk ranks token i's selections against
+// the chunk's earlier tokens; then all threads copy rows.
 __global__ void __launch_bounds__(256) group_tokens_kernel(
     const int *__restrict__ idx, const int *__restrict__ chunk_base,
     const int *__restrict__ offsets, const uint8_t *__restrict__ x, int Tn, int E, int k,
-    size_t row_bytes, int *perm, int *inv, uint8_t *x_perm) {
-    __shared__ int s_idx[kChunk * 2];
-    __shared__ int s_row[kChunk * 2];
+    int capacity, size_t row_bytes, int *perm, int *inv, uint8_t *x_perm) {
+    __shared__ int s_idx[kChunk * MOE_MAX_TOPK];
+    __shared__ int s_row[kChunk * MOE_MAX_TOPK];
     const int c = blockIdx.x;
     const int first = c * kChunk;
     const int ntok = min(kChunk, Tn - first);
-    if (threadIdx.x < ntok * k) s_idx[threadIdx.x] = idx[(size_t)first * k + threadIdx.x];
+    for (int i = threadIdx.x; i < ntok * k; i += blockDim.x)
+        s_idx[i] = idx[(size_t)first * k + i];
     __syncthreads();
     if (threadIdx.x < ntok) {
         const int i = threadIdx.x;
@@ -108,9 +116,11 @@ __global__ void __launch_bounds__(256) group_tokens_kernel(
             int rank = 0;
             for (int i2 = 0; i2 < i; ++i2)
                 for (int j2 = 0; j2 < k; ++j2) rank += (s_idx[i2 * k + j2] == e);
-            const int r = offsets[e] + chunk_base[(size_t)c * E + e] + rank;
+            rank += chunk_base[(size_t)c * E + e];
+            const bool kept = capacity <= 0 || rank < capacity;
+            const int r = kept ? offsets[e] + rank : -1;
             if (blockIdx.y == 0) {
-                perm[r] = t * k + j;
+                if (kept) perm[r] = t * k + j;
                 inv[(size_t)t * k + j] = r;
             }
             s_row[i * k + j] = r;
@@ -120,7 +130,7 @@ __global__ void __launch_bounds__(256) group_tokens_kernel(
     __syncthreads();
     // This block's slice of the chunk's rows (blockIdx.y of gridDim.y parts),
     // flattened to (token, 16-byte vector) pairs over all threads; each thread
-    // issues U loads, then writes each value to the token's k grouped rows.
+    // issues U loads, then writes each value to the token's kept rows.
     constexpr int U = 8;
     const int rowvec_all = static_cast<int>(row_bytes / 16);
     const int vbeg = (int)((long long)rowvec_all * blockIdx.y / gridDim.y);
@@ -142,11 +152,11 @@ __global__ void __launch_bounds__(256) group_tokens_kernel(
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (i0 + (int)blockDim.x * u < total) {
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    if (j < k)
-                        reinterpret_cast<uint4 *>(x_perm + (size_t)s_row[tok[u] * k + j] *
-                                                               row_bytes)[vec[u]] = val[u];
+                for (int j = 0; j < k; ++j) {
+                    const int r = s_row[tok[u] * k + j];
+                    if (r >= 0)
+                        reinterpret_cast<uint4 *>(x_perm + (size_t)r * row_bytes)[vec[u]] = val[u];
+                }
             }
         }
     }
@@ -161,21 +171,21 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint8_t *__restrict_
     const int t = perm[r] / k;
     const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * row_bytes);
     uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)r * row_bytes);
-    copy_row(src, dst, nullptr, static_cast<int>(row_bytes / 16), threadIdx.x & 31);
+    copy_row(src, dst, static_cast<int>(row_bytes / 16), threadIdx.x & 31);
 }
 
 }  // namespace
 
-cudaError_t launch_chunk_scan(const int *idx, int T, int k, int E, int *chunk_counts,
+cudaError_t launch_chunk_scan(const int *idx, int T, int k, int E, int capacity, int *chunk_counts,
                               int *chunk_base, int *counts, int *offsets, cudaStream_t s) {
-    chunk_scan_kernel<<<1, 1024, 0, s>>>(idx, T, k, E, chunk_counts, chunk_base, counts,
+    chunk_scan_kernel<<<1, 1024, 0, s>>>(idx, T, k, E, capacity, chunk_counts, chunk_base, counts,
                                          offsets);
     return cudaGetLastError();
 }
 
 cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int *offsets,
-                                const void *x, int T, int d, int E, int k, int elt, int *perm,
-                                int *inv, void *x_perm, cudaStream_t s) {
+                                const void *x, int T, int d, int E, int k, int capacity, int elt,
+                                int *perm, int *inv, void *x_perm, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const int nchunks = (T + kChunk - 1) / kChunk;
     // few chunks (small batches): split each chunk's row copy over several
@@ -189,8 +199,8 @@ cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int
         if (parts < 1) parts = 1;
     }
     group_tokens_kernel<<<dim3(nchunks, parts), 256, 0, s>>>(
-        idx, chunk_base, offsets, static_cast<const uint8_t *>(x), T, E, k, (size_t)d * elt, perm,
-        inv, static_cast<uint8_t *>(x_perm));
+        idx, chunk_base, offsets, static_cast<const uint8_t *>(x), T, E, k, capacity,
+        (size_t)d * elt, perm, inv, static_cast<uint8_t *>(x_perm));
     return cudaGetLastError();
 }
 

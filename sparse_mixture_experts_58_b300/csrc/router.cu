@@ -43,123 +43,122 @@ constexpr int kRouterThreads = 256;
 constexpr int kRouterTokens = 2;
 
 // Bias, selection, gates and outputs for one token, from its E logits.
-template <int EMAX>
-__device__ __forceinline__ void finish_token(float (&l)[EMAX], const float *bias, int t, int E,
-                                             int k, float *logits, int *idx, float *gates) {
-#pragma unroll
-    for (int e = 0; e < EMAX; ++e) {
-        if (e < E) {
-            l[e] += (bias != nullptr ? bias[e] : 0.f);
-            logits[(size_t)t * E + e] = l[e];
-        }
+__device__ __forceinline__ void finish_token(float *l, const float *bias, int t, int E, int k,
+                                             int gating, float *logits, int *idx, float *gates) {
+    for (int e = 0; e < E; ++e) {
+        l[e] += (bias != nullptr ? bias[e] : 0.f);
+        logits[(size_t)t * E + e] = l[e];
     }
-    int sel[2];
-    float g[2];
-    top2_gates(l, E, k, sel, g);
+    int sel[MOE_MAX_TOPK];
+    float g[MOE_MAX_TOPK];
+    topk_gates(l, E, k, gating, sel, g);
     for (int j = 0; j < k; ++j) {
         idx[(size_t)t * k + j] = sel[j];
         gates[(size_t)t * k + j] = g[j];
     }
 }
 
-// V: 16-byte slices per thread per pass (all loads of a pass are in flight
-// together).  Rows of experts >= E are clamped to a valid row and their sums
-// ignored, which keeps the loads free of branches.
-template <typename T, int EMAX, int V>
+// Experts are taken EG at a time (one pass over the token rows per group,
+// the later passes hitting L1).  V: 16-byte slices per thread per pass, all
+// of a pass's loads in flight together.  Rows of experts >= E are clamped to
+// a valid row and their sums ignored, which keeps the loads free of branches.
+template <typename T, int EG, int V>
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(
     const T *__restrict__ x, const T *__restrict__ Wg, const float *__restrict__ bias, int Tn,
-    int d, int E, int k, float *logits, int *idx, float *gates) {
+    int d, int E, int k, int gating, float *logits, int *idx, float *gates) {
     constexpr int VN = Vec<T>::n;
     constexpr int NW = kRouterThreads / 32;
-    __shared__ float s_part[NW][kRouterTokens][EMAX];
+    __shared__ float s_part[NW][kRouterTokens][MOE_MAX_EXPERTS];
+    __shared__ float s_l[kRouterTokens][MOE_MAX_EXPERTS];
 
     const int t0 = blockIdx.x * kRouterTokens;
     const bool has1 = t0 + 1 < Tn;
     const int nvec = d / VN;
     const uint4 *xr0 = reinterpret_cast<const uint4 *>(x + (size_t)t0 * d);
     const uint4 *xr1 = reinterpret_cast<const uint4 *>(x + (size_t)(has1 ? t0 + 1 : t0) * d);
-    const uint4 *wr[EMAX];
-#pragma unroll
-    for (int e = 0; e < EMAX; ++e)
-        wr[e] = reinterpret_cast<const uint4 *>(Wg + (size_t)(e < E ? e : E - 1) * d);
-
-    float acc0[EMAX], acc1[EMAX];
-#pragma unroll
-    for (int e = 0; e < EMAX; ++e) acc0[e] = acc1[e] = 0.f;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint4 zero = make_uint4(0, 0, 0, 0);
-    for (int v0 = threadIdx.x; v0 < nvec; v0 += kRouterThreads * V) {
-        uint4 xa[V], xb[V], w[V][EMAX];
+
+    for (int g0 = 0; g0 < E; g0 += EG) {
+        const uint4 *wr[EG];
 #pragma unroll
-        for (int u = 0; u < V; ++u) {
-            const int v = v0 + kRouterThreads * u;
-            const int vv = v < nvec ? v : 0;
-            xa[u] = __ldcs(xr0 + vv);
-            xb[u] = __ldcs(xr1 + vv);
+        for (int e = 0; e < EG; ++e)
+            wr[e] = reinterpret_cast<const uint4 *>(Wg + (size_t)(g0 + e < E ? g0 + e : E - 1) * d);
+        float acc0[EG], acc1[EG];
 #pragma unroll
-            for (int e = 0; e < EMAX; ++e) w[u][e] = __ldg(wr[e] + vv);
-            if (v >= nvec) xa[u] = xb[u] = zero;
+        for (int e = 0; e < EG; ++e) acc0[e] = acc1[e] = 0.f;
+        for (int v0 = threadIdx.x; v0 < nvec; v0 += kRouterThreads * V) {
+            uint4 xa[V], xb[V], w[V][EG];
+#pragma unroll
+            for (int u = 0; u < V; ++u) {
+                const int v = v0 + kRouterThreads * u;
+                const int vv = v < nvec ? v : 0;
+                xa[u] = __ldcs(xr0 + vv);
+                xb[u] = __ldcs(xr1 + vv);
+#pragma unroll
+                for (int e = 0; e < EG; ++e) w[u][e] = __ldg(wr[e] + vv);
+                if (v >= nvec) xa[u] = xb[u] = zero;
+            }
+#pragma unroll
+            for (int u = 0; u < V; ++u) {
+                float a[VN], b[VN];
+                Vec<T>::unpack(xa[u], a);
+                Vec<T>::unpack(xb[u], b);
+#pragma unroll
+                for (int e = 0; e < EG; ++e) {
+                    float wf[VN];
+                    Vec<T>::unpack(w[u][e], wf);
+#pragma unroll
+                    for (int i = 0; i < VN; ++i) {
+                        acc0[e] = fmaf(a[i], wf[i], acc0[e]);
+                        acc1[e] = fmaf(b[i], wf[i], acc1[e]);
+                    }
+                }
+            }
         }
+        // butterfly within each warp; lane 0 parks the warp's sums
 #pragma unroll
-        for (int u = 0; u < V; ++u) {
-            float a[VN], b[VN];
-            Vec<T>::unpack(xa[u], a);
-            Vec<T>::unpack(xb[u], b);
+        for (int e = 0; e < EG; ++e) {
 #pragma unroll
-            for (int e = 0; e < EMAX; ++e) {
-                float wf[VN];
-                Vec<T>::unpack(w[u][e], wf);
+            for (int off = 16; off > 0; off >>= 1) {
+                acc0[e] += __shfl_xor_sync(0xffffffffu, acc0[e], off);
+                acc1[e] += __shfl_xor_sync(0xffffffffu, acc1[e], off);
+            }
+        }
+        if (lane == 0) {
 #pragma unroll
-                for (int i = 0; i < VN; ++i) {
-                    acc0[e] = fmaf(a[i], wf[i], acc0[e]);
-                    acc1[e] = fmaf(b[i], wf[i], acc1[e]);
+            for (int e = 0; e < EG; ++e) {
+                if (g0 + e < E) {
+                    s_part[warp][0][g0 + e] = acc0[e];
+                    s_part[warp][1][g0 + e] = acc1[e];
                 }
             }
         }
     }
-    // block reduction: butterfly within each warp, then warps in order
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();
+    // warps added in order: one thread per (token, expert)
+    for (int i = threadIdx.x; i < kRouterTokens * E; i += kRouterThreads) {
+        const int j = i / E, e = i - j * E;
+        float s = s_part[0][j][e];
 #pragma unroll
-    for (int e = 0; e < EMAX; ++e) {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            acc0[e] += __shfl_xor_sync(0xffffffffu, acc0[e], off);
-            acc1[e] += __shfl_xor_sync(0xffffffffu, acc1[e], off);
-        }
-    }
-    if (lane == 0) {
-#pragma unroll
-        for (int e = 0; e < EMAX; ++e) {
-            s_part[warp][0][e] = acc0[e];
-            s_part[warp][1][e] = acc1[e];
-        }
+        for (int w2 = 1; w2 < NW; ++w2) s += s_part[w2][j][e];
+        s_l[j][e] = s;
     }
     __syncthreads();
-    if (threadIdx.x < kRouterTokens && (threadIdx.x == 0 || has1)) {
-        const int j = threadIdx.x;
-        float l[EMAX];
-#pragma unroll
-        for (int e = 0; e < EMAX; ++e) {
-            float s = s_part[0][j][e];
-#pragma unroll
-            for (int w2 = 1; w2 < NW; ++w2) s += s_part[w2][j][e];
-            l[e] = s;
-        }
-        finish_token<EMAX>(l, bias, t0 + j, E, k, logits, idx, gates);
-    }
+    if (threadIdx.x < kRouterTokens && (threadIdx.x == 0 || has1))
+        finish_token(s_l[threadIdx.x], bias, t0 + threadIdx.x, E, k, gating, logits, idx, gates);
 }
 
 // Selection from given logits: one thread per token.
-template <int EMAX>
 __global__ void __launch_bounds__(128) topk_kernel(const float *__restrict__ logits, int Tn, int E,
-                                                   int k, int *idx, float *gates) {
+                                                   int k, int gating, int *idx, float *gates) {
     const int t = blockIdx.x * 128 + threadIdx.x;
     if (t >= Tn) return;
-    float l[EMAX];
-#pragma unroll
-    for (int e = 0; e < EMAX; ++e) l[e] = e < E ? logits[(size_t)t * E + e] : 0.f;
-    int sel[2];
-    float g[2];
-    top2_gates(l, E, k, sel, g);
+    float l[MOE_MAX_EXPERTS];
+    for (int e = 0; e < E; ++e) l[e] = logits[(size_t)t * E + e];
+    int sel[MOE_MAX_TOPK];
+    float g[MOE_MAX_TOPK];
+    topk_gates(l, E, k, gating, sel, g);
     for (int j = 0; j < k; ++j) {
         idx[(size_t)t * k + j] = sel[j];
         gates[(size_t)t * k + j] = g[j];
@@ -168,43 +167,37 @@ __global__ void __launch_bounds__(128) topk_kernel(const float *__restrict__ log
 
 template <typename T>
 cudaError_t router_dispatch(const void *x, const void *Wg, const float *bias, int T_, int d,
-                            int E, int k, float *logits, int *idx, float *gates, cudaStream_t s) {
+                            int E, int k, int gating, float *logits, int *idx, float *gates,
+                            cudaStream_t s) {
     const int grid = (T_ + kRouterTokens - 1) / kRouterTokens;
     const T *xp = static_cast<const T *>(x);
     const T *wp = static_cast<const T *>(Wg);
-    // 16-byte loads in flight per thread per pass: V * (2 + EMAX)
+    // 16-byte loads in flight per thread per pass: V * (2 + EG)
     if (E <= 8)
-        router_kernel<T, 8, 2><<<grid, kRouterThreads, 0, s>>>(xp, wp, bias, T_, d, E, k, logits,
-                                                               idx, gates);
-    else if (E <= 16)
-        router_kernel<T, 16, 1><<<grid, kRouterThreads, 0, s>>>(xp, wp, bias, T_, d, E, k,
-                                                                logits, idx, gates);
+        router_kernel<T, 8, 2><<<grid, kRouterThreads, 0, s>>>(xp, wp, bias, T_, d, E, k, gating,
+                                                               logits, idx, gates);
     else
-        router_kernel<T, 32, 1><<<grid, kRouterThreads, 0, s>>>(xp, wp, bias, T_, d, E, k,
-                                                                logits, idx, gates);
+        router_kernel<T, 16, 1><<<grid, kRouterThreads, 0, s>>>(xp, wp, bias, T_, d, E, k,
+                                                                gating, logits, idx, gates);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_router(const void *x, const void *Wg, const float *bias, int T, int d, int E,
-                          int k, int dt, float *logits, int *idx, float *gates, cudaStream_t s) {
+                          int k, int dt, int gating, float *logits, int *idx, float *gates,
+                          cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (dt == MOE_BF16)
-        return router_dispatch<__nv_bfloat16>(x, Wg, bias, T, d, E, k, logits, idx, gates, s);
-    return router_dispatch<float>(x, Wg, bias, T, d, E, k, logits, idx, gates, s);
+        return router_dispatch<__nv_bfloat16>(x, Wg, bias, T, d, E, k, gating, logits, idx, gates,
+                                              s);
+    return router_dispatch<float>(x, Wg, bias, T, d, E, k, gating, logits, idx, gates, s);
 }
 
-cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, int *idx,
-                                    float *gates, cudaStream_t s) {
+cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, int gating,
+                                    int *idx, float *gates, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    const int grid = (T + 127) / 128;
-    if (E <= 8)
-        topk_kernel<8><<<grid, 128, 0, s>>>(logits, T, E, k, idx, gates);
-    else if (E <= 16)
-        topk_kernel<16><<<grid, 128, 0, s>>>(logits, T, E, k, idx, gates);
-    else
-        topk_kernel<32><<<grid, 128, 0, s>>>(logits, T, E, k, idx, gates);
+    topk_kernel<<<(T + 127) / 128, 128, 0, s>>>(logits, T, E, k, gating, idx, gates);
     return cudaGetLastError();
 }
 

@@ -62,12 +62,31 @@ _sig("moe_forward_static_scratch", _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i,
      _vp, _vp)
 STATIC_SCRATCH_BYTES = 16 << 20
 
+
+class Options(ctypes.Structure):
+    """moe_options: gating (0 softmax over kept, 1 full softmax then top-k),
+    capacity (rows per expert, 0 = no limit), drop_policy (0 lose, 1
+    renormalise)."""
+    _fields_ = [("gating", ctypes.c_int), ("capacity", ctypes.c_int),
+                ("drop_policy", ctypes.c_int)]
+
+
+GATING_TOPK_SOFTMAX, GATING_SOFTMAX_TOPK = 0, 1
+DROP_LOSE, DROP_RENORMALIZE = 0, 1
+MAX_TOPK = 8
+
+_sig("moe_forward_ex", _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _P(Options),
+     _vp, _vp, _sz, _vp)
+_sig("moe_capacity", _i, ctypes.c_double, _i, _i, _i, _P(_i))
+_sig("moe_route_from_logits_ex", _i, _vp, _i, _i, _i, _P(Options), _vp, _vp, _vp, _vp, _vp, _vp,
+     _vp, _sz, _vp)
+
 EXPORTED = [
     "moe_strerror", "moe_version", "moe_workspace_bytes", "moe_forward", "moe_forward_host_io",
     "moe_router", "moe_route_workspace_bytes", "moe_route_from_logits", "moe_permute",
     "moe_expert_swiglu", "moe_down_splits", "moe_expert_down", "moe_combine",
     "moe_add_rmsnorm", "moe_device_status", "moe_selftest_wait_timeout", "moe_forward_launches",
-    "moe_forward_static_scratch",
+    "moe_forward_static_scratch", "moe_forward_ex", "moe_capacity", "moe_route_from_logits_ex",
 ]
 
 
@@ -161,8 +180,17 @@ class Workspace:
         return self.buf
 
 
-def forward(x, Wg, W1, W3, W2, k=2, bias=None, out=None, workspace=None, stream=None):
-    """out = MoE(x) through moe_forward."""
+def capacity(factor, T, k, E) -> int:
+    """ceil(factor * T * k / E) through moe_capacity (0 for factor <= 0)."""
+    c = ctypes.c_int()
+    _check(_lib.moe_capacity(float(factor), T, k, E, ctypes.byref(c)), "moe_capacity")
+    return c.value
+
+
+def forward(x, Wg, W1, W3, W2, k=2, bias=None, out=None, workspace=None, stream=None,
+            gating=0, capacity=0, drop_policy=0):
+    """out = MoE(x) through moe_forward, or moe_forward_ex when a routing
+    option is set (gating, capacity in rows per expert, drop_policy)."""
     T, d, ffn, E = _shape(x, Wg, W1)
     dt = _dt(x)
     if out is None:
@@ -172,6 +200,12 @@ def forward(x, Wg, W1, W3, W2, k=2, bias=None, out=None, workspace=None, stream=
     if ws is None:
         ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
     p1, p3, p2 = _expert_ptrs(W1, E), _expert_ptrs(W3, E), _expert_ptrs(W2, E)
+    if gating or capacity or drop_policy:
+        opt = Options(int(gating), int(capacity), int(drop_policy))
+        _check(_lib.moe_forward_ex(_ptr(x), _ptr(Wg), _ptr(bias), p1, p3, p2, T, d, ffn, E, k, dt,
+                                   ctypes.byref(opt), _ptr(out), _ptr(ws), ws.numel(),
+                                   _stream(stream)), "moe_forward_ex")
+        return out
     _check(_lib.moe_forward(_ptr(x), _ptr(Wg), _ptr(bias), p1, p3, p2, T, d, ffn, E, k, dt,
                             _ptr(out), _ptr(ws), ws.numel(), _stream(stream)), "moe_forward")
     return out
@@ -213,7 +247,9 @@ def router(x, Wg, k=2, bias=None, stream=None):
     return logits, idx, gates
 
 
-def route_from_logits(logits, k=2, stream=None):
+def route_from_logits(logits, k=2, stream=None, gating=0, capacity=0):
+    """(idx, gates, counts, offsets, perm, inv); with a capacity, counts are
+    the kept counts, perm has offsets[E] valid rows, inv is -1 when dropped."""
     T, E = logits.shape
     dev = logits.device
     n = ctypes.c_size_t()
@@ -225,9 +261,17 @@ def route_from_logits(logits, k=2, stream=None):
     offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
     perm = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
     inv = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
-    _check(_lib.moe_route_from_logits(_ptr(logits), T, E, k, _ptr(idx), _ptr(gates), _ptr(counts),
-                                      _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(ws), ws.numel(),
-                                      _stream(stream)), "moe_route_from_logits")
+    if gating or capacity:
+        opt = Options(int(gating), int(capacity), 0)
+        _check(_lib.moe_route_from_logits_ex(_ptr(logits), T, E, k, ctypes.byref(opt), _ptr(idx),
+                                             _ptr(gates), _ptr(counts), _ptr(offsets), _ptr(perm),
+                                             _ptr(inv), _ptr(ws), ws.numel(), _stream(stream)),
+               "moe_route_from_logits_ex")
+    else:
+        _check(_lib.moe_route_from_logits(_ptr(logits), T, E, k, _ptr(idx), _ptr(gates),
+                                          _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv),
+                                          _ptr(ws), ws.numel(), _stream(stream)),
+               "moe_route_from_logits")
     return idx, gates, counts, offsets, perm[:T * k], inv[:T * k]
 
 

@@ -64,10 +64,10 @@ def test_workspace_sizes(moe):
 
 
 @pytest.mark.parametrize("args,code", [
-    ((16, 4096, 14336, 8, 3, 1), -2),      # only k in {1, 2}
+    ((16, 4096, 14336, 16, 9, 1), -2),     # top-k above 8
     ((16, 4096, 14336, 2, 3, 1), -1),      # k > E
     ((-1, 4096, 14336, 8, 2, 1), -1),      # negative T
-    ((16, 4096, 14336, 33, 2, 1), -2),     # too many experts
+    ((16, 4096, 14336, 65, 2, 1), -2),     # more than 64 experts
     ((16, 4000, 14336, 8, 2, 1), -2),      # bf16 needs d % 64 == 0
     ((16, 4096, 14300, 8, 2, 1), -2),      # bf16 needs ffn % 64 == 0
     ((16, 130, 448, 8, 2, 0), -2),         # fp32 needs d % 4 == 0
@@ -92,7 +92,7 @@ def _forward_call(moe, **over):
 
 
 def test_forward_validates_before_launch(moe):
-    assert _forward_call(moe, k=3) == -2
+    assert _forward_call(moe, k=9, E=16) == -2
     assert _forward_call(moe, x=None) == -1
     assert _forward_call(moe, W1=None) == -1
     assert _forward_call(moe, ws=None) == -3                       # no workspace
@@ -128,3 +128,21 @@ def test_binding_module_requires_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "not built" in r.stdout
+
+
+def test_capacity_helper(moe):
+    assert moe.capacity(1.0, 4096, 2, 8) == 1024
+    assert moe.capacity(1.25, 4096, 2, 8) == 1280
+    assert moe.capacity(1.1, 10, 2, 8) == 3          # ceil(2.75)
+    assert moe.capacity(0.0, 4096, 2, 8) == 0        # no limit
+
+
+def test_forward_ex_rejects_bad_options(moe):
+    E = 8
+    arr = ctypes.c_void_p * E
+    fake = ctypes.c_void_p(0x10000)
+    w = arr(*([0x10000] * E))
+    for opt in (moe.Options(2, 0, 0), moe.Options(0, 10, 5)):
+        rc = moe.lib().moe_forward_ex(fake, fake, None, w, w, w, 16, 256, 512, E, 2, moe.BF16,
+                                      ctypes.byref(opt), fake, None, 0, None)
+        assert rc == -1
