@@ -214,10 +214,13 @@ WORKLOAD_NAMES = {
 }
 
 
-def algorithmic(T, d, ffn, E, k, n_touched, rows_per_expert=None):
+def algorithmic(T, d, ffn, E, k, n_touched, rows=None):
     """Algorithmic FLOPs and HBM bytes of one layer forward (what the method
-    must do: touched experts' weights once, the router weights, x in, out)."""
-    flops = T * (2 * k * 3 * d * ffn + 2 * d * E)
+    must do: the expert rows computed -- T*k, or the kept ones under a
+    capacity limit -- the touched experts' weights once, the router weights,
+    x in, out)."""
+    rows = T * k if rows is None else rows
+    flops = rows * 2 * 3 * d * ffn + T * 2 * d * E
     bytes_ = n_touched * 3 * d * ffn * 2 + d * E * 2 + 2 * T * d * 2 + T * E * 4
     return flops, bytes_
 
@@ -312,12 +315,26 @@ def measure(args, rank, world, local):
     dev = torch.device("cuda", local)
     dist_init(world, "nccl")
     cfg = dict(inputs.WORKLOADS[args.config])
-    if args.T:
-        cfg["T"] = args.T
+    overrides = []
+    for key in ("T", "E", "k"):
+        v = getattr(args, key)
+        if v:
+            cfg[key] = v
+            overrides.append(f"{key}={v}")
     T, d, ffn, E, k = cfg["T"], cfg["d"], cfg["ffn"], cfg["E"], cfg["k"]
+    if cfg.get("bias") is not None and len(cfg["bias"]) != E:
+        cfg["bias"] = (list(cfg["bias"]) + [0.0] * E)[:E]
+    cap = moe.capacity(args.capacity_factor, T, k, E) if args.capacity_factor > 0 else 0
+    policy = 1 if args.drop_policy == "renorm" else 0
+    route_kw = dict(gating=args.gating, capacity=cap, drop_policy=policy if cap else 0)
+    if args.gating:
+        overrides.append("gating: softmax over all experts, then top-k")
+    if cap:
+        overrides.append(f"capacity factor {args.capacity_factor} -> {cap} rows/expert, "
+                         f"dropped mass {'renormalised' if policy else 'lost'}")
     workload = WORKLOAD_NAMES[args.config]
-    if args.T:
-        workload = f"{workload} (T overridden to {T})"
+    if overrides:
+        workload = f"{workload} ({'; '.join(overrides)})"
 
     # weights shared by every rank; tokens per rank
     gen = inputs.generator(cfg["seed"], dev)
@@ -333,12 +350,15 @@ def measure(args, rank, world, local):
 
     def step():
         moe.forward(x, layer.Wg, layer.W1, layer.W3, layer.W2, k, bias=bias, out=out,
-                    workspace=ws)
+                    workspace=ws, **route_kw)
 
-    # routing of this batch (for the touched-expert byte count)
-    _, idx, _ = moe.router(x, layer.Wg, k, bias)
-    counts = torch.bincount(idx.flatten().long(), minlength=E).cpu()
+    # routing of this batch: kept rows per expert (for the algorithmic counts)
+    logits0, _, _ = moe.router(x, layer.Wg, k, bias)
+    _, _, kept_counts, _, _, _ = moe.route_from_logits(logits0, k, gating=args.gating,
+                                                       capacity=cap)
+    counts = kept_counts.cpu()
     n_touched = int((counts > 0).sum())
+    rows_kept = int(counts.sum())
 
     for _ in range(args.warmup):
         step()
@@ -393,9 +413,10 @@ def measure(args, rank, world, local):
         evs[0].record(stream)
         logits, _, _ = moe.router(x, layer.Wg, k, bias)
         evs[1].record(stream)
-        _, gates2, _, offsets, perm, inv = moe.route_from_logits(logits, k)
+        _, gates2, _, offsets, perm, inv = moe.route_from_logits(logits, k, gating=args.gating,
+                                                                 capacity=cap)
         evs[2].record(stream)
-        xp = moe.permute(x, perm, k)
+        xp = moe.permute(x, perm, k, rows=rows_kept)
         evs[3].record(stream)
         h = moe.expert_swiglu(xp, offsets, layer.W1, layer.W3)
         evs[4].record(stream)
@@ -428,12 +449,12 @@ def measure(args, rank, world, local):
         return 0
 
     peaks, peak_src = load_peaks()
-    flops, bytes_ = algorithmic(T, d, ffn, E, k, n_touched)
+    flops, bytes_ = algorithmic(T, d, ffn, E, k, n_touched, rows=rows_kept)
     t_step = elapsed_max / args.steps
     t_roof = max(bytes_ / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
     layer_bound = "hbm" if bytes_ / peaks["hbm_gbs"] > flops / (peaks["bf16_tflops"] * 1e3) else "tensor"
 
-    g_flops, g_bytes = gemm1_algorithmic(T * k, d, ffn, n_touched)
+    g_flops, g_bytes = gemm1_algorithmic(rows_kept, d, ffn, n_touched)
     t_g = stage_s[3]
     g_bound = "hbm" if g_bytes / (peaks["hbm_gbs"] * 1e9) > g_flops / (peaks["bf16_tflops"] * 1e12) else "tensor"
     if g_bound == "hbm":
@@ -460,12 +481,13 @@ def measure(args, rank, world, local):
             "l2": "no flush: each step streams the touched experts' weights "
                   f"({n_touched * 3 * d * ffn * 2 / 1e9:.2f} GB) > 126 MB L2",
             "experts_touched": n_touched, "rows_per_expert": counts.tolist(),
+            "rows_computed": rows_kept, "routing": route_kw,
         },
         "roofline": {
             "kernel": "grouped gate/up GEMM + SwiGLU (tcgen05)",
             "bound": g_bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "peak_source": f"{peak_src} (burst)",
-            "traffic": recorded_traffic(f"gate_up_{args.config}"),
+            "traffic": None if overrides else recorded_traffic(f"gate_up_{args.config}"),
             "traffic_source": "profiles/ncu_traffic.json (dram__bytes_read.sum + "
                               "dram__bytes_write.sum, one ncu capture; null if the kernel "
                               "source changed since)",
@@ -482,7 +504,8 @@ def measure(args, rank, world, local):
         "e2e": {"value": T * world * args.steps / e2e_elapsed, "unit": "tokens/s",
                 "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2,
                 "how": "moe_forward_host_io called per step: pinned x -> device, layer, "
-                       "out -> pinned host, all on one stream"},
+                       "out -> pinned host, all on one stream" +
+                       ("" if not (args.gating or cap) else " (default routing options)")},
         "timed_as": "CUDA graph replay of one moe_forward call per step" if graph is not None
                     else "moe_forward called per step",
         "direct_call_tokens_per_s": T * world * args.steps / direct_elapsed,
@@ -611,6 +634,13 @@ def main(argv=None):
     ap.add_argument("--config", choices=sorted(WORKLOAD_NAMES) + ["sweep"], default="decode")
     ap.add_argument("--sweep-T", default="", help="comma-separated token counts for --config sweep")
     ap.add_argument("--T", type=int, default=0, help="override the workload's token count")
+    ap.add_argument("--E", type=int, default=0, help="override the number of experts")
+    ap.add_argument("--k", type=int, default=0, help="override the experts per token")
+    ap.add_argument("--gating", type=int, default=0, choices=[0, 1],
+                    help="0: softmax over the kept logits; 1: softmax over all, then top-k")
+    ap.add_argument("--capacity-factor", type=float, default=0.0,
+                    help="rows per expert = ceil(factor * T * k / E); 0 = no limit")
+    ap.add_argument("--drop-policy", choices=["lose", "renorm"], default="lose")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="time direct moe_forward calls instead of a captured CUDA graph")

@@ -189,9 +189,10 @@ int moe_route_from_logits_ex(const float *logits, int T, int E, int k,
                              size_t workspace_bytes, void *stream);
 
 /*
- * Gather: x_perm[r] = x[perm[r] / k] for r < T*k (exact copies).
+ * Gather: x_perm[r] = x[perm[r] / k] for r < rows (exact copies); rows <= T*k
+ * (T*k without a capacity limit, offsets[E] with one).
  */
-int moe_permute(const void *x, const int *perm, int T, int d, int k, int dtype,
+int moe_permute(const void *x, const int *perm, int rows, int T, int d, int k, int dtype,
                 void *x_perm, void *stream);
 
 /*

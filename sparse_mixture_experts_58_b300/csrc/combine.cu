@@ -48,6 +48,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
                                                       int rows, const float *__restrict__ gates,
                                                       const int *__restrict__ inv, int Tn, int d,
                                                       int k, int renorm, T *out) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x;
     const int nv = d / 4;
     const int v0 = blockIdx.y * 256 * C + threadIdx.x;  // first float4 column group
@@ -128,8 +130,8 @@ template <typename T, int K, int C, int SB>
 void launch_combine_t(const float *y, int splits, int rows, const float *gates, const int *inv,
                       int T_, int d, int k, int renorm, void *out, cudaStream_t s) {
     const dim3 grid(T_, (d / 4 + 256 * C - 1) / (256 * C));
-    combine_kernel<T, K, C, SB><<<grid, 256, 0, s>>>(y, splits, rows, gates, inv, T_, d, k, renorm,
-                                                     static_cast<T *>(out));
+    launch_pdl(combine_kernel<T, K, C, SB>, grid, 256, 0, s, y, splits, rows, gates, inv, T_, d, k,
+               renorm, static_cast<T *>(out));
 }
 
 // Kernel shape by slot count and split count: unsplit partials (large
@@ -159,6 +161,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) add_rmsnorm_kernel(T *x, const T *__restrict__ add, T *xn,
                                                           int d, float eps) {
     __shared__ float s_part[8];
+    pdl_wait();
+    pdl_trigger();
     const size_t o = (size_t)blockIdx.x * d;
     float ss = 0.f;
     for (int i = threadIdx.x; i < d; i += blockDim.x) {
@@ -210,14 +214,12 @@ cudaError_t launch_add_rmsnorm(void *x, const void *add, void *xn, int T, int d,
                                cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (dt == MOE_BF16)
-        add_rmsnorm_kernel<__nv_bfloat16><<<T, 256, 0, s>>>(
-            static_cast<__nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(add),
-            static_cast<__nv_bfloat16 *>(xn), d, eps);
-    else
-        add_rmsnorm_kernel<float><<<T, 256, 0, s>>>(static_cast<float *>(x),
-                                                    static_cast<const float *>(add),
-                                                    static_cast<float *>(xn), d, eps);
-    return cudaGetLastError();
+        return launch_pdl(add_rmsnorm_kernel<__nv_bfloat16>, T, 256, 0, s,
+                          static_cast<__nv_bfloat16 *>(x),
+                          static_cast<const __nv_bfloat16 *>(add),
+                          static_cast<__nv_bfloat16 *>(xn), d, eps);
+    return launch_pdl(add_rmsnorm_kernel<float>, T, 256, 0, s, static_cast<float *>(x),
+                      static_cast<const float *>(add), static_cast<float *>(xn), d, eps);
 }
 
 cudaError_t launch_wait_selftest(unsigned int limit_ns, cudaStream_t s) {

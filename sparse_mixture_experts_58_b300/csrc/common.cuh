@@ -36,6 +36,17 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
+// Programmatic dependent launch: every kernel of the layer is launched so it
+// may start while the previous one finishes.  A kernel calls pdl_wait()
+// before it touches anything an earlier kernel wrote (the wait returns once
+// the previous grid has completed and its writes are visible), and then
+// pdl_trigger() so the next kernel may be scheduled; since a kernel triggers
+// only after its own wait returned, every kernel before it has completed too.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // The first expired wait wins; later ones leave the word alone.
 __device__ __forceinline__ void report_status(int *status, int code) {
     if (status != nullptr) atomicCAS(status, 0, code);
@@ -54,42 +65,56 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
     return __float2bfloat16_rn(v);
 }
 
-// Selection of the k (<= MOE_MAX_TOPK) largest of E logits by insertion into
-// a descending list: slot 0 gets the largest; a value only moves ahead of a
-// strictly smaller one, so equal values keep ascending expert order.
+// Selection of the k (<= KMAX <= MOE_MAX_TOPK) largest of E logits: each
+// logit in expert order is carried down a list of KMAX entries kept in
+// (value descending, expert ascending) order, swapping places with any entry
+// it precedes in that order -- a larger value, or an equal value of a lower
+// expert (a displaced entry moving down can tie with the next one and must
+// then stay ahead of it).  Slot 0 ends with the largest logit; equal logits
+// keep ascending expert order.  Fully unrolled over the list: registers only.
 // Gates, relative to the largest logit l0 so every exponent is <= 0:
 //   gating 0: z_j = exp(l_j - l0), g_j = z_j / sum_j' z_j' (softmax over kept);
 //   gating 1: g_j = exp(l_j - l0) / sum_e exp(l_e - l0) (full softmax, kept
 //             entries not renormalised).
-__device__ __forceinline__ void topk_gates(const float *l, int E, int k, int gating, int *sel,
-                                           float *g) {
-    float val[MOE_MAX_TOPK];
-    int n = 0;
+template <int KMAX>
+__device__ __forceinline__ void topk_gates(const float *l, int E, int k, int gating,
+                                           int (&sel)[KMAX], float (&g)[KMAX]) {
+    float val[KMAX];
+#pragma unroll
+    for (int p = 0; p < KMAX; ++p) {
+        val[p] = -INFINITY;
+        sel[p] = -1;
+    }
     for (int e = 0; e < E; ++e) {
-        const float v = l[e];
-        if (n < k || v > val[n - 1]) {
-            int p = n < k ? n : k - 1;
-            while (p > 0 && v > val[p - 1]) {
-                val[p] = val[p - 1];
-                sel[p] = sel[p - 1];
-                --p;
-            }
-            val[p] = v;
-            sel[p] = e;
-            if (n < k) ++n;
+        float v = l[e];
+        int id = e;
+#pragma unroll
+        for (int p = 0; p < KMAX; ++p) {
+            const bool gt = sel[p] < 0 || v > val[p] || (v == val[p] && id < sel[p]);
+            const float tv = val[p];
+            const int ti = sel[p];
+            val[p] = gt ? v : tv;
+            sel[p] = gt ? id : ti;
+            v = gt ? tv : v;
+            id = gt ? ti : id;
         }
     }
-    float z[MOE_MAX_TOPK];
+    float z[KMAX];
     float s = 0.f;
-    for (int j = 0; j < k; ++j) {
-        z[j] = expf(val[j] - val[0]);
-        s += z[j];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        z[j] = 0.f;
+        if (j < k) {
+            z[j] = expf(val[j] - val[0]);
+            s += z[j];
+        }
     }
     if (gating == MOE_GATING_SOFTMAX_TOPK) {
         s = 0.f;
         for (int e = 0; e < E; ++e) s += expf(l[e] - val[0]);
     }
-    for (int j = 0; j < k; ++j) g[j] = z[j] / s;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) g[j] = z[j] / s;
 }
 
 }  // namespace moe

@@ -27,6 +27,8 @@ __global__ void __launch_bounds__(256) grouped_gemm_f32(const __grid_constant__ 
     __shared__ float sB1[SWIGLU ? BK : 1][BN + 4];
     __shared__ int s_off[kMaxE + 1], s_mt[kMaxE], s_ustart[kMaxE + 1];
 
+    pdl_wait();
+    pdl_trigger();
     const int tid = threadIdx.x;
     const int NT = (a.N + BN - 1) / BN;
     if (tid <= a.E) s_off[tid] = a.offsets[tid];
@@ -140,8 +142,7 @@ cudaError_t run_f32(const float *A, const int *offsets, const void *const *B0,
     args.K = K;
     args.N = N;
     const int grid = ((rows + BM - 1) / BM + E) * ((N + BN - 1) / BN);
-    grouped_gemm_f32<SWIGLU><<<grid, 256, 0, s>>>(args);
-    return cudaGetLastError();
+    return launch_pdl(grouped_gemm_f32<SWIGLU>, grid, 256, 0, s, args);
 }
 
 }  // namespace

@@ -134,6 +134,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_cons
         ptx::tmem_alloc(tmem_slot, kTmemCols);
         ptx::tmem_relinquish();
     }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&a.mapA);
+        ptx::prefetch_tensormap(&a.mapB0[0]);
+    }
+    // everything above overlaps the previous kernel's tail; the row offsets
+    // and the token rows are that kernel's (or an earlier one's) output
+    pdl_wait();
+    pdl_trigger();
     if (threadIdx.x <= E) s_off[threadIdx.x] = a.offsets[threadIdx.x];
     ptx::tc_fence_before_sync();
     __syncthreads();
@@ -156,7 +164,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_cons
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            ptx::prefetch_tensormap(&a.mapA);
             const uint32_t tx_bytes = static_cast<uint32_t>(a.bm * 128 + NB * 128);
             int stage = 0;
             uint32_t ph = 0;
@@ -346,8 +353,8 @@ int run_tc(TcArgs &args, int units_bound, cudaStream_t s) {
     }
     const int grid = units_bound < device_sm_count() ? units_bound : device_sm_count();
     if (grid <= 0) return MOE_OK;
-    kernel<<<grid, kThreads, L::kTotal, s>>>(args);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return launch_pdl(kernel, grid, kThreads, L::kTotal, s, args) == cudaSuccess ? MOE_OK
+                                                                                  : MOE_ERR_CUDA;
 }
 
 int fill_common(TcArgs &args, const void *A, const int *offsets, void *out, int rows, int K,

@@ -30,6 +30,29 @@ struct Plan {
 
 int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p);
 
+// Launch with programmatic stream serialisation allowed, so the kernel may be
+// scheduled while the previous kernel on the stream drains (the kernel itself
+// calls pdl_wait() before reading earlier results).  A previous kernel that
+// never triggers releases it at completion, as an ordinary launch would.
+// Whether launches carry the attribute (MOE_PDL=1; off by default).
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 int elem_size(int dt);
 int device_sm_count();
 // Device address of the status word for the current device (nullptr on error).
@@ -49,7 +72,8 @@ cudaError_t launch_chunk_scan(const int *idx, int T, int k, int E, int capacity,
 cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int *offsets,
                                 const void *x, int T, int d, int E, int k, int capacity, int elt,
                                 int *perm, int *inv, void *x_perm, cudaStream_t s);
-cudaError_t launch_permute(const void *x, const int *perm, int T, int d, int k, int elt,
+// x_perm[r] = x[perm[r] / k] for r < rows.
+cudaError_t launch_permute(const void *x, const int *perm, int rows, int d, int k, int elt,
                            void *x_perm, cudaStream_t s);
 
 // Grouped expert GEMMs.  `rows` = total expert rows (T*k); `bm` rows per tile.

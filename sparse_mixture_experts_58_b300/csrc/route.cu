@@ -28,21 +28,24 @@ __global__ void __launch_bounds__(1024) chunk_scan_kernel(const int *__restrict_
                                                           int *chunk_base, int *counts,
                                                           int *offsets) {
     __shared__ int s_tot[MOE_MAX_EXPERTS];
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nchunks = (Tn + kChunk - 1) / kChunk;
     for (int c = warp; c < nchunks; c += 32) {
         const int first = c * kChunk;
         const int nsel = min(kChunk, Tn - first) * k;
-        int mine[2] = {0, 0};
+        int mine_lo = 0, mine_hi = 0;  // experts lane and lane + 32
         for (int s0 = 0; s0 < nsel; s0 += 32) {
             const int sel = s0 + lane < nsel ? idx[(size_t)first * k + s0 + lane] : -1;
             for (int e = 0; e < E; ++e) {
                 const int n = __popc(__ballot_sync(0xffffffffu, sel == e));
-                if (lane == (e & 31)) mine[e >> 5] += n;
+                if (lane == e) mine_lo += n;
+                if (lane + 32 == e) mine_hi += n;
             }
         }
-        if (lane < E) cc[(size_t)c * E + lane] = mine[0];
-        if (lane + 32 < E) cc[(size_t)c * E + lane + 32] = mine[1];
+        if (lane < E) cc[(size_t)c * E + lane] = mine_lo;
+        if (lane + 32 < E) cc[(size_t)c * E + lane + 32] = mine_hi;
     }
     __syncthreads();
     for (int e = warp; e < E; e += 32) {
@@ -96,12 +99,15 @@ __device__ __forceinline__ void copy_row(const uint4 *__restrict__ src, uint4 *d
 // One block = one chunk of kChunk tokens (x up to 8 row slices for small
 // batches, blockIdx.y).  Thread i < kChunk ranks token i's selections against
 // the chunk's earlier tokens; then all threads copy rows.
+template <int KMAX>
 __global__ void __launch_bounds__(256) group_tokens_kernel(
     const int *__restrict__ idx, const int *__restrict__ chunk_base,
     const int *__restrict__ offsets, const uint8_t *__restrict__ x, int Tn, int E, int k,
     int capacity, size_t row_bytes, int *perm, int *inv, uint8_t *x_perm) {
     __shared__ int s_idx[kChunk * MOE_MAX_TOPK];
     __shared__ int s_row[kChunk * MOE_MAX_TOPK];
+    pdl_wait();
+    pdl_trigger();
     const int c = blockIdx.x;
     const int first = c * kChunk;
     const int ntok = min(kChunk, Tn - first);
@@ -152,10 +158,14 @@ __global__ void __launch_bounds__(256) group_tokens_kernel(
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (i0 + (int)blockDim.x * u < total) {
-                for (int j = 0; j < k; ++j) {
-                    const int r = s_row[tok[u] * k + j];
-                    if (r >= 0)
-                        reinterpret_cast<uint4 *>(x_perm + (size_t)r * row_bytes)[vec[u]] = val[u];
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    if (j < k) {
+                        const int r = s_row[tok[u] * k + j];
+                        if (r >= 0)
+                            reinterpret_cast<uint4 *>(x_perm + (size_t)r * row_bytes)[vec[u]] =
+                                val[u];
+                    }
                 }
             }
         }
@@ -166,6 +176,8 @@ __global__ void __launch_bounds__(256) group_tokens_kernel(
 __global__ void __launch_bounds__(256) permute_kernel(const uint8_t *__restrict__ x,
                                                       const int *__restrict__ perm, int rows, int k,
                                                       size_t row_bytes, uint8_t *x_perm) {
+    pdl_wait();
+    pdl_trigger();
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (r >= rows) return;
     const int t = perm[r] / k;
@@ -178,9 +190,8 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint8_t *__restrict_
 
 cudaError_t launch_chunk_scan(const int *idx, int T, int k, int E, int capacity, int *chunk_counts,
                               int *chunk_base, int *counts, int *offsets, cudaStream_t s) {
-    chunk_scan_kernel<<<1, 1024, 0, s>>>(idx, T, k, E, capacity, chunk_counts, chunk_base, counts,
-                                         offsets);
-    return cudaGetLastError();
+    return launch_pdl(chunk_scan_kernel, 1, 1024, 0, s, idx, T, k, E, capacity, chunk_counts,
+                      chunk_base, counts, offsets);
 }
 
 cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int *offsets,
@@ -198,19 +209,20 @@ cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int
         if (parts > rowvec) parts = rowvec > 0 ? rowvec : 1;
         if (parts < 1) parts = 1;
     }
-    group_tokens_kernel<<<dim3(nchunks, parts), 256, 0, s>>>(
-        idx, chunk_base, offsets, static_cast<const uint8_t *>(x), T, E, k, capacity,
-        (size_t)d * elt, perm, inv, static_cast<uint8_t *>(x_perm));
-    return cudaGetLastError();
+    if (k <= 2)
+        return launch_pdl(group_tokens_kernel<2>, dim3(nchunks, parts), 256, 0, s, idx,
+                          chunk_base, offsets, static_cast<const uint8_t *>(x), T, E, k, capacity,
+                          (size_t)d * elt, perm, inv, static_cast<uint8_t *>(x_perm));
+    return launch_pdl(group_tokens_kernel<MOE_MAX_TOPK>, dim3(nchunks, parts), 256, 0, s, idx,
+                      chunk_base, offsets, static_cast<const uint8_t *>(x), T, E, k, capacity,
+                      (size_t)d * elt, perm, inv, static_cast<uint8_t *>(x_perm));
 }
 
-cudaError_t launch_permute(const void *x, const int *perm, int T, int d, int k, int elt,
+cudaError_t launch_permute(const void *x, const int *perm, int rows, int d, int k, int elt,
                            void *x_perm, cudaStream_t s) {
-    const int rows = T * k;
     if (rows == 0) return cudaSuccess;
-    permute_kernel<<<(rows + 7) / 8, 256, 0, s>>>(static_cast<const uint8_t *>(x), perm, rows, k,
-                                                  (size_t)d * elt, static_cast<uint8_t *>(x_perm));
-    return cudaGetLastError();
+    return launch_pdl(permute_kernel, (rows + 7) / 8, 256, 0, s, static_cast<const uint8_t *>(x),
+                      perm, rows, k, (size_t)d * elt, static_cast<uint8_t *>(x_perm));
 }
 
 }  // namespace moe

@@ -42,6 +42,22 @@ template <> struct Vec<float> {
 constexpr int kRouterThreads = 256;
 constexpr int kRouterTokens = 2;
 
+// Selection and gates for one token, written out (KMAX >= k slots).
+template <int KMAX>
+__device__ __forceinline__ void select_and_store(const float *l, int t, int E, int k, int gating,
+                                                 int *idx, float *gates) {
+    int sel[KMAX];
+    float g[KMAX];
+    topk_gates<KMAX>(l, E, k, gating, sel, g);
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        if (j < k) {
+            idx[(size_t)t * k + j] = sel[j];
+            gates[(size_t)t * k + j] = g[j];
+        }
+    }
+}
+
 // Bias, selection, gates and outputs for one token, from its E logits.
 __device__ __forceinline__ void finish_token(float *l, const float *bias, int t, int E, int k,
                                              int gating, float *logits, int *idx, float *gates) {
@@ -49,13 +65,10 @@ __device__ __forceinline__ void finish_token(float *l, const float *bias, int t,
         l[e] += (bias != nullptr ? bias[e] : 0.f);
         logits[(size_t)t * E + e] = l[e];
     }
-    int sel[MOE_MAX_TOPK];
-    float g[MOE_MAX_TOPK];
-    topk_gates(l, E, k, gating, sel, g);
-    for (int j = 0; j < k; ++j) {
-        idx[(size_t)t * k + j] = sel[j];
-        gates[(size_t)t * k + j] = g[j];
-    }
+    if (k <= 2)
+        select_and_store<2>(l, t, E, k, gating, idx, gates);
+    else
+        select_and_store<MOE_MAX_TOPK>(l, t, E, k, gating, idx, gates);
 }
 
 // Experts are taken EG at a time (one pass over the token rows per group,
@@ -71,6 +84,8 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
     __shared__ float s_part[NW][kRouterTokens][MOE_MAX_EXPERTS];
     __shared__ float s_l[kRouterTokens][MOE_MAX_EXPERTS];
 
+    pdl_wait();
+    pdl_trigger();
     const int t0 = blockIdx.x * kRouterTokens;
     const bool has1 = t0 + 1 < Tn;
     const int nvec = d / VN;
@@ -152,17 +167,15 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
 // Selection from given logits: one thread per token.
 __global__ void __launch_bounds__(128) topk_kernel(const float *__restrict__ logits, int Tn, int E,
                                                    int k, int gating, int *idx, float *gates) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x * 128 + threadIdx.x;
     if (t >= Tn) return;
-    float l[MOE_MAX_EXPERTS];
-    for (int e = 0; e < E; ++e) l[e] = logits[(size_t)t * E + e];
-    int sel[MOE_MAX_TOPK];
-    float g[MOE_MAX_TOPK];
-    topk_gates(l, E, k, gating, sel, g);
-    for (int j = 0; j < k; ++j) {
-        idx[(size_t)t * k + j] = sel[j];
-        gates[(size_t)t * k + j] = g[j];
-    }
+    const float *l = logits + (size_t)t * E;
+    if (k <= 2)
+        select_and_store<2>(l, t, E, k, gating, idx, gates);
+    else
+        select_and_store<MOE_MAX_TOPK>(l, t, E, k, gating, idx, gates);
 }
 
 template <typename T>
@@ -174,12 +187,10 @@ cudaError_t router_dispatch(const void *x, const void *Wg, const float *bias, in
     const T *wp = static_cast<const T *>(Wg);
     // 16-byte loads in flight per thread per pass: V * (2 + EG)
     if (E <= 8)
-        router_kernel<T, 8, 2><<<grid, kRouterThreads, 0, s>>>(xp, wp, bias, T_, d, E, k, gating,
-                                                               logits, idx, gates);
-    else
-        router_kernel<T, 16, 1><<<grid, kRouterThreads, 0, s>>>(xp, wp, bias, T_, d, E, k,
-                                                                gating, logits, idx, gates);
-    return cudaGetLastError();
+        return launch_pdl(router_kernel<T, 8, 2>, grid, kRouterThreads, 0, s, xp, wp, bias, T_, d,
+                          E, k, gating, logits, idx, gates);
+    return launch_pdl(router_kernel<T, 16, 1>, grid, kRouterThreads, 0, s, xp, wp, bias, T_, d, E,
+                      k, gating, logits, idx, gates);
 }
 
 }  // namespace
@@ -197,8 +208,8 @@ cudaError_t launch_router(const void *x, const void *Wg, const float *bias, int 
 cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, int gating,
                                     int *idx, float *gates, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    topk_kernel<<<(T + 127) / 128, 128, 0, s>>>(logits, T, E, k, gating, idx, gates);
-    return cudaGetLastError();
+    return launch_pdl(topk_kernel, (T + 127) / 128, 128, 0, s, logits, T, E, k, gating, idx,
+                      gates);
 }
 
 }  // namespace moe

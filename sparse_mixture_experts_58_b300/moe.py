@@ -49,7 +49,7 @@ _sig("moe_forward_host_io", _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
 _sig("moe_router", _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp)
 _sig("moe_route_workspace_bytes", _i, _i, _i, _i, _P(_sz))
 _sig("moe_route_from_logits", _i, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp)
-_sig("moe_permute", _i, _vp, _vp, _i, _i, _i, _i, _vp, _vp)
+_sig("moe_permute", _i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp)
 _sig("moe_expert_swiglu", _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp)
 _sig("moe_down_splits", _i, _i, _i, _i, _i, _i, _i, _P(_i))
 _sig("moe_expert_down", _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp)
@@ -275,11 +275,14 @@ def route_from_logits(logits, k=2, stream=None, gating=0, capacity=0):
     return idx, gates, counts, offsets, perm[:T * k], inv[:T * k]
 
 
-def permute(x, perm, k=2, stream=None):
+def permute(x, perm, k=2, rows=None, stream=None):
+    """x_perm[r] = x[perm[r] // k] for r < rows (default T*k; the kept count
+    under a capacity limit).  x_perm has T*k rows."""
     T, d = x.shape
+    rows = T * k if rows is None else int(rows)
     x_perm = torch.empty(T * k, d, dtype=x.dtype, device=x.device)
-    _check(_lib.moe_permute(_ptr(x), _ptr(perm), T, d, k, _dt(x), _ptr(x_perm), _stream(stream)),
-           "moe_permute")
+    _check(_lib.moe_permute(_ptr(x), _ptr(perm), rows, T, d, k, _dt(x), _ptr(x_perm),
+                            _stream(stream)), "moe_permute")
     return x_perm
 
 
