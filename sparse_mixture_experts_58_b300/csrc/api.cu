@@ -233,6 +233,10 @@ int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p) {
         if (s > kblocks) s = kblocks;
         q.kps = (kblocks + (int)s - 1) / (int)s;
         q.splits = (kblocks + q.kps - 1) / q.kps;
+        // wide tiles run on CTA pairs (MOE_PLAN_PAIR=0|1 overrides)
+        q.pair = 0;
+        if (const char *pp = getenv("MOE_PLAN_PAIR")) q.pair = atoi(pp) != 0;
+        if (!q.wide || q.bm != 128) q.pair = 0;
     }
     const int elt = elem_size(dt);
     size_t off = 0;
@@ -314,12 +318,21 @@ int run_forward(const Plan &P, const Options &O, const void *x, const void *W_g,
                                           perm, inv, x_perm, s))) != MOE_OK)
         return rc;
     if (P.dt == MOE_BF16) {
-        if ((rc = launch_swiglu_tc(x_perm, offsets, W1, W3, P.rows, P.d, P.ffn, P.E, P.bm, P.wide,
-                                   h, s)) != MOE_OK)
-            return rc;
-        if ((rc = launch_down_tc(h, offsets, W2, P.rows, P.d, P.ffn, P.E, P.bm, P.wide, P.splits,
-                                 P.kps, y, s)) != MOE_OK)
-            return rc;
+        if (P.pair) {
+            if ((rc = launch_swiglu_pair(x_perm, offsets, W1, W3, P.rows, P.d, P.ffn, P.E, h,
+                                         s)) != MOE_OK)
+                return rc;
+            if ((rc = launch_down_pair(h, offsets, W2, P.rows, P.d, P.ffn, P.E, P.splits, P.kps,
+                                       y, s)) != MOE_OK)
+                return rc;
+        } else {
+            if ((rc = launch_swiglu_tc(x_perm, offsets, W1, W3, P.rows, P.d, P.ffn, P.E, P.bm,
+                                       P.wide, h, s)) != MOE_OK)
+                return rc;
+            if ((rc = launch_down_tc(h, offsets, W2, P.rows, P.d, P.ffn, P.E, P.bm, P.wide,
+                                     P.splits, P.kps, y, s)) != MOE_OK)
+                return rc;
+        }
     } else {
         if ((rc = cuda_rc(launch_swiglu_f32(static_cast<const float *>(x_perm), offsets, W1, W3,
                                             P.rows, P.d, P.ffn, P.E, static_cast<float *>(h),
@@ -554,6 +567,7 @@ int moe_expert_swiglu(const void *x_perm, const int *offsets, const void *const 
         Plan P;
         const int k = (rows % 2 == 0 && E >= 2) ? 2 : 1;
         if ((rc = make_plan(rows / k, d, ffn, E, k, dtype, &P)) != MOE_OK) return rc;
+        if (P.pair) return launch_swiglu_pair(x_perm, offsets, W1, W3, rows, d, ffn, E, h, s);
         return launch_swiglu_tc(x_perm, offsets, W1, W3, rows, d, ffn, E, P.bm, P.wide, h, s);
     }
     return cuda_rc(launch_swiglu_f32(static_cast<const float *>(x_perm), offsets, W1, W3, rows, d,
@@ -572,8 +586,10 @@ int moe_expert_down(const void *h, const int *offsets, const void *const *W2, in
     if (!aligned16(h) || !aligned16(y_partial)) return MOE_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == MOE_BF16)
-        return launch_down_tc(h, offsets, W2, P.rows, d, ffn, E, P.bm, P.wide, P.splits, P.kps,
-                              y_partial, s);
+        return P.pair ? launch_down_pair(h, offsets, W2, P.rows, d, ffn, E, P.splits, P.kps,
+                                         y_partial, s)
+                      : launch_down_tc(h, offsets, W2, P.rows, d, ffn, E, P.bm, P.wide, P.splits,
+                                       P.kps, y_partial, s);
     return cuda_rc(launch_down_f32(static_cast<const float *>(h), offsets, W2, P.rows, d, ffn, E,
                                    y_partial, s));
 }
