@@ -73,8 +73,20 @@ def rank_token_seed(base_seed: int, rank: int) -> int:
 # ---------------------------------------------------------------- peaks, clocks
 
 GEMM_SOURCES = ("sparse_mixture_experts_58_b300/csrc/gemm_tc.cu",
+                "sparse_mixture_experts_58_b300/csrc/gemm_pair.cu",
                 "sparse_mixture_experts_58_b300/csrc/ptx.cuh",
                 "sparse_mixture_experts_58_b300/csrc/common.cuh")
+
+
+def uses_pairs(T, k, E) -> bool:
+    """Whether the library's tile plan runs the expert GEMMs on CTA pairs
+    (at least 128 rows per expert on average, unless overridden)."""
+    wide = (T * k) // E >= 128
+    if os.environ.get("MOE_PLAN_WIDE"):
+        wide = int(os.environ["MOE_PLAN_WIDE"]) != 0
+    if os.environ.get("MOE_PLAN_PAIR"):
+        return int(os.environ["MOE_PLAN_PAIR"]) != 0
+    return wide
 
 
 def gemm_source_hash() -> str:
@@ -332,6 +344,9 @@ def measure(args, rank, world, local):
     if cap:
         overrides.append(f"capacity factor {args.capacity_factor} -> {cap} rows/expert, "
                          f"dropped mass {'renormalised' if policy else 'lost'}")
+    for var in ("MOE_PLAN_WIDE", "MOE_PLAN_PAIR", "MOE_PLAN_SPLITS", "MOE_PDL"):
+        if os.environ.get(var):
+            overrides.append(f"{var}={os.environ[var]}")
     workload = WORKLOAD_NAMES[args.config]
     if overrides:
         workload = f"{workload} ({'; '.join(overrides)})"
@@ -484,7 +499,8 @@ def measure(args, rank, world, local):
             "rows_computed": rows_kept, "routing": route_kw,
         },
         "roofline": {
-            "kernel": "grouped gate/up GEMM + SwiGLU (tcgen05)",
+            "kernel": "grouped gate/up GEMM + SwiGLU (tcgen05, "
+                      + ("CTA pairs, tokens as N)" if uses_pairs(T, k, E) else "one CTA per tile)"),
             "bound": g_bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "peak_source": f"{peak_src} (burst)",
             "traffic": None if overrides else recorded_traffic(f"gate_up_{args.config}"),

@@ -216,27 +216,33 @@ int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p) {
         q.wide = rows_per_expert >= 128 ? 1 : 0;
         q.bm = T >= 128 ? 128 : ((T + 7) / 8) * 8;
         if (q.bm < 8) q.bm = 8;
-        const int NB = q.wide ? 256 : 128;
+        // tuning overrides (measurement only): MOE_PLAN_WIDE=0|1, MOE_PLAN_PAIR=0|1,
+        // MOE_PLAN_SPLITS=n
+        if (const char *w = getenv("MOE_PLAN_WIDE")) q.wide = atoi(w) != 0;
+        // many rows per expert: CTA pairs with the tokens as the MMA's N side
+        q.pair = q.wide;
+        if (const char *pp = getenv("MOE_PLAN_PAIR")) q.pair = atoi(pp) != 0;
         const int kblocks = (ffn + kBlockK - 1) / kBlockK;
         const long long busy = q.rows < E ? q.rows : E;
-        const long long mtiles = q.wide ? (q.rows + q.bm - 1) / q.bm : busy;
-        const long long ntiles = (d + NB - 1) / NB;
-        const long long base_units = mtiles * ntiles;
-        long long s = base_units > 0 ? (8LL * kPlanSms + base_units - 1) / base_units : 1;
+        long long s = 1;
+        if (q.pair) {
+            // down-projection units: 256 features x one token tile of <= 256
+            // rows; split the contraction until each pair has about 4 units
+            const long long ttiles = busy > (q.rows + 255) / 256 ? busy : (q.rows + 255) / 256;
+            const long long base_units = ttiles * ((d + 255) / 256);
+            s = (4LL * (kPlanSms / 2) + base_units - 1) / base_units;
+        } else if (!q.wide) {
+            // one 128-feature x 128-row tile per busy expert; about 8 units per SM
+            const long long base_units = busy * ((d + 127) / 128);
+            s = base_units > 0 ? (8LL * kPlanSms + base_units - 1) / base_units : 1;
+        }
         const long long smax = kblocks / 8 > 0 ? kblocks / 8 : 1;
         if (s > smax) s = smax;
         if (s < 1) s = 1;
-        if (q.wide) s = 1;
-        // tuning overrides (measurement only): MOE_PLAN_WIDE=0|1, MOE_PLAN_SPLITS=n
-        if (const char *w = getenv("MOE_PLAN_WIDE")) q.wide = atoi(w) != 0;
         if (const char *sp = getenv("MOE_PLAN_SPLITS")) s = atoi(sp) > 0 ? atoi(sp) : s;
         if (s > kblocks) s = kblocks;
         q.kps = (kblocks + (int)s - 1) / (int)s;
         q.splits = (kblocks + q.kps - 1) / q.kps;
-        // wide tiles run on CTA pairs (MOE_PLAN_PAIR=0|1 overrides)
-        q.pair = 0;
-        if (const char *pp = getenv("MOE_PLAN_PAIR")) q.pair = atoi(pp) != 0;
-        if (!q.wide || q.bm != 128) q.pair = 0;
     }
     const int elt = elem_size(dt);
     size_t off = 0;

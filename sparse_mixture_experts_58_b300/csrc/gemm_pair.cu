@@ -1,17 +1,23 @@
-// Grouped expert GEMMs on CTA pairs: a cluster of two CTAs on neighbouring
-// SMs computes one 256-row x 256-column tile with tcgen05 .cta_group::2.
+// Grouped expert GEMMs on CTA pairs with the tokens as the MMA's N side.
 //
-// Same operation and work units as gemm_tc.cu (gate/up with the SwiGLU
-// epilogue, or the down projection), for the many-rows-per-expert regime:
-//   - each CTA holds 128 token rows (A) and half of the 256 weight rows (B):
-//     for gate/up CTA 0 holds the W1 rows and CTA 1 the W3 rows of the same
-//     128 features, for down each holds 128 of the 256 output rows;
-//   - the even CTA issues the MMAs; the tensor cores read A and B from both
-//     CTAs' shared memory and each CTA's tensor memory receives its own 128
-//     rows of the fp32 accumulator.
-// Per CTA and 64-deep contraction step that is 32 KB of operands instead of
-// 48 KB for a single-CTA 128 x 256 tile, so six pipeline stages fit in shared
-// memory and each SM streams a third fewer bytes per FLOP.
+// Same operation as gemm_tc.cu (gate/up with the SwiGLU epilogue, or the down
+// projection), organised for tensor-core efficiency when experts hold many
+// rows:
+//   - a cluster of two CTAs on neighbouring SMs issues tcgen05 .cta_group::2
+//     MMAs of M = 256 weight rows (128 in each CTA's shared memory) by
+//     N = up to 256 token rows (half in each CTA);
+//   - an expert's rows are cut into ceil(cnt / 256) token tiles of equal size
+//     rounded up to 16, the MMA's N granularity, so at most 15 padded rows per
+//     tile reach the tensor cores (a 128- or 256-row M tile pads up to 127 or
+//     255 at each expert's tail);
+//   - gate/up: each CTA's 128 weight rows are 64 rows of W1 and the same 64
+//     rows of W3 (two TMA boxes), so the gate of feature f sits in
+//     accumulator lane f and its up value in lane 64 + f, in another warp's
+//     quarter; the two warps swap half of each 32-token chunk through shared
+//     memory and each finishes silu(u) * v for 16 of the tokens;
+//   - down: each CTA holds 128 of the pair's 256 output features.
+// The accumulator is feature-major (lane = feature, column = token), so the
+// epilogue writes, per token, 32 consecutive features from one warp.
 //
 // Barriers (same offsets in both CTAs):
 //   full[s]      even CTA only: one arrival with the stage's byte count from
@@ -31,53 +37,74 @@
 namespace moe {
 namespace {
 
-constexpr int kPairM = 256;
-constexpr int kHalfM = 128;
-constexpr int kNB = 256;
-constexpr int kHalfN = 128;
+constexpr int kPairM = 256;        // weight rows per pair tile
+constexpr int kHalfM = 128;        // weight rows per CTA
+constexpr int kMaxTok = 256;       // token rows per tile (MMA N)
+constexpr int kTokMaps = kMaxTok / 16;  // token tensor maps, box heights 8, 16, ..., 128
+constexpr int kGate = kHalfM / 2;  // gate/up: W1 rows, then the same rows of W3, per CTA
 constexpr int kStages = 6;
 constexpr int kMaxE = MOE_MAX_EXPERTS;
 constexpr int kThreads = 192;
-constexpr int kABytes = kHalfM * 128;
-constexpr int kBBytes = kHalfN * 128;
+constexpr int kABytes = kHalfM * 128;       // weights, 64-wide contraction slice
+constexpr int kBBytes = (kMaxTok / 2) * 128;  // tokens, this CTA's half
 constexpr int kRing = kStages * (kABytes + kBBytes);
-constexpr int kBars = (2 * kStages + 6) * 8;
-constexpr int kMisc = 16 + 4 * (3 * kMaxE + 2);
-constexpr size_t kSmem = 1024 + kRing + kBars + kMisc;
-constexpr uint32_t kTmemCols = 2 * kNB;
+// gate/up exchange: [warp pair 2][chunk parity 2][direction 2][16 tokens][32 lanes] fp32
+constexpr int kXchFloats = 16 * 32;
+constexpr int kXch = 2 * 2 * 2 * kXchFloats * 4;
+constexpr int kBars = (2 * kStages + 8) * 8;
+constexpr int kMisc = 16 + 4 * (4 * kMaxE + 2);
+constexpr size_t kSmem = 1024 + kRing + kXch + kBars + kMisc;
+constexpr uint32_t kAccCols = kMaxTok;
+constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr int kAccEmptyArrivals = 8;  // lane 0 of the 4 epilogue warps of each CTA
 constexpr uint16_t kBothCtas = 0x3;
 
 struct PairArgs {
-    CUtensorMap mapA;          // token rows [rows][K] bf16, box {64, 128}
-    CUtensorMap mapB0[kMaxE];  // W1[e] (gate/up) or W2[e] (down): [N][K], box {64, 128}
-    CUtensorMap mapB1[kMaxE];  // W3[e] (gate/up only)
-    const int *offsets;        // [E + 1]
-    void *out;                 // h bf16 [rows][N]  or  y fp32 [splits][rows][N]
+    CUtensorMap mapTok[kTokMaps];  // token rows [rows][K] bf16; map i has box {64, 8 (i + 1)}
+    CUtensorMap mapW0[kMaxE];      // W1[e] (gate/up, box {64, 64}) or W2[e] (down, box {64, 128})
+    CUtensorMap mapW1[kMaxE];      // W3[e] (gate/up only, box {64, 64})
+    const int *offsets;            // [E + 1]
+    void *out;                     // h bf16 [rows][N]  or  y fp32 [splits][rows][N]
     int *status;
     unsigned long long wait_limit_ns;
     int E, rows, K, N, kblocks, kps, splits;
 };
 
 struct PairUnit {
-    int e, row0, nrows, n0, ks, kb0, kb1;  // row0 / nrows: the pair's 256-row tile
+    int e;       // expert
+    int t0;      // first token row of the tile (row of x_perm / h)
+    int nvalid;  // token rows in the tile
+    int ntok;    // MMA N: nvalid rounded up to 16
+    int n0;      // first output feature of the pair's tile
+    int ks, kb0, kb1;  // contraction split and its 64-wide blocks
 };
 
-__device__ __forceinline__ PairUnit decode_pair_unit(int u, const int *s_off, const int *s_mt,
-                                                     const int *s_ustart, const PairArgs &a,
-                                                     int NOUT) {
-    int e = 0;
-    while (e + 1 < a.E && u >= s_ustart[e + 1]) ++e;
+// Units are ordered expert -> feature tile -> split -> token tile, so the
+// pairs running together share one weight tile through L2.
+__device__ __forceinline__ PairUnit decode_pair_unit(int u, const int *s_off, const int *s_ntt,
+                                                     const int *s_nt, const int *s_ustart,
+                                                     const PairArgs &a, int NOUT) {
+    int lo = 0, hi = a.E - 1;
+    while (lo < hi) {  // last expert whose first unit is <= u (experts with no units share it)
+        const int mid = (lo + hi + 1) >> 1;
+        if (u >= s_ustart[mid])
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int e = lo;
     const int local = u - s_ustart[e];
-    const int mtn = s_mt[e];
-    const int mt = local % mtn;
-    const int rest = local / mtn;
+    const int ntt = s_ntt[e];
+    const int tt = local % ntt;
+    const int rest = local / ntt;
     PairUnit w;
     w.e = e;
     w.ks = rest % a.splits;
     w.n0 = (rest / a.splits) * NOUT;
-    w.row0 = s_off[e] + mt * kPairM;
-    w.nrows = min(kPairM, s_off[e + 1] - w.row0);
+    const int tl = tt * s_nt[e];
+    w.t0 = s_off[e] + tl;
+    w.nvalid = min(s_nt[e], s_off[e + 1] - s_off[e] - tl);
+    w.ntok = max(16, (w.nvalid + 15) & ~15);
     w.kb0 = w.ks * a.kps;
     w.kb1 = min(w.kb0 + a.kps, a.kblocks);
     return w;
@@ -86,26 +113,28 @@ __device__ __forceinline__ PairUnit decode_pair_unit(int u, const int *s_off, co
 template <bool SWIGLU>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_pair(const __grid_constant__ PairArgs a) {
-    constexpr int NOUT = SWIGLU ? kHalfN : kNB;
-    constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kPairM, kNB);
+    constexpr int NOUT = SWIGLU ? kPairM / 2 : kPairM;  // output features per pair tile
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + kStages * kABytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRing);
+    float *xch = reinterpret_cast<float *>(smem + kRing);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRing + kXch);
     uint64_t *empty = full + kStages;
     uint64_t *acc_full = empty + kStages;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *drain = acc_empty + 2;
     uint64_t *bye = drain + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bye + 1);
+    uint64_t *xbar = bye + 1;  // [2] gate/up exchange, one per epilogue warp pair
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xbar + 2);
     volatile int *s_abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *s_bye_ok = reinterpret_cast<volatile int *>(tmem_slot + 2);
     int *s_off = reinterpret_cast<int *>(tmem_slot + 4);  // [kMaxE + 1]
-    int *s_mt = s_off + kMaxE + 1;                         // [kMaxE]
-    int *s_ustart = s_mt + kMaxE;                          // [kMaxE + 1]
+    int *s_ntt = s_off + kMaxE + 1;                        // [kMaxE] token tiles
+    int *s_nt = s_ntt + kMaxE;                             // [kMaxE] rows per token tile
+    int *s_ustart = s_nt + kMaxE;                          // [kMaxE + 1]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = ptx::cluster_ctarank();
@@ -124,6 +153,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         ptx::mbar_init(drain, 1);
         ptx::mbar_init(bye, 1);
+        ptx::mbar_init(&xbar[0], 2);
+        ptx::mbar_init(&xbar[1], 2);
         *s_abort = 0;
         *s_bye_ok = 0;
         ptx::fence_barrier_init();
@@ -132,7 +163,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::tmem_alloc_pair(tmem_slot, kTmemCols);
         ptx::tmem_relinquish_pair();
     }
-    if (warp == 0 && lane == 0) ptx::prefetch_tensormap(&a.mapA);
+    if (warp == 0 && lane == 0) {
+        for (int i = 0; i < kTokMaps; ++i) ptx::prefetch_tensormap(&a.mapTok[i]);
+    }
     pdl_wait();
     pdl_trigger();
     if (threadIdx.x <= E) s_off[threadIdx.x] = a.offsets[threadIdx.x];
@@ -145,10 +178,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int acc = 0;
         for (int e = 0; e < E; ++e) {
             const int cnt = s_off[e + 1] - s_off[e];
-            const int mt = cnt > 0 ? (cnt + kPairM - 1) / kPairM : 0;
-            s_mt[e] = mt;
+            int ntt = 0, nt = 16;
+            if (cnt > 0) {
+                const int t0 = (cnt + kMaxTok - 1) / kMaxTok;
+                nt = (((cnt + t0 - 1) / t0) + 15) & ~15;  // <= kMaxTok
+                ntt = (cnt + nt - 1) / nt;
+            }
+            s_ntt[e] = ntt;
+            s_nt[e] = nt;
             s_ustart[e] = acc;
-            acc += mt * NT * a.splits;
+            acc += ntt * NT * a.splits;
         }
         s_ustart[E] = acc;
     }
@@ -162,17 +201,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ producers
         if (lane == 0) {
             const uint32_t full0 = ptx::map_to_rank(ptx::smem_addr(&full[0]), 0);
-            const uint32_t tx_bytes = 2u * (kABytes + kBBytes);
             int stage = 0;
             uint32_t ph = 0;
             int issued = 0;
             bool ok = true;
             for (int u = first; ok && u < total; u += stride) {
-                const PairUnit w = decode_pair_unit(u, s_off, s_mt, s_ustart, a, NOUT);
-                const CUtensorMap *mb =
-                    (SWIGLU && !even) ? &a.mapB1[w.e] : &a.mapB0[w.e];
-                const int brow = SWIGLU ? w.n0 : w.n0 + static_cast<int>(rank) * kHalfN;
-                const int arow = w.row0 + static_cast<int>(rank) * kHalfM;
+                const PairUnit w = decode_pair_unit(u, s_off, s_ntt, s_nt, s_ustart, a, NOUT);
+                const int half = w.ntok >> 1;  // token rows this CTA supplies
+                const CUtensorMap *mt = &a.mapTok[(half >> 3) - 1];
+                const uint32_t tx_bytes = 2u * kABytes + static_cast<uint32_t>(w.ntok) * 128u;
+                const int trow = w.t0 + static_cast<int>(rank) * half;
+                const int wrow = w.n0 + static_cast<int>(rank) * (SWIGLU ? kGate : kHalfM);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!ptx::mbar_wait_bounded(&empty[stage], ph ^ 1u, s_abort, a.status,
                                                 kStatusProducerWait, a.wait_limit_ns)) {
@@ -181,8 +220,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     if (even) ptx::mbar_arrive_expect_tx(&full[stage], tx_bytes);
                     const uint32_t fb = full0 + static_cast<uint32_t>(stage) * 8u;
-                    ptx::tma_load_2d_pair(sA + stage * kABytes, &a.mapA, kb * kBlockK, arow, fb);
-                    ptx::tma_load_2d_pair(sB + stage * kBBytes, mb, kb * kBlockK, brow, fb);
+                    uint8_t *dA = sA + stage * kABytes;
+                    const int kx = kb * kBlockK;
+                    if (SWIGLU) {
+                        ptx::tma_load_2d_pair(dA, &a.mapW0[w.e], kx, wrow, fb);
+                        ptx::tma_load_2d_pair(dA + kGate * 128, &a.mapW1[w.e], kx, wrow, fb);
+                    } else {
+                        ptx::tma_load_2d_pair(dA, &a.mapW0[w.e], kx, wrow, fb);
+                    }
+                    ptx::tma_load_2d_pair(sB + stage * kBBytes, mt, kx, trow, fb);
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;
@@ -212,7 +258,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int it = 0;
             bool ok = true;
             for (int u = first; ok && u < total; u += stride, ++it) {
-                const PairUnit w = decode_pair_unit(u, s_off, s_mt, s_ustart, a, NOUT);
+                const PairUnit w = decode_pair_unit(u, s_off, s_ntt, s_nt, s_ustart, a, NOUT);
+                const uint32_t idesc = ptx::idesc_bf16_f32(kPairM, w.ntok);
                 const int acc = it & 1;
                 const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
                 if (!ptx::mbar_wait_bounded(&acc_empty[acc], aph ^ 1u, s_abort, a.status,
@@ -221,7 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 }
                 ptx::tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kNB);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * kAccCols;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!ptx::mbar_wait_bounded(&full[stage], ph, s_abort, a.status,
                                                 kStatusMmaWait, a.wait_limit_ns)) {
@@ -234,7 +281,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 16; ++kk) {
                         ptx::mma_bf16_pair(d_tmem, ptx::desc_kmajor_sw128(a0 + kk * 32),
-                                           ptx::desc_kmajor_sw128(b0 + kk * 32), kIdesc,
+                                           ptx::desc_kmajor_sw128(b0 + kk * 32), idesc,
                                            (kb > w.kb0 || kk > 0) ? 1u : 0u);
                     }
                     ptx::mma_commit_pair_multicast(&empty[stage], kBothCtas);
@@ -253,69 +300,77 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;  // tensor-memory lanes 32*quad .. +31
-        const int r = quad * 32 + lane;
         const uint32_t acc_empty0 = ptx::map_to_rank(ptx::smem_addr(&acc_empty[0]), 0);
+        // gate/up: quarters 0 and 1 hold the gate values of features 0-31 and
+        // 32-63, quarters 2 and 3 the up values of the same features
+        const int pairq = quad & 1;
+        const bool is_up = quad >= 2;
+        float *xb = xch + pairq * (2 * 2 * kXchFloats);
+        uint32_t xk = 0;  // exchanges done by this warp pair
+        bool ok = true;
         int it = 0;
-        for (int u = first; u < total; u += stride, ++it) {
-            const PairUnit w = decode_pair_unit(u, s_off, s_mt, s_ustart, a, NOUT);
+        for (int u = first; ok && u < total; u += stride, ++it) {
+            const PairUnit w = decode_pair_unit(u, s_off, s_ntt, s_nt, s_ustart, a, NOUT);
             const int acc = it & 1;
             const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
             if (!ptx::mbar_wait_bounded(&acc_full[acc], aph, s_abort, a.status,
                                         kStatusEpilogueWait, a.wait_limit_ns))
                 break;
             ptx::tc_fence_after_sync();
-            const int hrow0 = w.row0 + static_cast<int>(rank) * kHalfM;
-            const int hrows = max(0, min(kHalfM, w.nrows - static_cast<int>(rank) * kHalfM));
             const uint32_t tb = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                static_cast<uint32_t>(acc * kNB);
-            if (quad * 32 < hrows) {
-                const bool row_ok = r < hrows;
-                if (SWIGLU) {
-                    __nv_bfloat16 *hrow =
-                        static_cast<__nv_bfloat16 *>(a.out) + (size_t)(hrow0 + r) * a.N + w.n0;
+                                static_cast<uint32_t>(acc) * kAccCols;
+            if (SWIGLU) {
+                // the gate warp finishes each chunk's first 16 tokens, the up
+                // warp the last 16; each sends the other the values it needs
+                const int f = w.n0 + static_cast<int>(rank) * kGate + pairq * 32 + lane;
+                __nv_bfloat16 *hcol = static_cast<__nv_bfloat16 *>(a.out) + f;
+                const bool f_ok = f < a.N;
 #pragma unroll 1
-                    for (int c = 0; c < kHalfN; c += 32) {
-                        uint32_t U[32], V[32];
-                        ptx::tmem_ld_32x32b_x32(tb + c, U);
-                        ptx::tmem_ld_32x32b_x32(tb + kHalfN + c, V);
-                        ptx::tmem_ld_wait();
-                        if (row_ok && w.n0 + c < a.N) {
-                            uint32_t packed[16];
+                for (int j0 = 0; j0 < w.ntok; j0 += 32) {
+                    uint32_t V[32];
+                    ptx::tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(j0), V);
+                    ptx::tmem_ld_wait();
+                    float *buf = xb + (xk & 1u) * (2 * kXchFloats);
+                    float *send = buf + (is_up ? kXchFloats : 0);
+                    const float *recv = buf + (is_up ? 0 : kXchFloats);
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const float u0 = __uint_as_float(U[2 * i]);
-                                const float u1 = __uint_as_float(U[2 * i + 1]);
-                                const float v0 = __uint_as_float(V[2 * i]);
-                                const float v1 = __uint_as_float(V[2 * i + 1]);
-                                const float h0 = u0 / (1.f + expf(-u0)) * v0;
-                                const float h1 = u1 / (1.f + expf(-u1)) * v1;
-                                const __nv_bfloat162 p = __floats2bfloat162_rn(h0, h1);
-                                packed[i] = *reinterpret_cast<const uint32_t *>(&p);
-                            }
-                            uint4 *dst = reinterpret_cast<uint4 *>(hrow + c);
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1],
-                                                    packed[4 * q + 2], packed[4 * q + 3]);
-                        }
+                    for (int i = 0; i < 16; ++i)
+                        send[i * 32 + lane] = __uint_as_float(is_up ? V[i] : V[16 + i]);
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&xbar[pairq]);
+                    if (!ptx::mbar_wait_bounded(&xbar[pairq], xk & 1u, s_abort, a.status,
+                                                kStatusEpilogueWait, a.wait_limit_ns)) {
+                        ok = false;
+                        break;
                     }
-                } else {
-                    float *yrow = static_cast<float *>(a.out) +
-                                  ((size_t)w.ks * a.rows + hrow0 + r) * a.N + w.n0;
-#pragma unroll 1
-                    for (int c = 0; c < kNB; c += 32) {
-                        uint32_t Y[32];
-                        ptx::tmem_ld_32x32b_x32(tb + c, Y);
-                        ptx::tmem_ld_wait();
-                        if (row_ok && w.n0 + c < a.N) {
-                            float4 *dst = reinterpret_cast<float4 *>(yrow + c);
+                    ++xk;
+                    const int jb = j0 + (is_up ? 16 : 0);
 #pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                dst[q] = make_float4(__uint_as_float(Y[4 * q]),
-                                                     __uint_as_float(Y[4 * q + 1]),
-                                                     __uint_as_float(Y[4 * q + 2]),
-                                                     __uint_as_float(Y[4 * q + 3]));
-                        }
+                    for (int i = 0; i < 16; ++i) {
+                        const float other = recv[i * 32 + lane];
+                        const float g = is_up ? other : __uint_as_float(V[i]);
+                        const float v = is_up ? __uint_as_float(V[16 + i]) : other;
+                        const int j = jb + i;
+                        if (f_ok && j < w.nvalid)
+                            hcol[(size_t)(w.t0 + j) * a.N] =
+                                __float2bfloat16_rn(g / (1.f + expf(-g)) * v);
+                    }
+                }
+                if (!ok) break;
+            } else {
+                const int f = w.n0 + static_cast<int>(rank) * kHalfM + quad * 32 + lane;
+                float *ycol = static_cast<float *>(a.out) + (size_t)w.ks * a.rows * a.N + f;
+                const bool f_ok = f < a.N;
+#pragma unroll 1
+                for (int j0 = 0; j0 < w.ntok; j0 += 32) {
+                    uint32_t Y[32];
+                    ptx::tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(j0), Y);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int j = j0 + i;
+                        if (f_ok && j < w.nvalid)
+                            ycol[(size_t)(w.t0 + j) * a.N] = __uint_as_float(Y[i]);
                     }
                 }
             }
@@ -377,8 +432,9 @@ int run_pair(PairArgs &args, int units_bound, cudaStream_t s) {
                : MOE_ERR_CUDA;
 }
 
-int fill_pair(PairArgs &args, const void *A, const int *offsets, void *out, int rows, int K, int N,
-              int E) {
+// Token maps (one per tile height), shapes and the status word.
+int fill_pair(PairArgs &args, const void *tokens, const int *offsets, void *out, int rows, int K,
+              int N, int E) {
     args.offsets = offsets;
     args.out = out;
     args.E = E;
@@ -389,8 +445,15 @@ int fill_pair(PairArgs &args, const void *A, const int *offsets, void *out, int 
     args.wait_limit_ns = kWaitLimitNs;
     args.status = device_status_ptr();
     if (args.status == nullptr) return MOE_ERR_CUDA;
-    return encode_map_bf16_2d(&args.mapA, A, K, rows, kBlockK, kHalfM);
+    for (int i = 0; i < kTokMaps; ++i) {
+        const int rc = encode_map_bf16_2d(&args.mapTok[i], tokens, K, rows, kBlockK, 8 * (i + 1));
+        if (rc != MOE_OK) return rc;
+    }
+    return MOE_OK;
 }
+
+// Upper bound on the token tiles of all experts together.
+int token_tiles_bound(int rows, int E) { return (rows + kMaxTok - 1) / kMaxTok + E; }
 
 }  // namespace
 
@@ -404,16 +467,15 @@ int launch_swiglu_pair(const void *x_perm, const int *offsets, const void *const
     int rc = fill_pair(args, x_perm, offsets, h, rows, d, ffn, E);
     if (rc != MOE_OK) return rc;
     for (int e = 0; e < E; ++e) {
-        if ((rc = encode_map_bf16_2d(&args.mapB0[e], W1[e], d, ffn, kBlockK, kHalfN)) != MOE_OK)
+        if ((rc = encode_map_bf16_2d(&args.mapW0[e], W1[e], d, ffn, kBlockK, kGate)) != MOE_OK)
             return rc;
-        if ((rc = encode_map_bf16_2d(&args.mapB1[e], W3[e], d, ffn, kBlockK, kHalfN)) != MOE_OK)
+        if ((rc = encode_map_bf16_2d(&args.mapW1[e], W3[e], d, ffn, kBlockK, kGate)) != MOE_OK)
             return rc;
     }
     args.splits = 1;
     args.kps = args.kblocks;
-    const int NT = (ffn + kHalfN - 1) / kHalfN;
-    const int units_bound = ((rows + kPairM - 1) / kPairM + E) * NT;
-    return run_pair<true>(args, units_bound, s);
+    const int NT = (ffn + kPairM / 2 - 1) / (kPairM / 2);
+    return run_pair<true>(args, token_tiles_bound(rows, E) * NT, s);
 }
 
 int launch_down_pair(const void *h, const int *offsets, const void *const *W2, int rows, int d,
@@ -423,13 +485,12 @@ int launch_down_pair(const void *h, const int *offsets, const void *const *W2, i
     int rc = fill_pair(args, h, offsets, y, rows, ffn, d, E);
     if (rc != MOE_OK) return rc;
     for (int e = 0; e < E; ++e)
-        if ((rc = encode_map_bf16_2d(&args.mapB0[e], W2[e], ffn, d, kBlockK, kHalfN)) != MOE_OK)
+        if ((rc = encode_map_bf16_2d(&args.mapW0[e], W2[e], ffn, d, kBlockK, kHalfM)) != MOE_OK)
             return rc;
     args.splits = splits;
     args.kps = kps;
-    const int NT = (d + kNB - 1) / kNB;
-    const int units_bound = ((rows + kPairM - 1) / kPairM + E) * NT * splits;
-    return run_pair<false>(args, units_bound, s);
+    const int NT = (d + kPairM - 1) / kPairM;
+    return run_pair<false>(args, token_tiles_bound(rows, E) * NT * splits, s);
 }
 
 }  // namespace moe

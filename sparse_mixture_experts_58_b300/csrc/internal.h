@@ -20,7 +20,7 @@ struct Plan {
     int nchunks;   // router chunks of kChunk tokens
     // grouped expert GEMMs (bf16 tensor-core path)
     int wide;      // 1: 256-wide tiles (many rows per expert); 0: 128-wide
-    int pair;      // 1: wide tiles on CTA pairs (256 token rows per tile)
+    int pair;      // 1: CTA pairs, 256 weight rows x up to 256 token rows per tile
     int bm;        // token rows per tile (<= 128)
     int splits;    // split of the down projection's contraction
     int kps;       // 64-wide contraction blocks per split
@@ -84,7 +84,7 @@ int launch_swiglu_tc(const void *x_perm, const int *offsets, const void *const *
 int launch_down_tc(const void *h, const int *offsets, const void *const *W2, int rows, int d,
                    int ffn, int E, int bm, int wide, int splits, int kps, float *y,
                    cudaStream_t s);
-// The same on CTA pairs (256-row x 256-column tiles; wide tiles only).
+// The same on CTA pairs: 256 weight rows x up to 256 tokens (rounded to 16) per tile.
 int launch_swiglu_pair(const void *x_perm, const int *offsets, const void *const *W1,
                        const void *const *W3, int rows, int d, int ffn, int E, void *h,
                        cudaStream_t s);

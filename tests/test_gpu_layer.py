@@ -77,6 +77,21 @@ def test_small_layers(moe, T, d, ffn, E, k, dtype):
     check_layer(moe, x, layer, k, dtype=dtype, label=f"T{T} d{d} ffn{ffn} E{E} k{k} {dtype}")
 
 
+@pytest.mark.parametrize("T,d,ffn,E,k", [
+    (16, 256, 448, 8, 2),
+    (129, 128, 256, 8, 2),
+    (700, 192, 384, 8, 2),
+    (1500, 128, 192, 4, 3),
+])
+@pytest.mark.parametrize("pair", ["0", "1"], ids=["one_cta", "pair"])
+def test_small_layers_forced_tile_plan(moe, monkeypatch, T, d, ffn, E, k, pair):
+    """The whole layer with the CTA-pair GEMMs forced off and on, on shapes
+    the automatic plan sends to the other kernel as well."""
+    monkeypatch.setenv("MOE_PLAN_PAIR", pair)
+    x, layer = inputs.make_workload(T, d, ffn, E, k, "bf16", seed=T + 7, device="cuda")
+    check_layer(moe, x, layer, k, dtype="bf16", label=f"T{T} E{E} k{k} pair={pair}")
+
+
 def test_empty_batch(moe):
     x, layer = inputs.make_workload(0, 128, 256, 8, 2, "bf16", 0, "cuda")
     out = moe.forward(x, layer.Wg, layer.W1, layer.W3, layer.W2, 2)

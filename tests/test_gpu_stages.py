@@ -126,8 +126,14 @@ def _torch_swiglu_rows(x_perm, offsets, W1, W3):
     (700, 192, 384, 8, False),     # wide tiles (175 rows/expert), ragged rows
     (1024, 256, 512, 8, True),     # skewed: one expert with many row tiles
     (5, 64, 64, 8, False),         # several experts empty
+    (2300, 192, 320, 8, False),    # pairs: several token tiles per expert, ragged features
 ])
-def test_grouped_gemms_against_torch(moe, T, d, ffn, E, skew):
+@pytest.mark.parametrize("pair", [None, "0", "1"], ids=["auto", "one_cta", "pair"])
+def test_grouped_gemms_against_torch(moe, monkeypatch, T, d, ffn, E, skew, pair):
+    """Both expert GEMMs against torch on the GPU's own permuted rows, under
+    the automatic tile plan and with the CTA-pair kernel forced off and on."""
+    if pair is not None:
+        monkeypatch.setenv("MOE_PLAN_PAIR", pair)
     x, layer = _grouped_case(T, d, ffn, E, "bf16", seed=T, skew=skew)
     logits, idx, gates = moe.router(x, layer.Wg, 2, layer.bias)
     idx2, gates2, counts, offsets, perm, inv = moe.route_from_logits(logits, 2)
