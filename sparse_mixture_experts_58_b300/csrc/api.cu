@@ -189,13 +189,15 @@ int encode_uncached(CUtensorMap *map, const void *base, unsigned long long inner
 
 }  // namespace
 
-// Tile plan.  Rows per expert decide the tile family: with many rows per
-// expert (prefill) 256-wide tiles keep the tensor cores fed; with few
-// (decode) 128-wide tiles give enough units for every SM to stream weights.
-// An expert never has more than T rows (a token picks an expert at most
-// once), so for T <= 128 one row tile of round_up(T, 8) rows holds any expert.
-// The down projection's contraction is split so that about 8 units per SM
-// exist when few experts are busy; the partial sums are added in the combine.
+// Tile plan.  Rows per expert decide the kernel: with 128 or more on average
+// (prefill) the CTA-pair kernel (256 weight rows x token tiles of up to 256
+// rows, gemm_pair.cu) keeps the tensor cores fed; with fewer (decode) the
+// one-CTA kernel's 128-wide tiles give enough units for every SM to stream
+// weights.  An expert never has more than T rows (a token picks an expert at
+// most once), so for T <= 128 one row tile of round_up(T, 8) rows holds any
+// expert.  The down projection's contraction is split so that enough units
+// exist for every SM (one-CTA: about 8 per SM; pairs: about 4 per pair); the
+// partial sums are added in the combine.
 int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p) {
     int rc = check_dims(T, d, ffn, E, k, dt);
     if (rc != MOE_OK) return rc;
@@ -260,6 +262,7 @@ int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p) {
     q.o_offsets = take((size_t)(E + 1) * 4);
     q.o_perm = take((size_t)q.rows * 4);
     q.o_inv = take((size_t)q.rows * 4);
+    q.o_rms = take((size_t)T * 4);
     q.o_xperm = take((size_t)q.rows * d * elt);
     q.o_h = take((size_t)q.rows * ffn * elt);
     q.o_y = take((size_t)q.splits * q.rows * d * 4);
@@ -297,9 +300,13 @@ int read_options(const moe_options *o, Options *out) {
     return MOE_OK;
 }
 
+// norm_eps != nullptr: a pre-norm block, out = x (in place):
+// x <- round(x + MoE(RMSNorm(x))), RMSNorm fused into the router and the
+// grouping, the residual add into the combine.
 int run_forward(const Plan &P, const Options &O, const void *x, const void *W_g,
                 const float *bias, const void *const *W1, const void *const *W3,
-                const void *const *W2, void *out, void *ws, cudaStream_t s) {
+                const void *const *W2, void *out, void *ws, cudaStream_t s,
+                const float *norm_eps = nullptr) {
     float *logits = ws_at<float>(ws, P.o_logits);
     int *idx = ws_at<int>(ws, P.o_idx);
     float *gates = ws_at<float>(ws, P.o_gates);
@@ -312,16 +319,18 @@ int run_forward(const Plan &P, const Options &O, const void *x, const void *W_g,
     void *x_perm = ws_at<uint8_t>(ws, P.o_xperm);
     void *h = ws_at<uint8_t>(ws, P.o_h);
     float *y = ws_at<float>(ws, P.o_y);
+    float *inv_rms = norm_eps != nullptr ? ws_at<float>(ws, P.o_rms) : nullptr;
+    const float eps = norm_eps != nullptr ? *norm_eps : 0.f;
     const int elt = elem_size(P.dt);
     int rc;
-    if ((rc = cuda_rc(launch_router(x, W_g, bias, P.T, P.d, P.E, P.k, P.dt, O.gating, logits, idx,
-                                    gates, s))) != MOE_OK)
+    if ((rc = cuda_rc(launch_router(x, W_g, bias, P.T, P.d, P.E, P.k, P.dt, O.gating, eps, inv_rms,
+                                    logits, idx, gates, s))) != MOE_OK)
         return rc;
     if ((rc = cuda_rc(launch_chunk_scan(idx, P.T, P.k, P.E, O.capacity, cc, cb, counts, offsets,
                                         s))) != MOE_OK)
         return rc;
-    if ((rc = cuda_rc(launch_group_tokens(idx, cb, offsets, x, P.T, P.d, P.E, P.k, O.capacity, elt,
-                                          perm, inv, x_perm, s))) != MOE_OK)
+    if ((rc = cuda_rc(launch_group_tokens(idx, cb, offsets, x, inv_rms, P.T, P.d, P.E, P.k,
+                                          O.capacity, elt, perm, inv, x_perm, s))) != MOE_OK)
         return rc;
     if (P.dt == MOE_BF16) {
         if (P.pair) {
@@ -348,8 +357,8 @@ int run_forward(const Plan &P, const Options &O, const void *x, const void *W_g,
                                           P.ffn, P.E, y, s))) != MOE_OK)
             return rc;
     }
-    return cuda_rc(
-        launch_combine(y, P.splits, P.rows, gates, inv, P.T, P.d, P.k, O.renorm, P.dt, out, s));
+    return cuda_rc(launch_combine(y, P.splits, P.rows, gates, inv, P.T, P.d, P.k, O.renorm,
+                                  norm_eps != nullptr ? 1 : 0, P.dt, out, s));
 }
 
 int check_forward_args(const void *x, const void *W_g, const void *const *W1,
@@ -444,6 +453,22 @@ int moe_forward_ex(const void *x, const void *W_g, const float *router_bias,
                        static_cast<cudaStream_t>(stream));
 }
 
+int moe_block_forward(void *x, const void *W_g, const float *router_bias, const void *const *W1,
+                      const void *const *W3, const void *const *W2, int T, int d, int ffn, int E,
+                      int k, int dtype, float eps, const moe_options *options, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+    if (!(eps >= 0.f)) return MOE_ERR_ARG;
+    Options O;
+    int rc = read_options(options, &O);
+    if (rc != MOE_OK) return rc;
+    Plan P;
+    rc = check_forward_args(x, W_g, W1, W3, W2, T, d, ffn, E, k, dtype, x, workspace,
+                            workspace_bytes, &P);
+    if (rc != MOE_OK || T == 0) return rc;
+    return run_forward(P, O, x, W_g, router_bias, W1, W3, W2, x, workspace,
+                       static_cast<cudaStream_t>(stream), &eps);
+}
+
 int moe_capacity(double capacity_factor, int T, int k, int E, int *capacity) {
     if (capacity == nullptr || T < 0 || k < 1 || E < 1) return MOE_ERR_ARG;
     if (!(capacity_factor > 0.0)) {
@@ -487,7 +512,8 @@ int moe_router(const void *x, const void *W_g, const float *router_bias, int T, 
     if (!x || !W_g || !logits || !idx || !gates) return MOE_ERR_ARG;
     if (!aligned16(x) || !aligned16(W_g)) return MOE_ERR_UNSUPPORTED;
     return cuda_rc(launch_router(x, W_g, router_bias, T, d, E, k, dtype, MOE_GATING_TOPK_SOFTMAX,
-                                 logits, idx, gates, static_cast<cudaStream_t>(stream)));
+                                 0.f, nullptr, logits, idx, gates,
+                                 static_cast<cudaStream_t>(stream)));
 }
 
 int moe_route_workspace_bytes(int T, int E, int k, size_t *bytes) {
@@ -539,8 +565,8 @@ int moe_route_from_logits_ex(const float *logits, int T, int E, int k,
     if ((rc = cuda_rc(launch_chunk_scan(idx, T, k, E, O.capacity, cc, cb, counts, offsets, s))) !=
         MOE_OK)
         return rc;
-    return cuda_rc(launch_group_tokens(idx, cb, offsets, nullptr, T, 0, E, k, O.capacity, 0, perm,
-                                       inv, nullptr, s));
+    return cuda_rc(launch_group_tokens(idx, cb, offsets, nullptr, nullptr, T, 0, E, k, O.capacity,
+                                       0, perm, inv, nullptr, s));
 }
 
 int moe_permute(const void *x, const int *perm, int rows, int T, int d, int k, int dtype,
@@ -608,7 +634,7 @@ int moe_combine(const float *y_partial, int splits, const float *gates, const in
     if (T == 0) return MOE_OK;
     if (!y_partial || !gates || !inv || !out) return MOE_ERR_ARG;
     if (d % 4 != 0 || !aligned16(y_partial) || !aligned16(out)) return MOE_ERR_UNSUPPORTED;
-    return cuda_rc(launch_combine(y_partial, splits, T * k, gates, inv, T, d, k, 0, dtype, out,
+    return cuda_rc(launch_combine(y_partial, splits, T * k, gates, inv, T, d, k, 0, 0, dtype, out,
                                   static_cast<cudaStream_t>(stream)));
 }
 
@@ -618,6 +644,9 @@ int moe_add_rmsnorm(void *x, const void *add, void *xn, int T, int d, float eps,
         return MOE_ERR_ARG;
     if (T == 0) return MOE_OK;
     if (!x || !xn) return MOE_ERR_ARG;
+    if ((d * elem_size(dtype)) % 16 != 0 || !aligned16(x) || !aligned16(xn) ||
+        (add != nullptr && !aligned16(add)))
+        return MOE_ERR_UNSUPPORTED;
     return cuda_rc(launch_add_rmsnorm(x, add, xn, T, d, eps, dtype,
                                       static_cast<cudaStream_t>(stream)));
 }

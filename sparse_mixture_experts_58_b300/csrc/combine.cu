@@ -6,7 +6,9 @@
 // Solution", routing paragraph; "Mixtral" curriculum page, "weighted expert
 // outputs").  The down projection leaves fp32 partial sums per contraction
 // split; they are added here in split order, then gated in slot order, then
-// rounded once.  HBM-bound: one warp per token, 16-byte loads.
+// rounded once.  HBM-bound: one warp per token, 16-byte loads.  In a
+// pre-norm block the residual add follows in the same pass:
+// out <- round(out + round(combined)), the rounding the separate add would do.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -29,6 +31,24 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *p, float4 v
     *reinterpret_cast<uint2 *>(p) = u;
 }
 
+template <typename T>
+__device__ __forceinline__ float4 load4(const T *p);
+template <>
+__device__ __forceinline__ float4 load4<float>(const float *p) {
+    return *reinterpret_cast<const float4 *>(p);
+}
+template <>
+__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16 *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+}
+
+template <typename T>
+__device__ __forceinline__ float round_to(float v) {
+    return to_f32(from_f32<T>(v));
+}
+
 __device__ __forceinline__ void add4(float4 &s, const float4 &p) {
     s.x += p.x;
     s.y += p.y;
@@ -47,7 +67,7 @@ template <typename T, int K, int C, int SB>
 __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ y, int splits,
                                                       int rows, const float *__restrict__ gates,
                                                       const int *__restrict__ inv, int Tn, int d,
-                                                      int k, int renorm, T *out) {
+                                                      int k, int renorm, int residual, T *out) {
     pdl_wait();
     pdl_trigger();
     const int t = blockIdx.x;
@@ -122,68 +142,87 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
                 acc.w = fmaf(gj[j], s[j][c].w, acc.w);
             }
         }
-        store4<T>(out + (size_t)t * d + 4 * v, acc);
+        T *dst = out + (size_t)t * d + 4 * v;
+        if (residual) {
+            const float4 r = load4<T>(dst);
+            acc = make_float4(r.x + round_to<T>(acc.x), r.y + round_to<T>(acc.y),
+                              r.z + round_to<T>(acc.z), r.w + round_to<T>(acc.w));
+        }
+        store4<T>(dst, acc);
     }
 }
 
 template <typename T, int K, int C, int SB>
 void launch_combine_t(const float *y, int splits, int rows, const float *gates, const int *inv,
-                      int T_, int d, int k, int renorm, void *out, cudaStream_t s) {
+                      int T_, int d, int k, int renorm, int residual, void *out, cudaStream_t s) {
     const dim3 grid(T_, (d / 4 + 256 * C - 1) / (256 * C));
     launch_pdl(combine_kernel<T, K, C, SB>, grid, 256, 0, s, y, splits, rows, gates, inv, T_, d, k,
-               renorm, static_cast<T *>(out));
+               renorm, residual, static_cast<T *>(out));
 }
 
-// Kernel shape by slot count and split count: unsplit partials (large
-// batches) take 4 column groups per thread; split partials (small batches)
-// one group and several splits per batch.
+// Kernel shape by slot count and split count, keeping about 16 loads in
+// flight per thread: unsplit or lightly split partials (large batches) take
+// 2-4 column groups per thread; heavily split partials (small batches) one
+// group and up to 8 splits per batch.
 template <typename T>
 void launch_combine_dt(const float *y, int splits, int rows, const float *gates, const int *inv,
-                       int T_, int d, int k, int renorm, void *out, cudaStream_t s) {
+                       int T_, int d, int k, int renorm, int residual, void *out, cudaStream_t s) {
+    void (*launch)(const float *, int, int, const float *, const int *, int, int, int, int, int,
+                   void *, cudaStream_t);
     if (k <= 2) {
         if (splits == 1)
-            launch_combine_t<T, 2, 4, 1>(y, splits, rows, gates, inv, T_, d, k, renorm, out, s);
+            launch = launch_combine_t<T, 2, 4, 1>;
+        else if (splits == 2)
+            launch = launch_combine_t<T, 2, 4, 2>;
+        else if (splits <= 4)
+            launch = launch_combine_t<T, 2, 2, 4>;
         else
-            launch_combine_t<T, 2, 1, 8>(y, splits, rows, gates, inv, T_, d, k, renorm, out, s);
+            launch = launch_combine_t<T, 2, 1, 8>;
     } else {
-        if (splits == 1)
-            launch_combine_t<T, MOE_MAX_TOPK, 1, 1>(y, splits, rows, gates, inv, T_, d, k, renorm,
-                                                    out, s);
-        else
-            launch_combine_t<T, MOE_MAX_TOPK, 1, 2>(y, splits, rows, gates, inv, T_, d, k, renorm,
-                                                    out, s);
+        launch = splits == 1 ? launch_combine_t<T, MOE_MAX_TOPK, 1, 1>
+                             : launch_combine_t<T, MOE_MAX_TOPK, 1, 2>;
     }
+    launch(y, splits, rows, gates, inv, T_, d, k, renorm, residual, out, s);
 }
 
-// One block per row: optional residual add (rounded to the storage type),
-// then RMSNorm with gain 1.
+// One block of kNormThreads per row: optional residual add (rounded to the
+// storage type), then RMSNorm with gain 1 in the order common.cuh fixes, the
+// order the router's fused normalisation repeats.  d is a multiple of one
+// 16-byte slice.
 template <typename T>
-__global__ void __launch_bounds__(256) add_rmsnorm_kernel(T *x, const T *__restrict__ add, T *xn,
-                                                          int d, float eps) {
-    __shared__ float s_part[8];
+__global__ void __launch_bounds__(kNormThreads)
+    add_rmsnorm_kernel(T *x, const T *__restrict__ add, T *xn, int d, float eps) {
+    constexpr int VN = Vec<T>::n;
+    __shared__ float s_part[kNormThreads / 32];
     pdl_wait();
     pdl_trigger();
     const size_t o = (size_t)blockIdx.x * d;
+    uint4 *xr = reinterpret_cast<uint4 *>(x + o);
+    const uint4 *ar = add != nullptr ? reinterpret_cast<const uint4 *>(add + o) : nullptr;
+    uint4 *xnr = reinterpret_cast<uint4 *>(xn + o);
+    const int nvec = d / VN;
     float ss = 0.f;
-    for (int i = threadIdx.x; i < d; i += blockDim.x) {
-        float v = to_f32(x[o + i]);
-        if (add != nullptr) {
-            const T r = from_f32<T>(v + to_f32(add[o + i]));
-            x[o + i] = r;
-            v = to_f32(r);
-        }
-        ss = fmaf(v, v, ss);
-    }
+    for (int v = threadIdx.x; v < nvec; v += kNormThreads) {
+        uint4 q = xr[v];
+        if (ar != nullptr) {
+            float a[VN], b[VN];
+            Vec<T>::unpack(q, a);
+            Vec<T>::unpack(ar[v], b);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            for (int i = 0; i < VN; ++i) a[i] += b[i];
+            q = Vec<T>::pack(a);
+            xr[v] = q;
+        }
+        ss = slice_sumsq<T>(ss, q);
+    }
+    ss = warp_butterfly_sum(ss);
     if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = ss;
     __syncthreads();
     float tot = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) tot += s_part[w];
-    const float scale = 1.f / sqrtf(tot / static_cast<float>(d) + eps);
-    for (int i = threadIdx.x; i < d; i += blockDim.x)
-        xn[o + i] = from_f32<T>(to_f32(x[o + i]) * scale);
+    for (int w = 0; w < kNormThreads / 32; ++w) tot += s_part[w];
+    const float scale = rms_scale(tot, d, eps);
+    for (int v = threadIdx.x; v < nvec; v += kNormThreads) xnr[v] = scale_slice<T>(xr[v], scale);
 }
 
 // Waits on a barrier nothing arrives at; the bounded wait gives up after
@@ -200,13 +239,14 @@ __global__ void wait_selftest_kernel(unsigned long long limit_ns, int *status) {
 }  // namespace
 
 cudaError_t launch_combine(const float *y, int splits, int rows, const float *gates,
-                           const int *inv, int T, int d, int k, int renorm, int dt, void *out,
-                           cudaStream_t s) {
+                           const int *inv, int T, int d, int k, int renorm, int residual, int dt,
+                           void *out, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (dt == MOE_BF16)
-        launch_combine_dt<__nv_bfloat16>(y, splits, rows, gates, inv, T, d, k, renorm, out, s);
+        launch_combine_dt<__nv_bfloat16>(y, splits, rows, gates, inv, T, d, k, renorm, residual,
+                                         out, s);
     else
-        launch_combine_dt<float>(y, splits, rows, gates, inv, T, d, k, renorm, out, s);
+        launch_combine_dt<float>(y, splits, rows, gates, inv, T, d, k, renorm, residual, out, s);
     return cudaGetLastError();
 }
 
@@ -214,11 +254,11 @@ cudaError_t launch_add_rmsnorm(void *x, const void *add, void *xn, int T, int d,
                                cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (dt == MOE_BF16)
-        return launch_pdl(add_rmsnorm_kernel<__nv_bfloat16>, T, 256, 0, s,
+        return launch_pdl(add_rmsnorm_kernel<__nv_bfloat16>, T, kNormThreads, 0, s,
                           static_cast<__nv_bfloat16 *>(x),
                           static_cast<const __nv_bfloat16 *>(add),
                           static_cast<__nv_bfloat16 *>(xn), d, eps);
-    return launch_pdl(add_rmsnorm_kernel<float>, T, 256, 0, s, static_cast<float *>(x),
+    return launch_pdl(add_rmsnorm_kernel<float>, T, kNormThreads, 0, s, static_cast<float *>(x),
                       static_cast<const float *>(add), static_cast<float *>(xn), d, eps);
 }
 

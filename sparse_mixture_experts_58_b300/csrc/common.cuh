@@ -65,6 +65,81 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
     return __float2bfloat16_rn(v);
 }
 
+// 16-byte slices of a row: unpacked to fp32 in element order, and packed
+// back with round-to-nearest-even to the storage type.
+template <typename T> struct Vec;
+template <> struct Vec<__nv_bfloat16> {
+    static constexpr int n = 8;
+    __device__ static void unpack(const uint4 &v, float (&f)[8]) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+    __device__ static uint4 pack(const float (&f)[8]) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 p = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t *>(&p);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+template <> struct Vec<float> {
+    static constexpr int n = 4;
+    __device__ static void unpack(const uint4 &v, float (&f)[4]) {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    }
+    __device__ static uint4 pack(const float (&f)[4]) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                          __float_as_uint(f[3]));
+    }
+};
+
+// RMSNorm with gain 1, computed the same way (so to the same bits) by the
+// stand-alone RMSNorm kernel and by the router's fused normalisation: with
+// kNormThreads threads per row, thread i takes the row's 16-byte slices i,
+// i + kNormThreads, ... and adds the squares of their elements in order
+// (fmaf); each warp's partial sums are added by a butterfly, then the warps'
+// sums in warp order; scale = 1 / sqrt(sum / d + eps); the normalised element
+// is round(x * scale) in the storage type.
+constexpr int kNormThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ float slice_sumsq(float ss, const uint4 &v) {
+    float f[Vec<T>::n];
+    Vec<T>::unpack(v, f);
+#pragma unroll
+    for (int i = 0; i < Vec<T>::n; ++i) ss = fmaf(f[i], f[i], ss);
+    return ss;
+}
+
+__device__ __forceinline__ float warp_butterfly_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+__device__ __forceinline__ float rms_scale(float sumsq, int d, float eps) {
+    return 1.f / sqrtf(sumsq / static_cast<float>(d) + eps);
+}
+
+// round(x * scale) for the elements of one 16-byte slice.
+template <typename T>
+__device__ __forceinline__ uint4 scale_slice(const uint4 &v, float scale) {
+    float f[Vec<T>::n];
+    Vec<T>::unpack(v, f);
+#pragma unroll
+    for (int i = 0; i < Vec<T>::n; ++i) f[i] *= scale;
+    return Vec<T>::pack(f);
+}
+
 // Selection of the k (<= KMAX <= MOE_MAX_TOPK) largest of E logits: each
 // logit in expert order is carried down a list of KMAX entries kept in
 // (value descending, expert ascending) order, swapping places with any entry

@@ -26,6 +26,7 @@ struct Plan {
     int kps;       // 64-wide contraction blocks per split
     // workspace layout (byte offsets, 256-aligned)
     size_t o_logits, o_idx, o_gates, o_ccount, o_cbase, o_counts, o_offsets, o_perm, o_inv;
+    size_t o_rms;  // per-token RMSNorm scale (pre-norm blocks)
     size_t o_xperm, o_h, o_y, bytes;
 };
 
@@ -60,9 +61,11 @@ int device_sm_count();
 int *device_status_ptr();
 
 // Kernel launchers (each returns the launch's cudaError_t).
+// inv_rms != nullptr: RMSNorm (eps) fused in front of the router; each
+// token's scale is written to inv_rms[T].
 cudaError_t launch_router(const void *x, const void *Wg, const float *bias, int T, int d, int E,
-                          int k, int dt, int gating, float *logits, int *idx, float *gates,
-                          cudaStream_t s);
+                          int k, int dt, int gating, float eps, float *inv_rms, float *logits,
+                          int *idx, float *gates, cudaStream_t s);
 cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, int gating,
                                     int *idx, float *gates, cudaStream_t s);
 // Per-chunk expert counts from idx (into chunk_counts), then their per-expert
@@ -70,9 +73,12 @@ cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, in
 // <= 0: all rows).
 cudaError_t launch_chunk_scan(const int *idx, int T, int k, int E, int capacity, int *chunk_counts,
                               int *chunk_base, int *counts, int *offsets, cudaStream_t s);
+// row_scale != nullptr: each copied row is multiplied by its token's scale
+// and rounded to the storage type (the fused RMSNorm).
 cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int *offsets,
-                                const void *x, int T, int d, int E, int k, int capacity, int elt,
-                                int *perm, int *inv, void *x_perm, cudaStream_t s);
+                                const void *x, const float *row_scale, int T, int d, int E, int k,
+                                int capacity, int elt, int *perm, int *inv, void *x_perm,
+                                cudaStream_t s);
 // x_perm[r] = x[perm[r] / k] for r < rows.
 cudaError_t launch_permute(const void *x, const int *perm, int rows, int d, int k, int elt,
                            void *x_perm, cudaStream_t s);
@@ -97,9 +103,11 @@ cudaError_t launch_swiglu_f32(const float *x_perm, const int *offsets, const voi
 cudaError_t launch_down_f32(const float *h, const int *offsets, const void *const *W2, int rows,
                             int d, int ffn, int E, float *y, cudaStream_t s);
 
+// residual != 0: out <- round(out + round(combined)) in place (the residual
+// add of a pre-norm block).
 cudaError_t launch_combine(const float *y, int splits, int rows, const float *gates,
-                           const int *inv, int T, int d, int k, int renorm, int dt, void *out,
-                           cudaStream_t s);
+                           const int *inv, int T, int d, int k, int renorm, int residual, int dt,
+                           void *out, cudaStream_t s);
 cudaError_t launch_add_rmsnorm(void *x, const void *add, void *xn, int T, int d, float eps,
                                int dt, cudaStream_t s);
 cudaError_t launch_wait_selftest(unsigned int limit_ns, cudaStream_t s);

@@ -98,14 +98,18 @@ __device__ __forceinline__ void copy_row(const uint4 *__restrict__ src, uint4 *d
 
 // One block = one chunk of kChunk tokens (x up to 8 row slices for small
 // batches, blockIdx.y).  Thread i < kChunk ranks token i's selections against
-// the chunk's earlier tokens; then all threads copy rows.
+// the chunk's earlier tokens; then all threads copy rows.  With row_scale
+// (elt 2: bf16, 4: fp32), each 16-byte slice is multiplied by its token's
+// scale and rounded to the storage type on the way.
 template <int KMAX>
 __global__ void __launch_bounds__(256) group_tokens_kernel(
     const int *__restrict__ idx, const int *__restrict__ chunk_base,
-    const int *__restrict__ offsets, const uint8_t *__restrict__ x, int Tn, int E, int k,
-    int capacity, size_t row_bytes, int *perm, int *inv, uint8_t *x_perm) {
+    const int *__restrict__ offsets, const uint8_t *__restrict__ x,
+    const float *__restrict__ row_scale, int elt, int Tn, int E, int k, int capacity,
+    size_t row_bytes, int *perm, int *inv, uint8_t *x_perm) {
     __shared__ int s_idx[kChunk * MOE_MAX_TOPK];
     __shared__ int s_row[kChunk * MOE_MAX_TOPK];
+    __shared__ float s_scale[kChunk];
     pdl_wait();
     pdl_trigger();
     const int c = blockIdx.x;
@@ -113,6 +117,8 @@ __global__ void __launch_bounds__(256) group_tokens_kernel(
     const int ntok = min(kChunk, Tn - first);
     for (int i = threadIdx.x; i < ntok * k; i += blockDim.x)
         s_idx[i] = idx[(size_t)first * k + i];
+    if (row_scale != nullptr && threadIdx.x < ntok)
+        s_scale[threadIdx.x] = row_scale[first + threadIdx.x];
     __syncthreads();
     if (threadIdx.x < ntok) {
         const int i = threadIdx.x;
@@ -155,6 +161,12 @@ __global__ void __launch_bounds__(256) group_tokens_kernel(
             vec[u] = vbeg + (ii - tok[u] * rowvec);
             val[u] = __ldcs(xs + (size_t)tok[u] * rowvec_all + vec[u]);
         }
+        if (row_scale != nullptr) {
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                val[u] = elt == 2 ? scale_slice<__nv_bfloat16>(val[u], s_scale[tok[u]])
+                                  : scale_slice<float>(val[u], s_scale[tok[u]]);
+        }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (i0 + (int)blockDim.x * u < total) {
@@ -195,8 +207,9 @@ cudaError_t launch_chunk_scan(const int *idx, int T, int k, int E, int capacity,
 }
 
 cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int *offsets,
-                                const void *x, int T, int d, int E, int k, int capacity, int elt,
-                                int *perm, int *inv, void *x_perm, cudaStream_t s) {
+                                const void *x, const float *row_scale, int T, int d, int E, int k,
+                                int capacity, int elt, int *perm, int *inv, void *x_perm,
+                                cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const int nchunks = (T + kChunk - 1) / kChunk;
     // few chunks (small batches): split each chunk's row copy over several
@@ -211,11 +224,12 @@ cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int
     }
     if (k <= 2)
         return launch_pdl(group_tokens_kernel<2>, dim3(nchunks, parts), 256, 0, s, idx,
-                          chunk_base, offsets, static_cast<const uint8_t *>(x), T, E, k, capacity,
-                          (size_t)d * elt, perm, inv, static_cast<uint8_t *>(x_perm));
+                          chunk_base, offsets, static_cast<const uint8_t *>(x), row_scale, elt, T,
+                          E, k, capacity, (size_t)d * elt, perm, inv,
+                          static_cast<uint8_t *>(x_perm));
     return launch_pdl(group_tokens_kernel<MOE_MAX_TOPK>, dim3(nchunks, parts), 256, 0, s, idx,
-                      chunk_base, offsets, static_cast<const uint8_t *>(x), T, E, k, capacity,
-                      (size_t)d * elt, perm, inv, static_cast<uint8_t *>(x_perm));
+                      chunk_base, offsets, static_cast<const uint8_t *>(x), row_scale, elt, T, E,
+                      k, capacity, (size_t)d * elt, perm, inv, static_cast<uint8_t *>(x_perm));
 }
 
 cudaError_t launch_permute(const void *x, const int *perm, int rows, int d, int k, int elt,

@@ -8,38 +8,17 @@
 // (one memory round trip when d <= 256 slices per thread pass), then the block
 // reduces the per-thread partial sums in a fixed order.  HBM traffic is x
 // once; the 64 KB router matrix is served from L1/L2.
+//
+// Fused RMSNorm (pre-norm blocks): a first pass over the two rows gives each
+// token's RMSNorm scale (stored for the grouping pass); the logits are then
+// taken of round(x * scale), the normalised row the stand-alone RMSNorm
+// kernel would have stored, read again from L1.
 #include "internal.h"
 
 namespace moe {
 namespace {
 
-__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-}
-
-__device__ __forceinline__ void unpack4f(const uint4 &v, float (&f)[4]) {
-    f[0] = __uint_as_float(v.x);
-    f[1] = __uint_as_float(v.y);
-    f[2] = __uint_as_float(v.z);
-    f[3] = __uint_as_float(v.w);
-}
-
-template <typename T> struct Vec;
-template <> struct Vec<__nv_bfloat16> {
-    static constexpr int n = 8;
-    __device__ static void unpack(const uint4 &v, float (&f)[8]) { unpack8(v, f); }
-};
-template <> struct Vec<float> {
-    static constexpr int n = 4;
-    __device__ static void unpack(const uint4 &v, float (&f)[4]) { unpack4f(v, f); }
-};
-
-constexpr int kRouterThreads = 256;
+constexpr int kRouterThreads = kNormThreads;
 constexpr int kRouterTokens = 2;
 
 // Selection and gates for one token, written out (KMAX >= k slots).
@@ -75,14 +54,18 @@ __device__ __forceinline__ void finish_token(float *l, const float *bias, int t,
 // the later passes hitting L1).  V: 16-byte slices per thread per pass, all
 // of a pass's loads in flight together.  Rows of experts >= E are clamped to
 // a valid row and their sums ignored, which keeps the loads free of branches.
-template <typename T, int EG, int V>
+// NORM: the fused RMSNorm (eps; each token's scale written to inv_rms).
+template <typename T, int EG, int V, bool NORM>
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(
     const T *__restrict__ x, const T *__restrict__ Wg, const float *__restrict__ bias, int Tn,
-    int d, int E, int k, int gating, float *logits, int *idx, float *gates) {
+    int d, int E, int k, int gating, float eps, float *inv_rms, float *logits, int *idx,
+    float *gates) {
     constexpr int VN = Vec<T>::n;
     constexpr int NW = kRouterThreads / 32;
     __shared__ float s_part[NW][kRouterTokens][MOE_MAX_EXPERTS];
     __shared__ float s_l[kRouterTokens][MOE_MAX_EXPERTS];
+    __shared__ float s_ss[NW][kRouterTokens];
+    __shared__ float s_scale[kRouterTokens];
 
     pdl_wait();
     pdl_trigger();
@@ -93,6 +76,32 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
     const uint4 *xr1 = reinterpret_cast<const uint4 *>(x + (size_t)(has1 ? t0 + 1 : t0) * d);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint4 zero = make_uint4(0, 0, 0, 0);
+    float sc0 = 1.f, sc1 = 1.f;
+    if (NORM) {
+        float ss0 = 0.f, ss1 = 0.f;
+        for (int v = threadIdx.x; v < nvec; v += kRouterThreads) {
+            ss0 = slice_sumsq<T>(ss0, xr0[v]);
+            ss1 = slice_sumsq<T>(ss1, xr1[v]);
+        }
+        ss0 = warp_butterfly_sum(ss0);
+        ss1 = warp_butterfly_sum(ss1);
+        if (lane == 0) {
+            s_ss[warp][0] = ss0;
+            s_ss[warp][1] = ss1;
+        }
+        __syncthreads();
+        if (threadIdx.x < kRouterTokens) {
+            float tot = 0.f;
+#pragma unroll
+            for (int w2 = 0; w2 < NW; ++w2) tot += s_ss[w2][threadIdx.x];
+            const float sc = rms_scale(tot, d, eps);
+            s_scale[threadIdx.x] = sc;
+            if (t0 + (int)threadIdx.x < Tn) inv_rms[t0 + threadIdx.x] = sc;
+        }
+        __syncthreads();
+        sc0 = s_scale[0];
+        sc1 = s_scale[1];
+    }
 
     for (int g0 = 0; g0 < E; g0 += EG) {
         const uint4 *wr[EG];
@@ -117,8 +126,8 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
 #pragma unroll
             for (int u = 0; u < V; ++u) {
                 float a[VN], b[VN];
-                Vec<T>::unpack(xa[u], a);
-                Vec<T>::unpack(xb[u], b);
+                Vec<T>::unpack(NORM ? scale_slice<T>(xa[u], sc0) : xa[u], a);
+                Vec<T>::unpack(NORM ? scale_slice<T>(xb[u], sc1) : xb[u], b);
 #pragma unroll
                 for (int e = 0; e < EG; ++e) {
                     float wf[VN];
@@ -178,31 +187,43 @@ __global__ void __launch_bounds__(128) topk_kernel(const float *__restrict__ log
         select_and_store<MOE_MAX_TOPK>(l, t, E, k, gating, idx, gates);
 }
 
-template <typename T>
-cudaError_t router_dispatch(const void *x, const void *Wg, const float *bias, int T_, int d,
-                            int E, int k, int gating, float *logits, int *idx, float *gates,
-                            cudaStream_t s) {
+template <typename T, bool NORM>
+cudaError_t router_dispatch_n(const void *x, const void *Wg, const float *bias, int T_, int d,
+                              int E, int k, int gating, float eps, float *inv_rms, float *logits,
+                              int *idx, float *gates, cudaStream_t s) {
     const int grid = (T_ + kRouterTokens - 1) / kRouterTokens;
     const T *xp = static_cast<const T *>(x);
     const T *wp = static_cast<const T *>(Wg);
     // 16-byte loads in flight per thread per pass: V * (2 + EG)
     if (E <= 8)
-        return launch_pdl(router_kernel<T, 8, 2>, grid, kRouterThreads, 0, s, xp, wp, bias, T_, d,
-                          E, k, gating, logits, idx, gates);
-    return launch_pdl(router_kernel<T, 16, 1>, grid, kRouterThreads, 0, s, xp, wp, bias, T_, d, E,
-                      k, gating, logits, idx, gates);
+        return launch_pdl(router_kernel<T, 8, 2, NORM>, grid, kRouterThreads, 0, s, xp, wp, bias,
+                          T_, d, E, k, gating, eps, inv_rms, logits, idx, gates);
+    return launch_pdl(router_kernel<T, 16, 1, NORM>, grid, kRouterThreads, 0, s, xp, wp, bias, T_,
+                      d, E, k, gating, eps, inv_rms, logits, idx, gates);
+}
+
+template <typename T>
+cudaError_t router_dispatch(const void *x, const void *Wg, const float *bias, int T_, int d,
+                            int E, int k, int gating, float eps, float *inv_rms, float *logits,
+                            int *idx, float *gates, cudaStream_t s) {
+    if (inv_rms != nullptr)
+        return router_dispatch_n<T, true>(x, Wg, bias, T_, d, E, k, gating, eps, inv_rms, logits,
+                                          idx, gates, s);
+    return router_dispatch_n<T, false>(x, Wg, bias, T_, d, E, k, gating, eps, inv_rms, logits,
+                                       idx, gates, s);
 }
 
 }  // namespace
 
 cudaError_t launch_router(const void *x, const void *Wg, const float *bias, int T, int d, int E,
-                          int k, int dt, int gating, float *logits, int *idx, float *gates,
-                          cudaStream_t s) {
+                          int k, int dt, int gating, float eps, float *inv_rms, float *logits,
+                          int *idx, float *gates, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (dt == MOE_BF16)
-        return router_dispatch<__nv_bfloat16>(x, Wg, bias, T, d, E, k, gating, logits, idx, gates,
-                                              s);
-    return router_dispatch<float>(x, Wg, bias, T, d, E, k, gating, logits, idx, gates, s);
+        return router_dispatch<__nv_bfloat16>(x, Wg, bias, T, d, E, k, gating, eps, inv_rms,
+                                              logits, idx, gates, s);
+    return router_dispatch<float>(x, Wg, bias, T, d, E, k, gating, eps, inv_rms, logits, idx,
+                                  gates, s);
 }
 
 cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, int gating,

@@ -27,7 +27,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 F32, BF16 = 0, 1
 OK, ERR_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE = 0, -1, -2, -3, -4, -5
-MAX_EXPERTS = 32
+MAX_EXPERTS = 64
 
 _vp, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 _P = ctypes.POINTER
@@ -78,6 +78,8 @@ MAX_TOPK = 8
 _sig("moe_forward_ex", _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _P(Options),
      _vp, _vp, _sz, _vp)
 _sig("moe_capacity", _i, ctypes.c_double, _i, _i, _i, _P(_i))
+_sig("moe_block_forward", _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_float,
+     _P(Options), _vp, _sz, _vp)
 _sig("moe_route_from_logits_ex", _i, _vp, _i, _i, _i, _P(Options), _vp, _vp, _vp, _vp, _vp, _vp,
      _vp, _sz, _vp)
 
@@ -87,6 +89,7 @@ EXPORTED = [
     "moe_expert_swiglu", "moe_down_splits", "moe_expert_down", "moe_combine",
     "moe_add_rmsnorm", "moe_device_status", "moe_selftest_wait_timeout", "moe_forward_launches",
     "moe_forward_static_scratch", "moe_forward_ex", "moe_capacity", "moe_route_from_logits_ex",
+    "moe_block_forward",
 ]
 
 
@@ -209,6 +212,25 @@ def forward(x, Wg, W1, W3, W2, k=2, bias=None, out=None, workspace=None, stream=
     _check(_lib.moe_forward(_ptr(x), _ptr(Wg), _ptr(bias), p1, p3, p2, T, d, ffn, E, k, dt,
                             _ptr(out), _ptr(ws), ws.numel(), _stream(stream)), "moe_forward")
     return out
+
+
+def block_forward(x, Wg, W1, W3, W2, k=2, bias=None, eps=1e-5, workspace=None, stream=None,
+                  gating=0, capacity=0, drop_policy=0):
+    """x <- x + MoE(RMSNorm(x)) in place through moe_block_forward (RMSNorm
+    fused into the router and the grouping, the residual add into the
+    combine); returns x."""
+    T, d, ffn, E = _shape(x, Wg, W1)
+    dt = _dt(x)
+    need = workspace_bytes(T, d, ffn, E, k, dt)
+    ws = workspace.get(need) if isinstance(workspace, Workspace) else workspace
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    p1, p3, p2 = _expert_ptrs(W1, E), _expert_ptrs(W3, E), _expert_ptrs(W2, E)
+    opt = Options(int(gating), int(capacity), int(drop_policy))
+    _check(_lib.moe_block_forward(_ptr(x), _ptr(Wg), _ptr(bias), p1, p3, p2, T, d, ffn, E, k, dt,
+                                  float(eps), ctypes.byref(opt), _ptr(ws), ws.numel(),
+                                  _stream(stream)), "moe_block_forward")
+    return x
 
 
 def forward_host_io(x_host, Wg, W1, W3, W2, k=2, bias=None, out_host=None, x_dev=None,

@@ -146,3 +146,25 @@ def test_forward_ex_rejects_bad_options(moe):
         rc = moe.lib().moe_forward_ex(fake, fake, None, w, w, w, 16, 256, 512, E, 2, moe.BF16,
                                       ctypes.byref(opt), fake, None, 0, None)
         assert rc == -1
+
+
+def test_block_forward_validates_before_launch(moe):
+    """moe_block_forward checks its arguments on the host like moe_forward_ex
+    (negative eps, null or misaligned x, missing workspace, bad options)."""
+    E = 8
+    arr = ctypes.c_void_p * E
+    fake = ctypes.c_void_p(0x10000)
+    w = arr(*([0x10000] * E))
+    lib = moe.lib()
+
+    def call(x=fake, T=16, eps=1e-5, ws=fake, ws_bytes=1 << 30, opt=None):
+        return lib.moe_block_forward(x, fake, None, w, w, w, T, 256, 512, E, 2, moe.BF16, eps,
+                                     opt, ws, ws_bytes, None)
+
+    assert call(eps=-1.0) == -1
+    assert call(eps=float("nan")) == -1
+    assert call(x=None) == -1
+    assert call(x=ctypes.c_void_p(0x10008)) == -2
+    assert call(ws=None) == -3
+    assert call(opt=ctypes.byref(moe.Options(2, 0, 0))) == -1
+    assert call(T=0) == 0

@@ -92,6 +92,19 @@ def test_small_layers_forced_tile_plan(moe, monkeypatch, T, d, ffn, E, k, pair):
     check_layer(moe, x, layer, k, dtype="bf16", label=f"T{T} E{E} k{k} pair={pair}")
 
 
+@pytest.mark.parametrize("splits", ["2", "3", "4", "8", "16"])
+@pytest.mark.parametrize("pair", ["0", "1"], ids=["one_cta", "pair"])
+def test_forced_down_splits(moe, monkeypatch, splits, pair):
+    """Split-K down projection with every combine shape (2, 3-4 and more
+    partials per row, and two batches of 8) on both GEMM kernels."""
+    monkeypatch.setenv("MOE_PLAN_PAIR", pair)
+    monkeypatch.setenv("MOE_PLAN_SPLITS", splits)
+    T, d, ffn, E, k = 300, 256, 1024, 8, 2
+    x, layer = inputs.make_workload(T, d, ffn, E, k, "bf16", seed=int(splits), device="cuda")
+    assert moe.down_splits(T, d, ffn, E, k, moe.BF16) == int(splits)
+    check_layer(moe, x, layer, k, dtype="bf16", label=f"splits={splits} pair={pair}")
+
+
 def test_empty_batch(moe):
     x, layer = inputs.make_workload(0, 128, 256, 8, 2, "bf16", 0, "cuda")
     out = moe.forward(x, layer.Wg, layer.W1, layer.W3, layer.W2, 2)
