@@ -1,15 +1,16 @@
-// Router: logits = x . W_g (fp32 accumulation), top-k selection (k <= 2,
-// ties to the lower expert index) and the softmax over the kept logits
-// ("Mixtral of Experts" (azimuth.plus), router paragraph).
+// Router: logits = x . W_g (fp32 accumulation), top-k selection (ties to the
+// lower expert index) and the gates ("Mixtral of Experts" (azimuth.plus),
+// router paragraph).
 //
-// One block handles two tokens.  Its 256 threads split the hidden dimension:
-// each thread takes 16-byte slices of both token rows and the same slices of
-// every expert's router row, issues all of those loads before any arithmetic
-// (one memory round trip when d <= 256 slices per thread pass), then the block
-// reduces the per-thread partial sums in a fixed order.  HBM traffic is x
-// once; the 64 KB router matrix is served from L1/L2.
+// One block handles TB tokens (2, 4 or 8).  Its 256 threads split the hidden
+// dimension: thread i takes 16-byte slices i, i + 256, ... of every token row
+// and the same slices of each expert's router row, issues a pass's loads
+// before any arithmetic, and the block reduces the per-thread partial sums in
+// a fixed order (butterfly in each warp, then warps in order).  HBM traffic is
+// x once; the router matrix is served from L1/L2 and unpacked once per TB
+// tokens.
 //
-// Fused RMSNorm (pre-norm blocks): a first pass over the two rows gives each
+// Fused RMSNorm (pre-norm blocks): a first pass over the rows gives each
 // token's RMSNorm scale (stored for the grouping pass); the logits are then
 // taken of round(x * scale), the normalised row the stand-alone RMSNorm
 // kernel would have stored, read again from L1.
@@ -19,7 +20,6 @@ namespace moe {
 namespace {
 
 constexpr int kRouterThreads = kNormThreads;
-constexpr int kRouterTokens = 2;
 
 // Selection and gates for one token, written out (KMAX >= k slots).
 template <int KMAX>
@@ -55,52 +55,57 @@ __device__ __forceinline__ void finish_token(float *l, const float *bias, int t,
 // of a pass's loads in flight together.  Rows of experts >= E are clamped to
 // a valid row and their sums ignored, which keeps the loads free of branches.
 // NORM: the fused RMSNorm (eps; each token's scale written to inv_rms).
-template <typename T, int EG, int V, bool NORM>
+template <typename T, int TB, int EG, int V, bool NORM>
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(
     const T *__restrict__ x, const T *__restrict__ Wg, const float *__restrict__ bias, int Tn,
     int d, int E, int k, int gating, float eps, float *inv_rms, float *logits, int *idx,
     float *gates) {
     constexpr int VN = Vec<T>::n;
     constexpr int NW = kRouterThreads / 32;
-    __shared__ float s_part[NW][kRouterTokens][MOE_MAX_EXPERTS];
-    __shared__ float s_l[kRouterTokens][MOE_MAX_EXPERTS];
-    __shared__ float s_ss[NW][kRouterTokens];
-    __shared__ float s_scale[kRouterTokens];
+    __shared__ float s_part[NW][TB][MOE_MAX_EXPERTS];
+    __shared__ float s_l[TB][MOE_MAX_EXPERTS];
+    __shared__ float s_ss[NW][TB];
+    __shared__ float s_scale[TB];
 
     pdl_wait();
     pdl_trigger();
-    const int t0 = blockIdx.x * kRouterTokens;
-    const bool has1 = t0 + 1 < Tn;
+    const int t0 = blockIdx.x * TB;
+    const int nt = min(TB, Tn - t0);
     const int nvec = d / VN;
-    const uint4 *xr0 = reinterpret_cast<const uint4 *>(x + (size_t)t0 * d);
-    const uint4 *xr1 = reinterpret_cast<const uint4 *>(x + (size_t)(has1 ? t0 + 1 : t0) * d);
+    const uint4 *xr[TB];
+#pragma unroll
+    for (int j = 0; j < TB; ++j)  // rows past the batch repeat its last token (results unused)
+        xr[j] = reinterpret_cast<const uint4 *>(x + (size_t)(t0 + min(j, nt - 1)) * d);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint4 zero = make_uint4(0, 0, 0, 0);
-    float sc0 = 1.f, sc1 = 1.f;
+    float sc[TB];
+#pragma unroll
+    for (int j = 0; j < TB; ++j) sc[j] = 1.f;
     if (NORM) {
-        float ss0 = 0.f, ss1 = 0.f;
+        float ss[TB];
+#pragma unroll
+        for (int j = 0; j < TB; ++j) ss[j] = 0.f;
         for (int v = threadIdx.x; v < nvec; v += kRouterThreads) {
-            ss0 = slice_sumsq<T>(ss0, xr0[v]);
-            ss1 = slice_sumsq<T>(ss1, xr1[v]);
+#pragma unroll
+            for (int j = 0; j < TB; ++j) ss[j] = slice_sumsq<T>(ss[j], xr[j][v]);
         }
-        ss0 = warp_butterfly_sum(ss0);
-        ss1 = warp_butterfly_sum(ss1);
-        if (lane == 0) {
-            s_ss[warp][0] = ss0;
-            s_ss[warp][1] = ss1;
+#pragma unroll
+        for (int j = 0; j < TB; ++j) {
+            ss[j] = warp_butterfly_sum(ss[j]);
+            if (lane == 0) s_ss[warp][j] = ss[j];
         }
         __syncthreads();
-        if (threadIdx.x < kRouterTokens) {
+        if (threadIdx.x < TB) {
             float tot = 0.f;
 #pragma unroll
             for (int w2 = 0; w2 < NW; ++w2) tot += s_ss[w2][threadIdx.x];
-            const float sc = rms_scale(tot, d, eps);
-            s_scale[threadIdx.x] = sc;
-            if (t0 + (int)threadIdx.x < Tn) inv_rms[t0 + threadIdx.x] = sc;
+            const float scale = rms_scale(tot, d, eps);
+            s_scale[threadIdx.x] = scale;
+            if ((int)threadIdx.x < nt) inv_rms[t0 + threadIdx.x] = scale;
         }
         __syncthreads();
-        sc0 = s_scale[0];
-        sc1 = s_scale[1];
+#pragma unroll
+        for (int j = 0; j < TB; ++j) sc[j] = s_scale[j];
     }
 
     for (int g0 = 0; g0 < E; g0 += EG) {
@@ -108,60 +113,55 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
 #pragma unroll
         for (int e = 0; e < EG; ++e)
             wr[e] = reinterpret_cast<const uint4 *>(Wg + (size_t)(g0 + e < E ? g0 + e : E - 1) * d);
-        float acc0[EG], acc1[EG];
+        float acc[TB][EG];
 #pragma unroll
-        for (int e = 0; e < EG; ++e) acc0[e] = acc1[e] = 0.f;
+        for (int j = 0; j < TB; ++j)
+#pragma unroll
+            for (int e = 0; e < EG; ++e) acc[j][e] = 0.f;
         for (int v0 = threadIdx.x; v0 < nvec; v0 += kRouterThreads * V) {
-            uint4 xa[V], xb[V], w[V][EG];
+            uint4 xs[V][TB], w[V][EG];
 #pragma unroll
             for (int u = 0; u < V; ++u) {
                 const int v = v0 + kRouterThreads * u;
                 const int vv = v < nvec ? v : 0;
-                xa[u] = __ldcs(xr0 + vv);
-                xb[u] = __ldcs(xr1 + vv);
+#pragma unroll
+                for (int j = 0; j < TB; ++j) xs[u][j] = v < nvec ? __ldcs(xr[j] + vv) : zero;
 #pragma unroll
                 for (int e = 0; e < EG; ++e) w[u][e] = __ldg(wr[e] + vv);
-                if (v >= nvec) xa[u] = xb[u] = zero;
             }
 #pragma unroll
             for (int u = 0; u < V; ++u) {
-                float a[VN], b[VN];
-                Vec<T>::unpack(NORM ? scale_slice<T>(xa[u], sc0) : xa[u], a);
-                Vec<T>::unpack(NORM ? scale_slice<T>(xb[u], sc1) : xb[u], b);
+                float a[TB][VN];
+#pragma unroll
+                for (int j = 0; j < TB; ++j)
+                    Vec<T>::unpack(NORM ? scale_slice<T>(xs[u][j], sc[j]) : xs[u][j], a[j]);
 #pragma unroll
                 for (int e = 0; e < EG; ++e) {
                     float wf[VN];
                     Vec<T>::unpack(w[u][e], wf);
 #pragma unroll
-                    for (int i = 0; i < VN; ++i) {
-                        acc0[e] = fmaf(a[i], wf[i], acc0[e]);
-                        acc1[e] = fmaf(b[i], wf[i], acc1[e]);
-                    }
+                    for (int i = 0; i < VN; ++i)
+#pragma unroll
+                        for (int j = 0; j < TB; ++j) acc[j][e] = fmaf(a[j][i], wf[i], acc[j][e]);
                 }
             }
         }
         // butterfly within each warp; lane 0 parks the warp's sums
 #pragma unroll
-        for (int e = 0; e < EG; ++e) {
+        for (int j = 0; j < TB; ++j)
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                acc0[e] += __shfl_xor_sync(0xffffffffu, acc0[e], off);
-                acc1[e] += __shfl_xor_sync(0xffffffffu, acc1[e], off);
-            }
-        }
+            for (int e = 0; e < EG; ++e) acc[j][e] = warp_butterfly_sum(acc[j][e]);
         if (lane == 0) {
 #pragma unroll
-            for (int e = 0; e < EG; ++e) {
-                if (g0 + e < E) {
-                    s_part[warp][0][g0 + e] = acc0[e];
-                    s_part[warp][1][g0 + e] = acc1[e];
-                }
-            }
+            for (int j = 0; j < TB; ++j)
+#pragma unroll
+                for (int e = 0; e < EG; ++e)
+                    if (g0 + e < E) s_part[warp][j][g0 + e] = acc[j][e];
         }
     }
     __syncthreads();
     // warps added in order: one thread per (token, expert)
-    for (int i = threadIdx.x; i < kRouterTokens * E; i += kRouterThreads) {
+    for (int i = threadIdx.x; i < TB * E; i += kRouterThreads) {
         const int j = i / E, e = i - j * E;
         float s = s_part[0][j][e];
 #pragma unroll
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
         s_l[j][e] = s;
     }
     __syncthreads();
-    if (threadIdx.x < kRouterTokens && (threadIdx.x == 0 || has1))
+    if ((int)threadIdx.x < nt)
         finish_token(s_l[threadIdx.x], bias, t0 + threadIdx.x, E, k, gating, logits, idx, gates);
 }
 
@@ -187,19 +187,37 @@ __global__ void __launch_bounds__(128) topk_kernel(const float *__restrict__ log
         select_and_store<MOE_MAX_TOPK>(l, t, E, k, gating, idx, gates);
 }
 
+template <typename T, int TB, int EG, int V, bool NORM>
+cudaError_t router_launch(const void *x, const void *Wg, const float *bias, int T_, int d, int E,
+                          int k, int gating, float eps, float *inv_rms, float *logits, int *idx,
+                          float *gates, cudaStream_t s) {
+    const int grid = (T_ + TB - 1) / TB;
+    return launch_pdl(router_kernel<T, TB, EG, V, NORM>, grid, kRouterThreads, 0, s,
+                      static_cast<const T *>(x), static_cast<const T *>(Wg), bias, T_, d, E, k,
+                      gating, eps, inv_rms, logits, idx, gates);
+}
+
+// Tokens per block: 2 for small batches (blocks for every SM), 4 or 8 once
+// there are at least two blocks per SM, so a block reads and unpacks the
+// router matrix once for more tokens.  16-byte loads in flight per thread per
+// pass: V * (TB + EG).  Every choice sums each token's products in the same
+// order, so a token's logits do not depend on the batch it comes in.
 template <typename T, bool NORM>
 cudaError_t router_dispatch_n(const void *x, const void *Wg, const float *bias, int T_, int d,
                               int E, int k, int gating, float eps, float *inv_rms, float *logits,
                               int *idx, float *gates, cudaStream_t s) {
-    const int grid = (T_ + kRouterTokens - 1) / kRouterTokens;
-    const T *xp = static_cast<const T *>(x);
-    const T *wp = static_cast<const T *>(Wg);
-    // 16-byte loads in flight per thread per pass: V * (2 + EG)
-    if (E <= 8)
-        return launch_pdl(router_kernel<T, 8, 2, NORM>, grid, kRouterThreads, 0, s, xp, wp, bias,
-                          T_, d, E, k, gating, eps, inv_rms, logits, idx, gates);
-    return launch_pdl(router_kernel<T, 16, 1, NORM>, grid, kRouterThreads, 0, s, xp, wp, bias, T_,
-                      d, E, k, gating, eps, inv_rms, logits, idx, gates);
+#define MOE_ROUTER(TB, EG, V)                                                                      \
+    return router_launch<T, TB, EG, V, NORM>(x, Wg, bias, T_, d, E, k, gating, eps, inv_rms,      \
+                                             logits, idx, gates, s)
+    const int blocks_per_sm = 2;
+    if (E <= 8) {
+        if (T_ >= 8 * blocks_per_sm * kPlanSms) MOE_ROUTER(8, 4, 1);
+        if (T_ >= 4 * blocks_per_sm * kPlanSms) MOE_ROUTER(4, 8, 1);
+        MOE_ROUTER(2, 8, 2);
+    }
+    if (T_ >= 4 * blocks_per_sm * kPlanSms) MOE_ROUTER(4, 8, 1);
+    MOE_ROUTER(2, 16, 1);
+#undef MOE_ROUTER
 }
 
 template <typename T>

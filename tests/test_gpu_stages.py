@@ -39,7 +39,8 @@ def _logits_with_ties(T, E, seed):
 
 @pytest.mark.parametrize("T,E,k", [(1, 8, 2), (16, 8, 2), (17, 8, 2), (300, 8, 2), (4096, 8, 2),
                                    (1000, 3, 1), (257, 32, 2), (64, 2, 2), (50, 1, 1),
-                                   (16384, 8, 2)])
+                                   (16384, 8, 2),
+                                   (20000, 64, 8)])   # chunk counts too large for shared memory
 def test_route_from_logits_bit_exact(moe, T, E, k):
     l = _logits_with_ties(T, E, seed=T * 31 + E)
     idx, gates, counts, offsets, perm, inv = moe.route_from_logits(torch.from_numpy(l).cuda(), k)
@@ -73,6 +74,21 @@ def test_router_matches_oracle(moe, name, T):
     keep = ~helpers.near_tie_mask(rl, k)
     assert np.array_equal(idx.cpu().numpy()[keep], ridx[keep])
     assert np.allclose(gates.cpu().numpy()[keep], rg[keep], atol=2e-5)
+
+
+@pytest.mark.parametrize("E,k,Ts", [(8, 2, (1, 16, 1500, 2400, 4096)), (64, 8, (3, 16, 1200))])
+def test_router_logits_do_not_depend_on_batch(moe, E, k, Ts):
+    """A token's logits, selection and gates are the same bits whether it is
+    routed alone, in a small batch or in a large one: the router takes 2, 4
+    or 8 tokens per block by batch size but sums every token's products in
+    the same order."""
+    x, layer = inputs.make_workload(max(Ts), 4096, 64, E, k, "bf16", seed=E, device="cuda")
+    full = moe.router(x, layer.Wg, k)
+    for T in Ts:
+        part = moe.router(x[:T].contiguous(), layer.Wg, k)
+        torch.cuda.synchronize()
+        for a, b in zip(full, part):
+            assert torch.equal(a[:T], b), T
 
 
 def test_router_skew_bias(moe):

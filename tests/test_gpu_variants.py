@@ -45,6 +45,7 @@ def _logits(T, E, seed, skew=True):
     (300, 8, 2, 0, 40), (300, 8, 2, 1, 0), (300, 8, 2, 1, 25), (1000, 8, 2, 0, 1),
     (257, 64, 8, 0, 0), (257, 64, 8, 1, 30), (100, 4, 4, 0, 60), (129, 16, 3, 0, 17),
     (16384, 8, 2, 0, 3000), (33, 8, 2, 0, 100000),
+    (16, 8, 2, 0, 3), (12, 64, 8, 1, 1),            # batches of one chunk
 ])
 def test_route_variants_bit_exact(moe, T, E, k, gating, capacity):
     l = _logits(T, E, seed=T + E + k)
