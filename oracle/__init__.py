@@ -70,6 +70,11 @@ def _declare(lib):
     lib.oracle_bf16_to_double.restype = ctypes.c_double
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = c_int
+    lib.oracle_moe_backward.argtypes = [
+        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+        c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
+        c_int, c_int, c_int]
+    lib.oracle_moe_backward.restype = c_int
     return lib
 
 
@@ -153,6 +158,48 @@ class Oracle:
         if exact:
             return out, logits, idx, gates, ex
         return out, logits, idx, gates
+
+    def moe_backward(self, x, Wg, W1, W3, W2, k, dout, bias=None, threads=0, rows1=None,
+                     rows2=None, weights=True):
+        """Gradients of sum(dout * layer(x)) (gating 0, no capacity limit), in
+        float64: returns dict(dx [T,d], dWg [E,d], dW1, dW3 (lists of E arrays
+        [c1-c0, d]) and dW2 (list of [n1-n0, ffn])).  rows1 = (c0, c1) and
+        rows2 = (n0, n1) restrict the weight-gradient rows (default: all);
+        weights=False skips dW1/dW3/dW2."""
+        x = np.ascontiguousarray(x)
+        dt = _dt_code(x)
+        T, d = x.shape
+        E = Wg.shape[0]
+        Wg = np.ascontiguousarray(Wg)
+        W1 = [np.ascontiguousarray(w) for w in W1]
+        W3 = [np.ascontiguousarray(w) for w in W3]
+        W2 = [np.ascontiguousarray(w) for w in W2]
+        dout = np.ascontiguousarray(dout)
+        ffn = W1[0].shape[0]
+        assert dout.shape == (T, d) and dout.dtype == x.dtype
+        for w in (Wg, *W1, *W3, *W2):
+            assert w.dtype == x.dtype
+        c0, c1 = rows1 if rows1 is not None else (0, ffn)
+        n0, n1 = rows2 if rows2 is not None else (0, d)
+        arr = ctypes.c_void_p * E
+        p1 = arr(*[w.ctypes.data for w in W1])
+        p3 = arr(*[w.ctypes.data for w in W3])
+        p2 = arr(*[w.ctypes.data for w in W2])
+        b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+        dx = np.empty((T, d), np.float64)
+        dWg = np.empty((E, d), np.float64)
+        g1 = [np.empty((c1 - c0, d), np.float64) for _ in range(E)] if weights else []
+        g3 = [np.empty((c1 - c0, d), np.float64) for _ in range(E)] if weights else []
+        g2 = [np.empty((n1 - n0, ffn), np.float64) for _ in range(E)] if weights else []
+        q1 = arr(*[a.ctypes.data for a in g1]) if weights else None
+        q3 = arr(*[a.ctypes.data for a in g3]) if weights else None
+        q2 = arr(*[a.ctypes.data for a in g2]) if weights else None
+        rc = self.lib.oracle_moe_backward(
+            _ptr(x), _ptr(Wg), _ptr(b), p1, p3, p2, T, d, ffn, E, k, dt, _ptr(dout), _ptr(dx),
+            _ptr(dWg), q1, q3, q2, int(c0), int(c1), int(n0), int(n1), int(threads))
+        if rc != 0:
+            raise RuntimeError(f"oracle_moe_backward failed: {rc}")
+        return dict(dx=dx, dWg=dWg, dW1=g1, dW3=g3, dW2=g2)
 
     def router(self, x, Wg, k, bias=None, gating=0):
         x = np.ascontiguousarray(x)

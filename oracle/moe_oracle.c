@@ -471,6 +471,199 @@ int oracle_add(const void *a, const void *b, size_t n, int dt, void *z)
     return ORACLE_OK;
 }
 
+/* ---- backward (training) ------------------------------------------------ */
+
+/* Logistic function and the derivative of silu(u) = u s(u):
+ * silu'(u) = s(u) + u s(u) (1 - s(u)). */
+static double logistic(double u) { return 1.0 / (1.0 + exp(-u)); }
+
+/*
+ * Gradients of L = sum_t <dout[t], out[t]> (dout: the upstream gradient of the
+ * layer output) for the layer with gating 0 and no capacity limit, by the
+ * chain rule through the forward's steps, in double, term by term.  Which
+ * experts a token picks is piecewise constant in the inputs, so no gradient
+ * flows through the selection; the fp32 rounding of the logits is taken as
+ * the identity.  For token t and each slot j (expert e = e_j, gate g_j):
+ *   u = W1[e] x,  v = W3[e] x,  h = silu(u) * v,  y_j = W2[e] h      (forward)
+ *   dy_j = g_j dout[t]                                (weighted sum)
+ *   dg_j = <dout[t], y_j>
+ *   dh   = W2[e]^T dy_j,              dW2[e] += dy_j h^T
+ *   du   = dh * v * silu'(u),  dv = dh * silu(u)      (SwiGLU product)
+ *   dW1[e] += du x^T,  dW3[e] += dv x^T,  dx[t] += W1[e]^T du + W3[e]^T dv
+ *   dl_j = g_j (dg_j - sum_m g_m dg_m)                (softmax over the kept)
+ *   dW_g[e_j] += dl_j x,  dx[t] += sum_j dl_j W_g[e_j]
+ * Outputs (double, any may be NULL): dx [T][d], dWg [E][d], and per expert
+ * dW1[e], dW3[e] rows [c0, c1) of [ffn][d] (stored [c1-c0][d]) and dW2[e]
+ * rows [n0, n1) of [d][ffn] (stored [n1-n0][ffn]).  Every weight-gradient
+ * element sums its terms in token order, then slot order.
+ */
+int oracle_moe_backward(const void *x, const void *Wg, const float *bias,
+                        const void *const *W1, const void *const *W3, const void *const *W2,
+                        int T, int d, int ffn, int E, int k, int dt, const void *dout,
+                        double *dx, double *dWg, double *const *dW1, double *const *dW3,
+                        double *const *dW2, int c0, int c1, int n0, int n1, int nthreads)
+{
+    if (T < 0 || d < 1 || ffn < 1 || E < 1 || k < 1 || k > E ||
+        (dt != ORACLE_F32 && dt != ORACLE_BF16) || c0 < 0 || c1 > ffn || c0 > c1 || n0 < 0 ||
+        n1 > d || n0 > n1)
+        return ORACLE_BAD_ARG;
+    if (T == 0)
+        return ORACLE_OK;
+    if (!x || !Wg || !W1 || !W3 || !W2 || !dout)
+        return ORACLE_BAD_ARG;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    const size_t S = (size_t)T * k; /* (token, slot) pairs */
+    int *IDX = (int *)malloc(sizeof(int) * S);
+    double *G = (double *)malloc(sizeof(double) * S);
+    double *DL = (double *)malloc(sizeof(double) * S);
+    double *H = (double *)malloc(sizeof(double) * S * ffn);
+    double *DU = (double *)malloc(sizeof(double) * S * ffn);
+    double *DV = (double *)malloc(sizeof(double) * S * ffn);
+    double *DY = (double *)malloc(sizeof(double) * S * d);
+    if (!IDX || !G || !DL || !H || !DU || !DV || !DY) {
+        free(IDX); free(G); free(DL); free(H); free(DU); free(DV); free(DY);
+        return ORACLE_NO_MEM;
+    }
+    int status = ORACLE_OK;
+    /* phase 1, per token: forward again, then the backward down to the
+     * per-slot vectors and the token's input gradient */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int t = 0; t < T; ++t) {
+        float *l = (float *)malloc(sizeof(float) * (size_t)E);
+        double *u = (double *)malloc(sizeof(double) * (size_t)ffn);
+        double *v = (double *)malloc(sizeof(double) * (size_t)ffn);
+        double *dg = (double *)malloc(sizeof(double) * (size_t)k);
+        if (!l || !u || !v || !dg) {
+#pragma omp atomic write
+            status = ORACLE_NO_MEM;
+            free(l); free(u); free(v); free(dg);
+            continue;
+        }
+        const size_t xo = (size_t)t * d;
+        for (int e = 0; e < E; ++e)
+            l[e] = router_logit(x, xo, Wg, bias, d, e, dt);
+        if (!all_finite_f32(l, (size_t)E)) {
+#pragma omp atomic write
+            status = ORACLE_NONFINITE;
+        }
+        int *chosen = IDX + (size_t)t * k;
+        double *g = G + (size_t)t * k;
+        select_top_k(l, E, k, chosen);
+        gates_of(l, chosen, E, k, 0, g);
+        for (int i = 0; i < d; ++i)
+            if (dx)
+                dx[xo + (size_t)i] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            const int e = chosen[j];
+            const size_t sj = (size_t)t * k + j;
+            double *h = H + sj * ffn, *du = DU + sj * ffn, *dv = DV + sj * ffn;
+            double *dy = DY + sj * d;
+            for (int c = 0; c < ffn; ++c) {
+                double uu = 0.0, vv = 0.0;
+                for (int i = 0; i < d; ++i) {
+                    double xi = elem(x, xo + (size_t)i, dt);
+                    uu += xi * elem(W1[e], (size_t)c * d + i, dt);
+                    vv += xi * elem(W3[e], (size_t)c * d + i, dt);
+                }
+                u[c] = uu;
+                v[c] = vv;
+                h[c] = uu * logistic(uu) * vv;
+            }
+            /* y_j . dout and dy_j */
+            double dgj = 0.0;
+            for (int n = 0; n < d; ++n) {
+                double y = 0.0;
+                for (int c = 0; c < ffn; ++c)
+                    y += elem(W2[e], (size_t)n * ffn + c, dt) * h[c];
+                double o = elem(dout, xo + (size_t)n, dt);
+                dgj += o * y;
+                dy[n] = g[j] * o;
+            }
+            dg[j] = dgj;
+            /* dh = W2^T dy, then through the SwiGLU product */
+            for (int c = 0; c < ffn; ++c) {
+                double dh = 0.0;
+                for (int n = 0; n < d; ++n)
+                    dh += elem(W2[e], (size_t)n * ffn + c, dt) * dy[n];
+                double s = logistic(u[c]);
+                du[c] = dh * v[c] * (s + u[c] * s * (1.0 - s));
+                dv[c] = dh * u[c] * s;
+            }
+            if (dx)
+                for (int i = 0; i < d; ++i) {
+                    double acc = 0.0;
+                    for (int c = 0; c < ffn; ++c)
+                        acc += elem(W1[e], (size_t)c * d + i, dt) * du[c] +
+                               elem(W3[e], (size_t)c * d + i, dt) * dv[c];
+                    dx[xo + (size_t)i] += acc;
+                }
+        }
+        /* softmax over the kept logits */
+        double gdg = 0.0;
+        for (int j = 0; j < k; ++j)
+            gdg += g[j] * dg[j];
+        for (int j = 0; j < k; ++j)
+            DL[(size_t)t * k + j] = g[j] * (dg[j] - gdg);
+        if (dx)
+            for (int j = 0; j < k; ++j)
+                for (int i = 0; i < d; ++i)
+                    dx[xo + (size_t)i] +=
+                        DL[(size_t)t * k + j] * elem(Wg, (size_t)chosen[j] * d + i, dt);
+        free(l); free(u); free(v); free(dg);
+    }
+    /* phase 2, per weight-gradient row: sums over tokens in token order */
+    if (dWg) {
+#pragma omp parallel for schedule(static)
+        for (int e = 0; e < E; ++e)
+            for (int i = 0; i < d; ++i) {
+                double acc = 0.0;
+                for (size_t s = 0; s < S; ++s)
+                    if (IDX[s] == e)
+                        acc += DL[s] * elem(x, (s / (size_t)k) * d + (size_t)i, dt);
+                dWg[(size_t)e * d + i] = acc;
+            }
+    }
+    if (dW1 || dW3) {
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+        for (int e = 0; e < E; ++e)
+            for (int c = c0; c < c1; ++c)
+                for (int i = 0; i < d; ++i) {
+                    double a1 = 0.0, a3 = 0.0;
+                    for (size_t s = 0; s < S; ++s) {
+                        if (IDX[s] != e)
+                            continue;
+                        double xi = elem(x, (s / (size_t)k) * d + (size_t)i, dt);
+                        a1 += DU[s * ffn + c] * xi;
+                        a3 += DV[s * ffn + c] * xi;
+                    }
+                    if (dW1 && dW1[e])
+                        dW1[e][(size_t)(c - c0) * d + i] = a1;
+                    if (dW3 && dW3[e])
+                        dW3[e][(size_t)(c - c0) * d + i] = a3;
+                }
+    }
+    if (dW2) {
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+        for (int e = 0; e < E; ++e)
+            for (int n = n0; n < n1; ++n)
+                for (int c = 0; c < ffn; ++c) {
+                    double a = 0.0;
+                    for (size_t s = 0; s < S; ++s)
+                        if (IDX[s] == e)
+                            a += DY[s * d + n] * H[s * ffn + c];
+                    if (dW2[e])
+                        dW2[e][(size_t)(n - n0) * ffn + c] = a;
+                }
+    }
+    free(IDX); free(G); free(DL); free(H); free(DU); free(DV); free(DY);
+    return status;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP

@@ -572,4 +572,122 @@ def pin_page_shape_numbers(o=None):
     assert MIXTRAL_SHAPE["k"] / MIXTRAL_SHAPE["E"] == v["fraction_active"]
 
 
+# ---------------------------------------------------------------------------
+# Backward (gradients of sum(dout * layer(x)), for training).  Pinned to the
+# forward itself by finite differences, to torch's autograd on the layer with
+# the oracle's expert choice held fixed, and to properties of the softmax.
+# ---------------------------------------------------------------------------
+
+def _loss(o, x, Wg, W1, W3, W2, k, dout):
+    """sum(dout * exact layer output) and the expert choice, from the forward."""
+    _, _, idx, _, ex = o.moe_forward(x, Wg, W1, W3, W2, k, exact=True)
+    return float((ex * dout.astype(np.float64)).sum()), idx
+
+
+def pin_backward_finite_differences(o):
+    """For each input (x, W_g, all W1, all W3, all W2) and a random direction
+    R: L(P + hR) - L(P - hR) equals <grad, (P + hR) - (P - hR)> up to third-
+    order terms (L from the forward's exact output; the expert choice stays
+    the same under the perturbation)."""
+    rng = _rng(101)
+    T, d, ffn, E, k = 5, 12, 20, 4, 2
+    x, Wg, W1, W3, W2 = _rand_layer(rng, T, d, ffn, E)
+    dout = rng.standard_normal((T, d)).astype(np.float32)
+    g = o.moe_backward(x, Wg, W1, W3, W2, k, dout)
+    grads = dict(x=g["dx"], Wg=g["dWg"], W1=np.stack(g["dW1"]), W3=np.stack(g["dW3"]),
+                 W2=np.stack(g["dW2"]))
+    params = dict(x=x, Wg=Wg, W1=W1, W3=W3, W2=W2)
+    _, idx0 = _loss(o, x, Wg, W1, W3, W2, k, dout)
+    # W_g acts only through the logits, which the forward stores as fp32: the
+    # difference sees that rounding (~6e-8 absolute per logit), so it takes a
+    # larger step and a looser bound than the other inputs
+    steps = dict(x=(1e-3, 1e-5), Wg=(1e-2, 2e-4), W1=(1e-3, 1e-5), W3=(1e-3, 1e-5),
+                 W2=(1e-3, 1e-5))
+    for name, P in params.items():
+        R = rng.standard_normal(P.shape).astype(np.float32)
+        h, tol = steps[name]
+        Pp = (P + np.float32(h) * R).astype(np.float32)
+        Pm = (P - np.float32(h) * R).astype(np.float32)
+        lp, idxp = _loss(o, **{**params, name: Pp}, k=k, dout=dout)
+        lm, idxm = _loss(o, **{**params, name: Pm}, k=k, dout=dout)
+        assert np.array_equal(idxp, idx0) and np.array_equal(idxm, idx0), name
+        fd = lp - lm
+        an = float((grads[name] * (Pp.astype(np.float64) - Pm.astype(np.float64))).sum())
+        assert abs(fd - an) <= tol * abs(an) + 1e-10, (name, fd, an)
+
+
+def pin_backward_matches_autograd(o):
+    """torch float64 autograd of the layer written with torch ops (logits,
+    softmax over the oracle's kept experts, SwiGLU experts, weighted sum)
+    gives the same gradients for every input."""
+    rng = _rng(102)
+    T, d, ffn, E, k = 7, 10, 16, 5, 2
+    x, Wg, W1, W3, W2 = _rand_layer(rng, T, d, ffn, E)
+    dout = rng.standard_normal((T, d)).astype(np.float32)
+    g = o.moe_backward(x, Wg, W1, W3, W2, k, dout)
+    _, _, idx, _ = o.moe_forward(x, Wg, W1, W3, W2, k)
+    tx, tg, t1, t3, t2 = (torch.tensor(a, dtype=torch.float64, requires_grad=True)
+                          for a in (x, Wg, W1, W3, W2))
+    logits = tx @ tg.T
+    sel = torch.tensor(idx, dtype=torch.long)
+    gates = torch.softmax(torch.gather(logits, 1, sel), dim=1)
+    out = torch.zeros(T, d, dtype=torch.float64)
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            hid = torch.nn.functional.silu(t1[e] @ tx[t]) * (t3[e] @ tx[t])
+            out[t] = out[t] + gates[t, j] * (t2[e] @ hid)
+    (out * torch.tensor(dout, dtype=torch.float64)).sum().backward()
+    # the oracle's logits carry one fp32 rounding: agree to ~1e-7 relative
+    for got, ref in ((g["dx"], tx.grad), (g["dWg"], tg.grad), (np.stack(g["dW1"]), t1.grad),
+                     (np.stack(g["dW3"]), t3.grad), (np.stack(g["dW2"]), t2.grad)):
+        ref = ref.numpy()
+        assert np.allclose(got, ref, rtol=1e-5, atol=1e-7 * np.abs(ref).max()), \
+            float(np.abs(got - ref).max())
+
+
+def pin_backward_router_properties(o):
+    """The kept gates always sum to 1, so the logit gradients of a token sum
+    to 0 and sum_e dW_g[e] = 0; with one expert and k = 1 the gate is the
+    constant 1 and dW_g = 0; gradients are linear in dout (doubling dout
+    doubles every gradient exactly)."""
+    rng = _rng(103)
+    x, Wg, W1, W3, W2 = _rand_layer(rng, 9, 8, 12, 6)
+    dout = rng.standard_normal((9, 8)).astype(np.float32)
+    g = o.moe_backward(x, Wg, W1, W3, W2, 2, dout)
+    assert np.abs(g["dWg"].sum(axis=0)).max() <= 1e-12 * max(1.0, np.abs(g["dWg"]).max())
+    g2 = o.moe_backward(x, Wg, W1, W3, W2, 2, (2 * dout).astype(np.float32))
+    for key in ("dx", "dWg"):
+        assert np.array_equal(g2[key], 2 * g[key])
+    for key in ("dW1", "dW3", "dW2"):
+        assert all(np.array_equal(a, 2 * b) for a, b in zip(g2[key], g[key]))
+    x1, Wg1, W11, W31, W21 = _rand_layer(rng, 6, 8, 12, 1)
+    g1 = o.moe_backward(x1, Wg1, W11, W31, W21, 1, dout[:6])
+    assert np.all(g1["dWg"] == 0.0)
+
+
+def pin_backward_dtype_and_windows(o):
+    """bf16 inputs give the same gradients as their exact fp32 copies; the
+    weight-gradient row windows are slices of the full gradients."""
+    rng = _rng(104)
+    x, Wg, W1, W3, W2 = _rand_layer(rng, 6, 16, 24, 4)
+    dout = rng.standard_normal((6, 16)).astype(np.float32)
+    to_bf = lambda a: torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    to_f32 = lambda b: bf16_bits_to_f64(b).astype(np.float32)
+    bx, bg, b1, b3, b2, bd = (to_bf(a) for a in (x, Wg, W1, W3, W2, dout))
+    gb = o.moe_backward(bx, bg, list(b1), list(b3), list(b2), 2, bd)
+    gf = o.moe_backward(to_f32(bx), to_f32(bg), list(to_f32(b1)), list(to_f32(b3)),
+                        list(to_f32(b2)), 2, to_f32(bd))
+    for key in ("dx", "dWg"):
+        assert np.array_equal(gb[key], gf[key])
+    for key in ("dW1", "dW3", "dW2"):
+        assert all(np.array_equal(a, b) for a, b in zip(gb[key], gf[key]))
+    gw = o.moe_backward(x, Wg, W1, W3, W2, 2, dout, rows1=(5, 11), rows2=(3, 9))
+    gfull = o.moe_backward(x, Wg, W1, W3, W2, 2, dout)
+    for e in range(4):
+        assert np.array_equal(gw["dW1"][e], gfull["dW1"][e][5:11])
+        assert np.array_equal(gw["dW3"][e], gfull["dW3"][e][5:11])
+        assert np.array_equal(gw["dW2"][e], gfull["dW2"][e][3:9])
+
+
 ALL = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -44,6 +44,24 @@ MUTANTS = [
      "int e = j;\n            kept"),
     ("renorm_ignores_total", "g0[j] * total / kept_total", "g0[j] / kept_total"),
     ("dropped_row_kept_in_grouping", "if (!kept[(size_t)t * k + j]) {", "if (0) {"),
+    # backward
+    ("bwd_silu_prime_missing_term", "du[c] = dh * v[c] * (s + u[c] * s * (1.0 - s));",
+     "du[c] = dh * v[c] * s;"),
+    ("bwd_dv_uses_v", "dv[c] = dh * u[c] * s;", "dv[c] = dh * v[c] * s;"),
+    ("bwd_softmax_not_centred", "DL[(size_t)t * k + j] = g[j] * (dg[j] - gdg);",
+     "DL[(size_t)t * k + j] = g[j] * dg[j];"),
+    ("bwd_dx_without_router_term", "DL[(size_t)t * k + j] * elem(Wg, (size_t)chosen[j] * d + i, dt);",
+     "0.0 * elem(Wg, (size_t)chosen[j] * d + i, dt);"),
+    ("bwd_dy_ungated", "dy[n] = g[j] * o;", "dy[n] = o;"),
+    ("bwd_dW1_from_dv", "a1 += DU[s * ffn + c] * xi;", "a1 += DV[s * ffn + c] * xi;"),
+    ("bwd_dW2_shifted", "a += DY[s * d + n] * H[s * ffn + c];",
+     "a += DY[s * d + n] * H[s * ffn + (c + 1) % ffn];"),
+    ("bwd_dx_w1_transposed", "acc += elem(W1[e], (size_t)c * d + i, dt) * du[c] +",
+     "acc += elem(W1[e], (size_t)i * ffn + c, dt) * du[c] +"),
+    ("bwd_dWg_sign", "acc += DL[s] * elem(x, (s / (size_t)k) * d + (size_t)i, dt);",
+     "acc -= DL[s] * elem(x, (s / (size_t)k) * d + (size_t)i, dt);"),
+    ("bwd_dh_without_w2", "dh += elem(W2[e], (size_t)n * ffn + c, dt) * dy[n];",
+     "dh += dy[n];"),
 ]
 
 RUNNER = r"""
