@@ -155,6 +155,32 @@ int moe_block_forward(void *x, const void *W_g, const float *router_bias,
                       const moe_options *options, void *workspace, size_t workspace_bytes,
                       void *stream);
 
+/*
+ * Backward of the layer, for training ("Mixtral & Sparse MoE (2024) > The
+ * Solution" and "Mixtral of Experts" (azimuth.plus) describe training the
+ * model; no page prints the backward, which is the chain rule through the
+ * forward above).  For the upstream gradient d_out [T][d] (dtype) of the
+ * layer output it writes, overwriting:
+ *   d_x   [T][d] dtype          gradient of x (rounded once);
+ *   d_W_g [E][d] fp32           gradient of the router matrix;
+ *   d_W1[e], d_W3[e] [ffn][d] fp32 and d_W2[e] [d][ffn] fp32 (host arrays of E
+ *   device pointers, 16-byte aligned).
+ * Which experts a token picks is piecewise constant in the inputs, so no
+ * gradient flows through the choice; the softmax over the kept logits is
+ * differentiated.  Routing and the gate/up projections are recomputed from x,
+ * so nothing from a forward call has to be kept.  Every sum runs in a fixed
+ * order (no atomics): the gradients are deterministic.  Limits: dtype MOE_BF16
+ * (fp32 gives MOE_ERR_UNSUPPORTED) and the default routing (top-k softmax, no
+ * capacity limit).  router_bias may be NULL.  workspace: at least
+ * moe_backward_workspace_bytes(...) bytes, 256-byte aligned.
+ */
+int moe_backward_workspace_bytes(int T, int d, int ffn, int E, int k, int dtype, size_t *bytes);
+int moe_backward(const void *x, const void *W_g, const float *router_bias,
+                 const void *const *W1, const void *const *W3, const void *const *W2,
+                 int T, int d, int ffn, int E, int k, int dtype, const void *d_out, void *d_x,
+                 float *d_W_g, float *const *d_W1, float *const *d_W3, float *const *d_W2,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
 /* Capacity for a capacity factor: ceil(factor * T * k / E), written to
  * *capacity (factor <= 0 gives 0, i.e. no limit). */
 int moe_capacity(double capacity_factor, int T, int k, int E, int *capacity);

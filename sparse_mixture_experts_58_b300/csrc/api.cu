@@ -379,6 +379,125 @@ int check_forward_args(const void *x, const void *W_g, const void *const *W1,
     return MOE_OK;
 }
 
+// ---- backward ---------------------------------------------------------------
+
+// Scratch of the backward: routing arrays, then row buffers for the padded
+// grouping (each expert's block of rows padded to a multiple of 64).
+struct BwdPlan {
+    int T, d, ffn, E, k, rows, nchunks, nblk;
+    size_t o_logits, o_idx, o_gates, o_cc, o_cb, o_counts, o_offsets, o_perm, o_inv, o_gate;
+    size_t o_x, o_g, o_U, o_V, o_dU, o_dV, o_gH, o_dgp, o_dx, o_dl, o_part, bytes;
+};
+
+int make_bwd_plan(int T, int d, int ffn, int E, int k, int dt, BwdPlan *p) {
+    int rc = check_dims(T, d, ffn, E, k, dt);
+    if (rc != MOE_OK) return rc;
+    if (dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    BwdPlan q;
+    memset(&q, 0, sizeof q);
+    q.T = T;
+    q.d = d;
+    q.ffn = ffn;
+    q.E = E;
+    q.k = k;
+    q.rows = (T * k + 63) / 64 * 64 + 64 * E;
+    q.nchunks = (T + kChunk - 1) / kChunk;
+    q.nblk = ffn / 32;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes);
+        return o;
+    };
+    const size_t rows = (size_t)q.rows;
+    q.o_logits = take((size_t)T * E * 4);
+    q.o_idx = take((size_t)T * k * 4);
+    q.o_gates = take((size_t)T * k * 4);
+    q.o_cc = take((size_t)q.nchunks * E * 4);
+    q.o_cb = take((size_t)q.nchunks * E * 4);
+    q.o_counts = take((size_t)E * 4);
+    q.o_offsets = take((size_t)(E + 1) * 4);
+    q.o_perm = take(rows * 4);
+    q.o_inv = take((size_t)T * k * 4);
+    q.o_gate = take(rows * 4);
+    q.o_x = take(rows * d * 2);
+    q.o_g = take(rows * d * 2);
+    q.o_U = take(rows * ffn * 2);
+    q.o_V = take(rows * ffn * 2);
+    q.o_dU = take(rows * ffn * 2);
+    q.o_dV = take(rows * ffn * 2);
+    q.o_gH = take(rows * ffn * 2);
+    q.o_dgp = take(rows * q.nblk * 4);
+    q.o_dx = take(rows * d * 4);
+    q.o_dl = take((size_t)T * k * 4);
+    q.o_part = take(router_wg_part_floats(T, E, d) * 4);
+    q.bytes = off;
+    *p = q;
+    return MOE_OK;
+}
+
+int run_backward(const BwdPlan &P, const void *x, const void *W_g, const float *bias,
+                 const void *const *W1, const void *const *W3, const void *const *W2,
+                 const void *d_out, void *d_x, float *d_Wg, float *const *d_W1,
+                 float *const *d_W3, float *const *d_W2, void *ws, cudaStream_t s) {
+    const int T = P.T, d = P.d, ffn = P.ffn, E = P.E, k = P.k, rows = P.rows;
+    float *logits = ws_at<float>(ws, P.o_logits);
+    int *idx = ws_at<int>(ws, P.o_idx);
+    float *gates = ws_at<float>(ws, P.o_gates);
+    int *cc = ws_at<int>(ws, P.o_cc);
+    int *cb = ws_at<int>(ws, P.o_cb);
+    int *counts = ws_at<int>(ws, P.o_counts);
+    int *offsets = ws_at<int>(ws, P.o_offsets);
+    int *perm = ws_at<int>(ws, P.o_perm);
+    int *inv = ws_at<int>(ws, P.o_inv);
+    float *row_gate = ws_at<float>(ws, P.o_gate);
+    void *x_rows = ws_at<uint8_t>(ws, P.o_x);
+    void *g_rows = ws_at<uint8_t>(ws, P.o_g);
+    void *U = ws_at<uint8_t>(ws, P.o_U);
+    void *V = ws_at<uint8_t>(ws, P.o_V);
+    void *dU = ws_at<uint8_t>(ws, P.o_dU);
+    void *dV = ws_at<uint8_t>(ws, P.o_dV);
+    void *gH = ws_at<uint8_t>(ws, P.o_gH);
+    float *dgp = ws_at<float>(ws, P.o_dgp);
+    float *dx_rows = ws_at<float>(ws, P.o_dx);
+    float *dl = ws_at<float>(ws, P.o_dl);
+    float *part = ws_at<float>(ws, P.o_part);
+    int rc;
+    // routing again, grouped with each expert's rows padded to 64
+    if ((rc = cuda_rc(launch_router(x, W_g, bias, T, d, E, k, MOE_BF16, MOE_GATING_TOPK_SOFTMAX,
+                                    0.f, nullptr, logits, idx, gates, s))) != MOE_OK)
+        return rc;
+    if ((rc = cuda_rc(launch_chunk_scan(idx, T, k, E, 0, cc, cb, counts, offsets, s, 64))) !=
+        MOE_OK)
+        return rc;
+    if ((rc = cuda_rc(cudaMemsetAsync(perm, 0xFF, (size_t)rows * 4, s))) != MOE_OK) return rc;
+    if ((rc = cuda_rc(launch_group_tokens(idx, cb, offsets, nullptr, nullptr, T, 0, E, k, 0, 0,
+                                          perm, inv, nullptr, s))) != MOE_OK)
+        return rc;
+    if ((rc = cuda_rc(launch_gather_rows(x, perm, offsets, E, rows, k, d, nullptr, nullptr,
+                                         x_rows, s))) != MOE_OK)
+        return rc;
+    if ((rc = cuda_rc(launch_gather_rows(d_out, perm, offsets, E, rows, k, d, gates, row_gate,
+                                         g_rows, s))) != MOE_OK)
+        return rc;
+    // expert GEMMs
+    if ((rc = launch_bwd_uv(x_rows, offsets, W1, W3, rows, d, ffn, E, U, V, s)) != MOE_OK)
+        return rc;
+    if ((rc = launch_bwd_z(g_rows, offsets, W2, rows, d, ffn, E, U, V, row_gate, dU, dV, gH, dgp,
+                           s)) != MOE_OK)
+        return rc;
+    if ((rc = launch_bwd_dx(dU, dV, offsets, W1, W3, rows, d, ffn, E, dx_rows, s)) != MOE_OK)
+        return rc;
+    if ((rc = launch_bwd_wgrad(x_rows, g_rows, dU, dV, gH, offsets, rows, d, ffn, E, d_W1, d_W3,
+                               d_W2, s)) != MOE_OK)
+        return rc;
+    // router and input gradients
+    if ((rc = cuda_rc(launch_router_bwd(idx, gates, inv, dgp, P.nblk, dx_rows, W_g, T, d, k, dl,
+                                        d_x, s))) != MOE_OK)
+        return rc;
+    return cuda_rc(launch_router_wgrad(idx, dl, x, T, d, E, k, part, d_Wg, s));
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -407,6 +526,58 @@ int moe_workspace_bytes(int T, int d, int ffn, int E, int k, int dtype, size_t *
     if (rc != MOE_OK) return rc;
     *bytes = P.bytes;
     return MOE_OK;
+}
+
+int moe_backward_workspace_bytes(int T, int d, int ffn, int E, int k, int dtype, size_t *bytes) {
+    if (bytes == nullptr) return MOE_ERR_ARG;
+    BwdPlan P;
+    const int rc = make_bwd_plan(T, d, ffn, E, k, dtype, &P);
+    if (rc != MOE_OK) return rc;
+    *bytes = P.bytes;
+    return MOE_OK;
+}
+
+int moe_backward(const void *x, const void *W_g, const float *router_bias, const void *const *W1,
+                 const void *const *W3, const void *const *W2, int T, int d, int ffn, int E, int k,
+                 int dtype, const void *d_out, void *d_x, float *d_W_g, float *const *d_W1,
+                 float *const *d_W3, float *const *d_W2, void *workspace, size_t workspace_bytes,
+                 void *stream) {
+    BwdPlan P;
+    int rc = make_bwd_plan(T, d, ffn, E, k, dtype, &P);
+    if (rc != MOE_OK) return rc;
+    if ((rc = injected_fault()) != MOE_OK) return rc;
+    if (W_g == nullptr || d_W_g == nullptr || d_W1 == nullptr || d_W3 == nullptr ||
+        d_W2 == nullptr)
+        return MOE_ERR_ARG;
+    if ((rc = check_weights(W1, E)) != MOE_OK) return rc;
+    if ((rc = check_weights(W3, E)) != MOE_OK) return rc;
+    if ((rc = check_weights(W2, E)) != MOE_OK) return rc;
+    for (int e = 0; e < E; ++e)
+        if (d_W1[e] == nullptr || d_W3[e] == nullptr || d_W2[e] == nullptr)
+            return MOE_ERR_ARG;
+    for (int e = 0; e < E; ++e)
+        if (!aligned16(d_W1[e]) || !aligned16(d_W3[e]) || !aligned16(d_W2[e]))
+            return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(W_g) || !aligned16(d_W_g)) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        // no tokens: every gradient is zero
+        if (cudaMemsetAsync(d_W_g, 0, sizeof(float) * E * d, s) != cudaSuccess) return MOE_ERR_CUDA;
+        for (int e = 0; e < E; ++e) {
+            const size_t n = sizeof(float) * (size_t)ffn * d;
+            if (cudaMemsetAsync(d_W1[e], 0, n, s) != cudaSuccess ||
+                cudaMemsetAsync(d_W3[e], 0, n, s) != cudaSuccess ||
+                cudaMemsetAsync(d_W2[e], 0, n, s) != cudaSuccess)
+                return MOE_ERR_CUDA;
+        }
+        return MOE_OK;
+    }
+    if (x == nullptr || d_out == nullptr || d_x == nullptr) return MOE_ERR_ARG;
+    if (!aligned16(x) || !aligned16(d_out) || !aligned16(d_x)) return MOE_ERR_UNSUPPORTED;
+    if (workspace == nullptr || workspace_bytes < P.bytes) return MOE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return MOE_ERR_WORKSPACE;
+    return run_backward(P, x, W_g, router_bias, W1, W3, W2, d_out, d_x, d_W_g, d_W1, d_W3, d_W2,
+                        workspace, s);
 }
 
 int moe_forward_launches(int T, int d, int ffn, int E, int k, int dtype, int *launches) {

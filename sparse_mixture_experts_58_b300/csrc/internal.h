@@ -70,9 +70,11 @@ cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, in
                                     int *idx, float *gates, cudaStream_t s);
 // Per-chunk expert counts from idx (into chunk_counts), then their per-expert
 // exclusive scan: chunk_base; counts and offsets of the kept rows (capacity
-// <= 0: all rows).
+// <= 0: all rows).  pad > 1: each expert's block of rows starts on a multiple
+// of pad (offsets[e + 1] - offsets[e] = counts[e] rounded up to pad).
 cudaError_t launch_chunk_scan(const int *idx, int T, int k, int E, int capacity, int *chunk_counts,
-                              int *chunk_base, int *counts, int *offsets, cudaStream_t s);
+                              int *chunk_base, int *counts, int *offsets, cudaStream_t s,
+                              int pad = 1);
 // row_scale != nullptr: each copied row is multiplied by its token's scale
 // and rounded to the storage type (the fused RMSNorm).
 cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int *offsets,
@@ -97,6 +99,41 @@ int launch_swiglu_pair(const void *x_perm, const int *offsets, const void *const
 int launch_down_pair(const void *h, const int *offsets, const void *const *W2, int rows, int d,
                      int ffn, int E, int splits, int kps, float *y, cudaStream_t s);
 size_t pair_gemm_smem_bytes();
+
+// Backward of the expert GEMMs (gemm_bwd.cu), on rows grouped by expert with
+// each expert's block padded to a multiple of 64 (offsets).  rows: the row
+// capacity of the row buffers.
+int launch_bwd_uv(const void *x_rows, const int *offsets, const void *const *W1,
+                  const void *const *W3, int rows, int d, int ffn, int E, void *U, void *V,
+                  cudaStream_t s);
+int launch_bwd_z(const void *g_rows, const int *offsets, const void *const *W2, int rows, int d,
+                 int ffn, int E, const void *U, const void *V, const float *row_gate, void *dU,
+                 void *dV, void *gH, float *dgp, cudaStream_t s);
+int launch_bwd_dx(const void *dU, const void *dV, const int *offsets, const void *const *W1,
+                  const void *const *W3, int rows, int d, int ffn, int E, float *dx_rows,
+                  cudaStream_t s);
+int launch_bwd_wgrad(const void *x_rows, const void *g_rows, const void *dU, const void *dV,
+                     const void *gH, const int *offsets, int rows, int d, int ffn, int E,
+                     float *const *dW1, float *const *dW3, float *const *dW2, cudaStream_t s);
+size_t bwd_gemm_smem_bytes();
+
+// Backward helpers (bwd.cu).  Rows r < offsets[E] of dst get src[perm[r] / k]
+// (zero for padding rows, perm < 0); with gates, row_gate[r] = gates[perm[r]]
+// (0 for padding).
+cudaError_t launch_gather_rows(const void *src, const int *perm, const int *offsets, int E,
+                               int rows, int k, int d, const float *gates, float *row_gate,
+                               void *dst, cudaStream_t s);
+// Per token: dg of each slot (sum of the dgp blocks of its row), the logit
+// gradients of the kept softmax (dl [T][k]) and dx = sum_j dx_rows[row_j] +
+// sum_j dl_j W_g[e_j], rounded once to bf16.
+cudaError_t launch_router_bwd(const int *idx, const float *gates, const int *inv,
+                              const float *dgp, int nblk, const float *dx_rows, const void *Wg,
+                              int T, int d, int k, float *dl, void *dx, cudaStream_t s);
+// dWg[e] = sum over tokens (in token order) of dl[t][j] x[t] for idx[t][j] = e;
+// part: scratch of router_wg_part_floats(T, E, d) floats.
+size_t router_wg_part_floats(int T, int E, int d);
+cudaError_t launch_router_wgrad(const int *idx, const float *dl, const void *x, int T, int d,
+                                int E, int k, float *part, float *dWg, cudaStream_t s);
 cudaError_t launch_swiglu_f32(const float *x_perm, const int *offsets, const void *const *W1,
                               const void *const *W3, int rows, int d, int ffn, int E, float *h,
                               cudaStream_t s);

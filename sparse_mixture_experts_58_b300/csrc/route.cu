@@ -24,8 +24,8 @@ namespace {
 // global memory (cc); __syncthreads() orders the block's writes before its
 // reads.  Then warp w scans the columns of experts w and w + 32.
 __global__ void __launch_bounds__(1024) chunk_scan_kernel(const int *__restrict__ idx, int Tn,
-                                                          int k, int E, int capacity, int *cc,
-                                                          int *chunk_base, int *counts,
+                                                          int k, int E, int capacity, int pad,
+                                                          int *cc, int *chunk_base, int *counts,
                                                           int *offsets) {
     __shared__ int s_tot[MOE_MAX_EXPERTS];
     pdl_wait();
@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(1024) chunk_scan_kernel(const int *__restrict_
         offsets[0] = 0;
         for (int e = 0; e < E; ++e) {
             counts[e] = s_tot[e];
-            acc += s_tot[e];
+            acc += (s_tot[e] + pad - 1) / pad * pad;
             offsets[e + 1] = acc;
         }
     }
@@ -201,8 +201,8 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint8_t *__restrict_
 }  // namespace
 
 cudaError_t launch_chunk_scan(const int *idx, int T, int k, int E, int capacity, int *chunk_counts,
-                              int *chunk_base, int *counts, int *offsets, cudaStream_t s) {
-    return launch_pdl(chunk_scan_kernel, 1, 1024, 0, s, idx, T, k, E, capacity, chunk_counts,
+                              int *chunk_base, int *counts, int *offsets, cudaStream_t s, int pad) {
+    return launch_pdl(chunk_scan_kernel, 1, 1024, 0, s, idx, T, k, E, capacity, pad, chunk_counts,
                       chunk_base, counts, offsets);
 }
 

@@ -80,6 +80,9 @@ _sig("moe_forward_ex", _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
 _sig("moe_capacity", _i, ctypes.c_double, _i, _i, _i, _P(_i))
 _sig("moe_block_forward", _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_float,
      _P(Options), _vp, _sz, _vp)
+_sig("moe_backward_workspace_bytes", _i, _i, _i, _i, _i, _i, _i, _P(_sz))
+_sig("moe_backward", _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp,
+     _vp, _vp, _vp, _sz, _vp)
 _sig("moe_route_from_logits_ex", _i, _vp, _i, _i, _i, _P(Options), _vp, _vp, _vp, _vp, _vp, _vp,
      _vp, _sz, _vp)
 
@@ -89,7 +92,7 @@ EXPORTED = [
     "moe_expert_swiglu", "moe_down_splits", "moe_expert_down", "moe_combine",
     "moe_add_rmsnorm", "moe_device_status", "moe_selftest_wait_timeout", "moe_forward_launches",
     "moe_forward_static_scratch", "moe_forward_ex", "moe_capacity", "moe_route_from_logits_ex",
-    "moe_block_forward",
+    "moe_block_forward", "moe_backward_workspace_bytes", "moe_backward",
 ]
 
 
@@ -231,6 +234,38 @@ def block_forward(x, Wg, W1, W3, W2, k=2, bias=None, eps=1e-5, workspace=None, s
                                   float(eps), ctypes.byref(opt), _ptr(ws), ws.numel(),
                                   _stream(stream)), "moe_block_forward")
     return x
+
+
+def backward_workspace_bytes(T, d, ffn, E, k, dtype) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.moe_backward_workspace_bytes(T, d, ffn, E, k, dtype, ctypes.byref(n)),
+           "moe_backward_workspace_bytes")
+    return n.value
+
+
+def backward(x, Wg, W1, W3, W2, dout, k=2, bias=None, workspace=None, stream=None, grads=None):
+    """Gradients of sum(dout * layer(x)) through moe_backward: returns dict
+    dx [T,d] (x's dtype), dWg [E,d], dW1, dW3 [E,ffn,d] and dW2 [E,d,ffn]
+    (fp32).  ``grads`` may pass that dict to be overwritten."""
+    T, d, ffn, E = _shape(x, Wg, W1)
+    dt = _dt(x)
+    dev = x.device
+    if grads is None:
+        grads = dict(dx=torch.empty_like(x),
+                     dWg=torch.empty(E, d, dtype=torch.float32, device=dev),
+                     dW1=torch.empty(E, ffn, d, dtype=torch.float32, device=dev),
+                     dW3=torch.empty(E, ffn, d, dtype=torch.float32, device=dev),
+                     dW2=torch.empty(E, d, ffn, dtype=torch.float32, device=dev))
+    need = backward_workspace_bytes(T, d, ffn, E, k, dt)
+    ws = workspace.get(need) if isinstance(workspace, Workspace) else workspace
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    p1, p3, p2 = _expert_ptrs(W1, E), _expert_ptrs(W3, E), _expert_ptrs(W2, E)
+    g1, g3, g2 = (_expert_ptrs(grads[key], E) for key in ("dW1", "dW3", "dW2"))
+    _check(_lib.moe_backward(_ptr(x), _ptr(Wg), _ptr(bias), p1, p3, p2, T, d, ffn, E, k, dt,
+                             _ptr(dout), _ptr(grads["dx"]), _ptr(grads["dWg"]), g1, g3, g2,
+                             _ptr(ws), ws.numel(), _stream(stream)), "moe_backward")
+    return grads
 
 
 def forward_host_io(x_host, Wg, W1, W3, W2, k=2, bias=None, out_host=None, x_dev=None,

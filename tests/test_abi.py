@@ -168,3 +168,30 @@ def test_block_forward_validates_before_launch(moe):
     assert call(ws=None) == -3
     assert call(opt=ctypes.byref(moe.Options(2, 0, 0))) == -1
     assert call(T=0) == 0
+
+
+def test_backward_validates_before_launch(moe):
+    """moe_backward checks its arguments on the host: fp32 is not supported,
+    null and misaligned tensors and a missing workspace are rejected."""
+    E = 8
+    arr = ctypes.c_void_p * E
+    fake = ctypes.c_void_p(0x10000)
+    w = arr(*([0x10000] * E))
+    lib = moe.lib()
+
+    def call(x=fake, dt=moe.BF16, dWg=fake, ws=fake, ws_bytes=1 << 34, gW=w, dx=fake, d=256):
+        return lib.moe_backward(x, fake, None, w, w, w, 16, d, 512, E, 2, dt, fake, dx, dWg,
+                                gW, gW, gW, ws, ws_bytes, None)
+
+    assert call(dt=moe.F32) == -2
+    assert call(d=96) == -2
+    assert call(x=None) == -1
+    assert call(dx=None) == -1
+    assert call(dWg=None) == -1
+    assert call(gW=arr(*([0] * E))) == -1
+    assert call(x=ctypes.c_void_p(0x10008)) == -2
+    assert call(ws=None) == -3
+    n = ctypes.c_size_t()
+    assert lib.moe_backward_workspace_bytes(16, 256, 512, E, 2, moe.BF16, ctypes.byref(n)) == 0
+    assert n.value > 0
+    assert lib.moe_backward_workspace_bytes(16, 256, 512, E, 2, moe.F32, ctypes.byref(n)) == -2
