@@ -642,6 +642,127 @@ def measure_sweep(args, rank, world, local):
     return 0
 
 
+def backward_algorithmic(T, d, ffn, E, k, n_touched):
+    """FLOPs and bytes the layer's backward must move.  FLOPs: the gate/up
+    projections again (4 T k d ffn), Z = dout W2 (2), dX = dU W1 + dV W3 (4),
+    the three weight gradients (6), the router (4 T d E).  Bytes: W1 and W3
+    of the touched experts read twice and W2 once, the fp32 weight gradients
+    of every expert written (overwritten, zero for an untouched expert), x and
+    dout read, dx written, the router matrix and its gradient."""
+    flops = 16 * T * k * d * ffn + 4 * T * d * E
+    bytes_ = (n_touched * 5 * d * ffn * 2 + E * 3 * d * ffn * 4 + 3 * T * d * 2
+              + E * d * (2 + 4))
+    return flops, bytes_
+
+
+def measure_backward(args, rank, world, local):
+    """The layer's backward (moe_backward): CUDA-graph replays of one call per
+    step on the chosen workload, timed with CUDA events; the roofline counts
+    the backward's algorithmic work at the measured peaks."""
+    import torch
+
+    from sparse_mixture_experts_58_b300 import inputs, moe
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    cfg = dict(inputs.WORKLOADS[args.config])
+    overrides = []
+    for key in ("T", "E", "k"):
+        v = getattr(args, key)
+        if v:
+            cfg[key] = v
+            overrides.append(f"{key}={v}")
+    T, d, ffn, E, k = cfg["T"], cfg["d"], cfg["ffn"], cfg["E"], cfg["k"]
+    if cfg.get("bias") is not None and len(cfg["bias"]) != E:
+        cfg["bias"] = (list(cfg["bias"]) + [0.0] * E)[:E]
+    workload = "backward of the " + WORKLOAD_NAMES[args.config]
+    if overrides:
+        workload = f"{workload} ({'; '.join(overrides)})"
+    gen = inputs.generator(cfg["seed"], dev)
+    x0, _ = inputs.draw_tokens(gen, T, d, "bf16", dev, cfg.get("dup_frac", 0.0))
+    layer = inputs.draw_weights(gen, d, ffn, E, "bf16", dev, cfg.get("bias"))
+    tok_gen = inputs.generator(rank_token_seed(cfg["seed"] + 17, rank), dev)
+    if rank > 0:
+        x0, _ = inputs.draw_tokens(inputs.generator(rank_token_seed(cfg["seed"], rank), dev),
+                                   T, d, "bf16", dev, cfg.get("dup_frac", 0.0))
+    x = x0.contiguous()
+    dout = torch.randn(T, d, generator=tok_gen, device=dev).to(torch.bfloat16)
+    grads = dict(dx=torch.empty_like(x),
+                 dWg=torch.empty(E, d, dtype=torch.float32, device=dev),
+                 dW1=torch.empty(E, ffn, d, dtype=torch.float32, device=dev),
+                 dW3=torch.empty(E, ffn, d, dtype=torch.float32, device=dev),
+                 dW2=torch.empty(E, d, ffn, dtype=torch.float32, device=dev))
+    ws = moe.Workspace(dev)
+
+    def step():
+        moe.backward(x, layer.Wg, layer.W1, layer.W3, layer.W2, dout, k, bias=layer.bias,
+                     workspace=ws, grads=grads)
+
+    logits0, _, _ = moe.router(x, layer.Wg, k, layer.bias)
+    _, _, counts, _, _, _ = moe.route_from_logits(logits0, k)
+    n_touched = int((counts.cpu() > 0).sum())
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(local)
+    clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    barrier(world)
+    elapsed = reduce_max(e0.elapsed_time(e1) / 1e3, world, dev)
+    if moe.device_status(clear=True) != 0:
+        raise RuntimeError("device status set during the timed region")
+    if rank != 0:
+        return 0
+    peaks, peak_src = load_peaks()
+    flops, bytes_ = backward_algorithmic(T, d, ffn, E, k, n_touched)
+    t_step = elapsed / args.steps
+    t_hbm = bytes_ / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    bound = "hbm" if t_hbm > t_tc else "tensor"
+    achieved = (bytes_ / t_step / 1e9) if bound == "hbm" else (flops / t_step / 1e12)
+    peak = peaks["hbm_gbs"] if bound == "hbm" else peaks["bf16_tflops"]
+    line = {
+        "metric": "MoE-layer backward tokens/s (d4096 ffn14336 E8 top2 bf16; dx bf16, "
+                  "weight gradients fp32)",
+        "value": T * world / t_step, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded x~N(0,1), dout~N(0,1), weights~N(0,1/fan_in)",
+        "config": {"workload": workload, "T": T, "d": d, "ffn": ffn, "E": E, "k": k,
+                   "experts_touched": n_touched,
+                   "l2": "no flush: each step reads the weights and writes the fp32 weight "
+                         f"gradients ({(E * 3 * d * ffn * 4) / 1e9:.2f} GB) > 126 MB L2"},
+        "roofline": {"kernel": "whole backward (12 kernels)", "bound": bound,
+                     "achieved": achieved, "peak": peak,
+                     "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_src} (burst)", "traffic": None,
+                     "algorithmic_per_step": {"bytes": bytes_, "flops": flops},
+                     "roofline_us": max(t_hbm, t_tc) * 1e6},
+        "timed_as": "CUDA graph replay of one moe_backward call per step",
+        "gpu_launches": 12 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -661,6 +782,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="time direct moe_forward calls instead of a captured CUDA graph")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the layer's backward (moe_backward) instead of the forward")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -671,6 +794,8 @@ def main(argv=None):
         return run_reference(args, rank, world)
     if args.config == "sweep":
         return measure_sweep(args, rank, world, local)
+    if args.backward:
+        return measure_backward(args, rank, world, local)
     return measure(args, rank, world, local)
 
 

@@ -118,24 +118,42 @@ constexpr int kWgTokens = 256;
 __global__ void __launch_bounds__(kWgThreads) router_wgrad_part_kernel(
     const int *__restrict__ idx, const float *__restrict__ dl,
     const __nv_bfloat16 *__restrict__ x, int T, int d, int E, int k, float *part) {
+    // k <= 8 selections per token; the slice's expert ids and logit gradients
+    // are staged first so the token loop only waits on x
     __shared__ float s_acc[MOE_MAX_EXPERTS][kWgThreads];
+    __shared__ int s_e[kWgTokens * 4];
+    __shared__ float s_g[kWgTokens * 4];
     pdl_wait();
     pdl_trigger();
     const int i = blockIdx.x * kWgThreads + threadIdx.x;
     const int slice = blockIdx.y;
     for (int e = 0; e < E; ++e) s_acc[e][threadIdx.x] = 0.f;
-    const int t1 = min(T, (slice + 1) * kWgTokens);
-    if (i < d) {
-        for (int t = slice * kWgTokens; t < t1; ++t) {
-            const float xv = __bfloat162float(x[(size_t)t * d + i]);
-            for (int j = 0; j < k; ++j) {
-                const int e = idx[(size_t)t * k + j];
-                s_acc[e][threadIdx.x] = fmaf(dl[(size_t)t * k + j], xv, s_acc[e][threadIdx.x]);
+    const int t_first = slice * kWgTokens;
+    const int t1 = min(T, t_first + kWgTokens);
+    // tokens per stage so the staged selections fit (k <= 8)
+    const int tstep = (kWgTokens * 4) / k;
+    for (int ts = t_first; ts < t1; ts += tstep) {
+        const int te = min(t1, ts + tstep);
+        __syncthreads();
+        for (int q = threadIdx.x; q < (te - ts) * k; q += kWgThreads) {
+            s_e[q] = idx[(size_t)ts * k + q];
+            s_g[q] = dl[(size_t)ts * k + q];
+        }
+        __syncthreads();
+        if (i < d) {
+#pragma unroll 4
+            for (int t = ts; t < te; ++t) {
+                const float xv = __bfloat162float(x[(size_t)t * d + i]);
+                for (int j = 0; j < k; ++j) {
+                    const int q = (t - ts) * k + j;
+                    s_acc[s_e[q]][threadIdx.x] = fmaf(s_g[q], xv, s_acc[s_e[q]][threadIdx.x]);
+                }
             }
         }
+    }
+    if (i < d)
         for (int e = 0; e < E; ++e)
             part[((size_t)slice * E + e) * d + i] = s_acc[e][threadIdx.x];
-    }
 }
 
 // Second pass: dWg[e][i] = sum of the slices' partial sums in slice order.

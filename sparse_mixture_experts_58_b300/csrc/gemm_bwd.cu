@@ -59,7 +59,8 @@ constexpr int kBBytes = 2 * kBox;           // this CTA's half of the token / N 
 constexpr int kRing = kStages * (kABytes + kBBytes);
 constexpr int kBars = (2 * kStages + 6) * 8;
 constexpr int kMisc = 16 + 4 * (4 * kMaxE + 2);
-constexpr size_t kSmem = 1024 + kRing + kBars + kMisc;
+constexpr int kXpose = 4 * 32 * 33 * 4;  // kWG: a 32 x 32 fp32 tile per epilogue warp
+constexpr size_t kSmem = 1024 + kRing + kXpose + kBars + kMisc;
 constexpr uint32_t kAccCols = kMaxTok;
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr int kAccEmptyArrivals = 8;
@@ -91,7 +92,7 @@ struct BwdArgs {
     CUtensorMap act_a[3];        // kWG, box {64, 64}: dU, dV, G  ([rows][M])
     CUtensorMap act_b[3];        // kWG, box {64, 64}: X, X, gH   ([rows][N])
     const int *offsets;          // [E + 1] row offsets, multiples of 64
-    __nv_bfloat16 *U, *V;        // kUV out, kZ in: [rows][ffn]
+    __nv_bfloat16 *U, *V;        // kUV out, kZ in: feature-major [ffn][rows]
     __nv_bfloat16 *dU, *dV, *gH; // kZ out: [rows][ffn]
     const float *row_gate;       // kZ: [rows] gate of each row (0 for padding)
     float *dgp;                  // kZ: [rows][ffn / 32]
@@ -172,7 +173,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + kStages * kABytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRing);
+    float *xpose = reinterpret_cast<float *>(smem + kRing);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRing + kXpose);
     uint64_t *empty = full + kStages;
     uint64_t *acc_full = empty + kStages;
     uint64_t *acc_empty = acc_full + 2;
@@ -389,20 +391,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t tb = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                 static_cast<uint32_t>(acc) * kAccCols;
             if (MODE == kUV) {
-                // lanes 0-63: U of features wrow .. +63, lanes 64-127: V of the same
+                // lanes 0-63: U of features wrow .. +63, lanes 64-127: V of the
+                // same; stored feature-major, so a thread's 32 tokens are 64
+                // contiguous bytes
                 const int f = w.n0 + static_cast<int>(rank) * (kHalfM / 2) + 32 * (quad & 1) + lane;
-                __nv_bfloat16 *dst = (quad >= 2 ? a.V : a.U) + f;
+                __nv_bfloat16 *dst = (quad >= 2 ? a.V : a.U) + (size_t)f * a.rows;
                 const bool f_ok = f < a.ffn;
 #pragma unroll 1
                 for (int j0 = 0; j0 < w.ntok; j0 += 32) {
                     uint32_t R[32];
                     ptx::tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(j0), R);
                     ptx::tmem_ld_wait();
+                    if (!f_ok) continue;
+                    __nv_bfloat16 *row = dst + w.t0 + j0;
+                    if (j0 + 32 <= w.nvalid) {
+                        uint32_t pk[16];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (f_ok && j0 + i < w.nvalid)
-                            dst[(size_t)(w.t0 + j0 + i) * a.ffn] =
-                                __float2bfloat16_rn(__uint_as_float(R[i]));
+                        for (int i = 0; i < 16; ++i) {
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(
+                                __uint_as_float(R[2 * i]), __uint_as_float(R[2 * i + 1]));
+                            pk[i] = *reinterpret_cast<const uint32_t *>(&b2);
+                        }
+                        uint4 *v4 = reinterpret_cast<uint4 *>(row);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            v4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (j0 + i < w.nvalid) row[i] = __float2bfloat16_rn(__uint_as_float(R[i]));
+                    }
                 }
             } else if (MODE == kZ) {
                 const int f = w.n0 + static_cast<int>(rank) * kHalfM + 32 * quad + lane;
@@ -414,31 +432,75 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     uint32_t R[32];
                     ptx::tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(j0), R);
                     ptx::tmem_ld_wait();
-                    float mine = 0.f;
+                    float p[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int j = j0 + i;
-                        float p = 0.f;
-                        if (f_ok && j < w.nvalid) {
-                            const size_t o = (size_t)(w.t0 + j) * a.ffn + f;
-                            const float z = __uint_as_float(R[i]);
-                            const float gg = a.row_gate[w.t0 + j];
-                            const float uu = __bfloat162float(a.U[o]);
-                            const float vv = __bfloat162float(a.V[o]);
+                    for (int hb = 0; hb < 32; hb += 16) {
+                        // a half-chunk's inputs are loaded before any of its
+                        // stores: 16 tokens of U and V are 32 contiguous bytes
+                        // each (feature-major)
+                        // (a half starting below nvalid ends within the
+                        // expert's 16-aligned block of rows)
+                        float ub[16], vb[16], gb[16];
+                        const bool half_ok = f_ok && j0 + hb < w.nvalid;
+                        const size_t fo = (size_t)(f_ok ? f : 0) * a.rows + w.t0 + j0 + hb;
+                        const uint4 *u4 = reinterpret_cast<const uint4 *>(a.U + fo);
+                        const uint4 *v4 = reinterpret_cast<const uint4 *>(a.V + fo);
+                        const uint4 z4 = make_uint4(0, 0, 0, 0);
+                        const uint4 uq0 = half_ok ? u4[0] : z4, uq1 = half_ok ? u4[1] : z4;
+                        const uint4 vq0 = half_ok ? v4[0] : z4, vq1 = half_ok ? v4[1] : z4;
+                        {
+                            float t8[8];
+                            Vec<__nv_bfloat16>::unpack(uq0, t8);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) ub[i] = t8[i];
+                            Vec<__nv_bfloat16>::unpack(uq1, t8);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) ub[8 + i] = t8[i];
+                            Vec<__nv_bfloat16>::unpack(vq0, t8);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) vb[i] = t8[i];
+                            Vec<__nv_bfloat16>::unpack(vq1, t8);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) vb[8 + i] = t8[i];
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int j = j0 + hb + i;
+                            gb[i] = (f_ok && j < w.nvalid) ? a.row_gate[w.t0 + j] : 0.f;
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int j = j0 + hb + i;
+                            const float z = __uint_as_float(R[hb + i]);
+                            const float uu = ub[i], vv = vb[i];
                             const float sg = 1.f / (1.f + expf(-uu));
                             const float su = uu * sg;
                             const float h = su * vv;
-                            const float dh = gg * z;
-                            a.dU[o] = __float2bfloat16_rn(dh * vv * (sg + uu * sg * (1.f - sg)));
-                            a.dV[o] = __float2bfloat16_rn(dh * su);
-                            a.gH[o] = __float2bfloat16_rn(gg * h);
-                            p = h * z;
+                            const float dh = gb[i] * z;
+                            const bool ok = f_ok && j < w.nvalid;
+                            p[hb + i] = ok ? h * z : 0.f;
+                            if (ok) {
+                                const size_t o = (size_t)(w.t0 + j) * a.ffn + f;
+                                a.dU[o] = __float2bfloat16_rn(dh * vv * (sg + uu * sg * (1.f - sg)));
+                                a.dV[o] = __float2bfloat16_rn(dh * su);
+                                a.gH[o] = __float2bfloat16_rn(gb[i] * h);
+                            }
                         }
-                        p = warp_butterfly_sum(p);
-                        if (lane == i) mine = p;
+                    }
+                    // sum over the warp's 32 features for each of the 32 tokens:
+                    // halving exchanges leave lane l with token l's sum
+#pragma unroll
+                    for (int sft = 16; sft >= 1; sft >>= 1) {
+                        const bool upper = (lane & sft) != 0;
+#pragma unroll
+                        for (int i = 0; i < sft; ++i) {
+                            const float send = upper ? p[i] : p[i + sft];
+                            const float keep = upper ? p[i + sft] : p[i];
+                            p[i] = keep + __shfl_xor_sync(0xffffffffu, send, sft);
+                        }
                     }
                     if (j0 + lane < w.nvalid && cb < nblk)
-                        a.dgp[(size_t)(w.t0 + j0 + lane) * nblk + cb] = mine;
+                        a.dgp[(size_t)(w.t0 + j0 + lane) * nblk + cb] = p[0];
                 }
             } else if (MODE == kDX) {
                 const int f = w.n0 + static_cast<int>(rank) * kHalfM + 32 * quad + lane;
@@ -455,26 +517,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             col[(size_t)(w.t0 + j0 + i) * a.d] = __uint_as_float(R[i]);
                 }
             } else {
+                // each warp holds 32 rows x 32 columns per chunk; through a
+                // padded shared tile, each store writes one row's 32 columns
+                // (128 contiguous bytes)
                 const int M = a.wg_M[w.g], N = a.wg_N[w.g];
-                const int m = w.m0 + static_cast<int>(rank) * kHalfM + 32 * quad + lane;
+                const int mrow0 = w.m0 + static_cast<int>(rank) * kHalfM + 32 * quad;
                 const bool has_k = w.kb1 > w.kb0;
-                float *row = a.wgrad[w.g][w.e] + (size_t)m * N;
+                float *tile = xpose + (warp - 2) * 32 * 33;
+                float *out = a.wgrad[w.g][w.e];
 #pragma unroll 1
                 for (int j0 = 0; j0 < kMaxTok; j0 += 32) {
                     uint32_t R[32];
                     ptx::tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(j0), R);
                     ptx::tmem_ld_wait();
                     const int n = w.nw0 + j0;
-                    if (m < M && n < N) {
-                        float4 *dst = reinterpret_cast<float4 *>(row + n);
+                    if (n >= N) continue;
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[q] = has_k ? make_float4(__uint_as_float(R[4 * q]),
-                                                         __uint_as_float(R[4 * q + 1]),
-                                                         __uint_as_float(R[4 * q + 2]),
-                                                         __uint_as_float(R[4 * q + 3]))
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
+                    for (int i = 0; i < 32; ++i) tile[lane * 33 + i] = has_k ? __uint_as_float(R[i]) : 0.f;
+                    __syncwarp();
+#pragma unroll 4
+                    for (int i = 0; i < 32; ++i)
+                        if (mrow0 + i < M) out[(size_t)(mrow0 + i) * N + n + lane] = tile[i * 33 + lane];
+                    __syncwarp();
                 }
             }
             ptx::tc_fence_before_sync();
