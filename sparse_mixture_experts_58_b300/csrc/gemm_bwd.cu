@@ -59,7 +59,8 @@ constexpr int kBBytes = 2 * kBox;           // this CTA's half of the token / N 
 constexpr int kRing = kStages * (kABytes + kBBytes);
 constexpr int kBars = (2 * kStages + 6) * 8;
 constexpr int kMisc = 16 + 4 * (4 * kMaxE + 2);
-constexpr int kXpose = 4 * 32 * 33 * 4;  // kWG: a 32 x 32 fp32 tile per epilogue warp
+constexpr int kXpitch = 36;              // floats per row of the transpose tile (16-byte rows)
+constexpr int kXpose = 4 * 32 * kXpitch * 4;  // kWG: a 32 x 32 fp32 tile per epilogue warp
 constexpr size_t kSmem = 1024 + kRing + kXpose + kBars + kMisc;
 constexpr uint32_t kAccCols = kMaxTok;
 constexpr uint32_t kTmemCols = 2 * kAccCols;
@@ -518,13 +519,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             } else {
                 // each warp holds 32 rows x 32 columns per chunk; through a
-                // padded shared tile, each store writes one row's 32 columns
-                // (128 contiguous bytes)
+                // shared tile (rows padded to 36 floats: both phases free of
+                // bank conflicts), each 16-byte store of the warp writes 4 rows
+                // x 128 contiguous bytes
                 const int M = a.wg_M[w.g], N = a.wg_N[w.g];
                 const int mrow0 = w.m0 + static_cast<int>(rank) * kHalfM + 32 * quad;
                 const bool has_k = w.kb1 > w.kb0;
-                float *tile = xpose + (warp - 2) * 32 * 33;
+                float *tile = xpose + (warp - 2) * 32 * kXpitch;
                 float *out = a.wgrad[w.g][w.e];
+                const int rsub = lane >> 3, c4 = (lane & 7) * 4;
 #pragma unroll 1
                 for (int j0 = 0; j0 < kMaxTok; j0 += 32) {
                     uint32_t R[32];
@@ -532,12 +535,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     ptx::tmem_ld_wait();
                     const int n = w.nw0 + j0;
                     if (n >= N) continue;
+                    float4 *mine = reinterpret_cast<float4 *>(tile + lane * kXpitch);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) tile[lane * 33 + i] = has_k ? __uint_as_float(R[i]) : 0.f;
+                    for (int q = 0; q < 8; ++q)
+                        mine[q] = has_k ? make_float4(__uint_as_float(R[4 * q]),
+                                                      __uint_as_float(R[4 * q + 1]),
+                                                      __uint_as_float(R[4 * q + 2]),
+                                                      __uint_as_float(R[4 * q + 3]))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
                     __syncwarp();
-#pragma unroll 4
-                    for (int i = 0; i < 32; ++i)
-                        if (mrow0 + i < M) out[(size_t)(mrow0 + i) * N + n + lane] = tile[i * 33 + lane];
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const int row = 4 * r + rsub;
+                        const float4 v = *reinterpret_cast<const float4 *>(tile + row * kXpitch + c4);
+                        if (mrow0 + row < M)
+                            *reinterpret_cast<float4 *>(out + (size_t)(mrow0 + row) * N + n + c4) = v;
+                    }
                     __syncwarp();
                 }
             }
