@@ -113,25 +113,31 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(
 // Router-matrix gradient, first pass: block (column chunk, token slice)
 // accumulates, for every expert, dl * x over its slice's tokens in order.
 constexpr int kWgThreads = 128;
-constexpr int kWgTokens = 256;
+constexpr int kWgTokens = 64;
 
+template <int EREG>
 __global__ void __launch_bounds__(kWgThreads) router_wgrad_part_kernel(
     const int *__restrict__ idx, const float *__restrict__ dl,
     const __nv_bfloat16 *__restrict__ x, int T, int d, int E, int k, float *part) {
-    // k <= 8 selections per token; the slice's expert ids and logit gradients
-    // are staged first so the token loop only waits on x
-    __shared__ float s_acc[MOE_MAX_EXPERTS][kWgThreads];
+    // The slice's expert ids and logit gradients are staged in shared memory
+    // first, so the token loop waits on x only.  EREG > 0 (E <= EREG): one
+    // register accumulator per expert, each selection added with a compare
+    // and select; otherwise accumulators in shared memory.
+    __shared__ float s_acc[EREG > 0 ? 1 : MOE_MAX_EXPERTS][kWgThreads];
     __shared__ int s_e[kWgTokens * 4];
     __shared__ float s_g[kWgTokens * 4];
     pdl_wait();
     pdl_trigger();
     const int i = blockIdx.x * kWgThreads + threadIdx.x;
     const int slice = blockIdx.y;
-    for (int e = 0; e < E; ++e) s_acc[e][threadIdx.x] = 0.f;
+    float acc[EREG > 0 ? EREG : 1];
+#pragma unroll
+    for (int e = 0; e < (EREG > 0 ? EREG : 1); ++e) acc[e] = 0.f;
+    if (EREG == 0)
+        for (int e = 0; e < E; ++e) s_acc[e][threadIdx.x] = 0.f;
     const int t_first = slice * kWgTokens;
     const int t1 = min(T, t_first + kWgTokens);
-    // tokens per stage so the staged selections fit (k <= 8)
-    const int tstep = (kWgTokens * 4) / k;
+    const int tstep = (kWgTokens * 4) / k;  // tokens per staging round (k <= 8)
     for (int ts = t_first; ts < t1; ts += tstep) {
         const int te = min(t1, ts + tstep);
         __syncthreads();
@@ -146,14 +152,21 @@ __global__ void __launch_bounds__(kWgThreads) router_wgrad_part_kernel(
                 const float xv = __bfloat162float(x[(size_t)t * d + i]);
                 for (int j = 0; j < k; ++j) {
                     const int q = (t - ts) * k + j;
-                    s_acc[s_e[q]][threadIdx.x] = fmaf(s_g[q], xv, s_acc[s_e[q]][threadIdx.x]);
+                    const int e = s_e[q];
+                    const float gx = s_g[q] * xv;
+                    if (EREG > 0) {
+#pragma unroll
+                        for (int r = 0; r < (EREG > 0 ? EREG : 1); ++r) acc[r] += (e == r) ? gx : 0.f;
+                    } else {
+                        s_acc[e][threadIdx.x] += gx;
+                    }
                 }
             }
         }
     }
     if (i < d)
         for (int e = 0; e < E; ++e)
-            part[((size_t)slice * E + e) * d + i] = s_acc[e][threadIdx.x];
+            part[((size_t)slice * E + e) * d + i] = EREG > 0 ? acc[e < EREG ? e : 0] : s_acc[e][threadIdx.x];
 }
 
 // Second pass: dWg[e][i] = sum of the slices' partial sums in slice order.
@@ -200,10 +213,12 @@ cudaError_t launch_router_wgrad(const int *idx, const float *dl, const void *x, 
                                 int E, int k, float *part, float *dWg, cudaStream_t s) {
     const int slices = (T + kWgTokens - 1) / kWgTokens;
     if (slices == 0) return cudaMemsetAsync(dWg, 0, sizeof(float) * E * d, s);
-    cudaError_t e = launch_pdl(router_wgrad_part_kernel, dim3((d + kWgThreads - 1) / kWgThreads,
-                                                             slices),
-                               kWgThreads, 0, s, idx, dl, static_cast<const __nv_bfloat16 *>(x),
-                               T, d, E, k, part);
+    const dim3 grid((d + kWgThreads - 1) / kWgThreads, slices);
+    const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
+    cudaError_t e = E <= 8 ? launch_pdl(router_wgrad_part_kernel<8>, grid, kWgThreads, 0, s, idx,
+                                        dl, xb, T, d, E, k, part)
+                           : launch_pdl(router_wgrad_part_kernel<0>, grid, kWgThreads, 0, s, idx,
+                                        dl, xb, T, d, E, k, part);
     if (e != cudaSuccess) return e;
     const size_t n = (size_t)E * d;
     return launch_pdl(router_wgrad_sum_kernel, (unsigned)((n + 255) / 256), 256, 0, s,

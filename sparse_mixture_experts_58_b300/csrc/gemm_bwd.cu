@@ -35,7 +35,13 @@
 // N) LBO = 8 KB apart, groups of 8 contraction rows SBO = 1 KB apart, and a
 // 16-deep MMA step advances the start by 16 rows (2 KB).
 //
-// Barriers, roles and bounded waits as in gemm_pair.cu.
+// Roles as in gemm_pair.cu (warp 0 TMA, warp 1 MMA), but with eight
+// epilogue warps: the two warps on each tensor-memory lane quarter take
+// alternate 32-column chunks, since the kZ and kWG epilogues do more work per
+// element than one warp per quarter hides behind the MMAs.  Five 32 KB ring
+// stages leave room for the kWG transpose tiles.  Barriers and bounded waits as
+// in gemm_pair.cu (an accumulator is released by all 16 epilogue warps of the
+// pair).
 #include <string.h>
 
 #include <mutex>
@@ -50,9 +56,10 @@ constexpr int kPairM = 256;
 constexpr int kHalfM = 128;
 constexpr int kMaxTok = 256;
 constexpr int kTokMaps = kMaxTok / 16;
-constexpr int kStages = 6;
+constexpr int kStages = 5;
 constexpr int kMaxE = MOE_MAX_EXPERTS;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;  // two per tensor-memory lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kBox = 64 * 128;              // one 64 x 64 bf16 box
 constexpr int kABytes = 2 * kBox;           // 128 weight-side rows x 64, or 64 x 128 MN-major
 constexpr int kBBytes = 2 * kBox;           // this CTA's half of the token / N side
@@ -60,11 +67,11 @@ constexpr int kRing = kStages * (kABytes + kBBytes);
 constexpr int kBars = (2 * kStages + 6) * 8;
 constexpr int kMisc = 16 + 4 * (4 * kMaxE + 2);
 constexpr int kXpitch = 36;              // floats per row of the transpose tile (16-byte rows)
-constexpr int kXpose = 4 * 32 * kXpitch * 4;  // kWG: a 32 x 32 fp32 tile per epilogue warp
+constexpr int kXpose = kEpiWarps * 32 * kXpitch * 4;  // kWG: a 32 x 32 fp32 tile per epilogue warp
 constexpr size_t kSmem = 1024 + kRing + kXpose + kBars + kMisc;
 constexpr uint32_t kAccCols = kMaxTok;
 constexpr uint32_t kTmemCols = 2 * kAccCols;
-constexpr int kAccEmptyArrivals = 8;
+constexpr int kAccEmptyArrivals = 2 * kEpiWarps;  // lane 0 of each epilogue warp, both CTAs
 constexpr uint16_t kBothCtas = 0x3;
 
 enum Mode { kUV = 0, kZ = 1, kDX = 2, kWG = 3 };
@@ -378,7 +385,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        // warps w and w + 4 read the same lane quarter (w % 4) and take
+        // alternate 32-column chunks
         const int quad = warp & 3;
+        const int c_first = 32 * ((warp - 2) >> 2);
         const uint32_t acc_empty0 = ptx::map_to_rank(ptx::smem_addr(&acc_empty[0]), 0);
         int it = 0;
         for (int u = first; u < total; u += stride, ++it) {
@@ -399,7 +409,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 __nv_bfloat16 *dst = (quad >= 2 ? a.V : a.U) + (size_t)f * a.rows;
                 const bool f_ok = f < a.ffn;
 #pragma unroll 1
-                for (int j0 = 0; j0 < w.ntok; j0 += 32) {
+                for (int j0 = c_first; j0 < w.ntok; j0 += 64) {
                     uint32_t R[32];
                     ptx::tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(j0), R);
                     ptx::tmem_ld_wait();
@@ -426,29 +436,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             } else if (MODE == kZ) {
                 const int f = w.n0 + static_cast<int>(rank) * kHalfM + 32 * quad + lane;
                 const bool f_ok = f < a.ffn;
+                const int fs = f_ok ? f : 0;
                 const int nblk = a.ffn / 32;
                 const int cb = (w.n0 + static_cast<int>(rank) * kHalfM + 32 * quad) / 32;
+                const size_t ld = a.ffn;
 #pragma unroll 1
-                for (int j0 = 0; j0 < w.ntok; j0 += 32) {
+                for (int j0 = c_first; j0 < w.ntok; j0 += 64) {
                     uint32_t R[32];
                     ptx::tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(j0), R);
+                    // lane i fetches token j0 + i's gate; the warp shares them
+                    const float my_gate = j0 + lane < w.nvalid ? a.row_gate[w.t0 + j0 + lane] : 0.f;
                     ptx::tmem_ld_wait();
                     float p[32];
 #pragma unroll
                     for (int hb = 0; hb < 32; hb += 16) {
                         // a half-chunk's inputs are loaded before any of its
                         // stores: 16 tokens of U and V are 32 contiguous bytes
-                        // each (feature-major)
-                        // (a half starting below nvalid ends within the
-                        // expert's 16-aligned block of rows)
-                        float ub[16], vb[16], gb[16];
-                        const bool half_ok = f_ok && j0 + hb < w.nvalid;
-                        const size_t fo = (size_t)(f_ok ? f : 0) * a.rows + w.t0 + j0 + hb;
+                        // each (feature-major); a half starting below nvalid
+                        // ends within the expert's 16-aligned block of rows
+                        const int nv = min(16, w.nvalid - (j0 + hb));  // valid tokens in the half
+                        const bool half_ok = f_ok && nv > 0;
+                        const size_t fo = (size_t)fs * a.rows + w.t0 + j0 + hb;
                         const uint4 *u4 = reinterpret_cast<const uint4 *>(a.U + fo);
                         const uint4 *v4 = reinterpret_cast<const uint4 *>(a.V + fo);
                         const uint4 z4 = make_uint4(0, 0, 0, 0);
                         const uint4 uq0 = half_ok ? u4[0] : z4, uq1 = half_ok ? u4[1] : z4;
                         const uint4 vq0 = half_ok ? v4[0] : z4, vq1 = half_ok ? v4[1] : z4;
+                        float ub[16], vb[16];
                         {
                             float t8[8];
                             Vec<__nv_bfloat16>::unpack(uq0, t8);
@@ -464,27 +478,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int i = 0; i < 8; ++i) vb[8 + i] = t8[i];
                         }
+                        const size_t ro = (size_t)(w.t0 + j0 + hb) * ld + fs;
+                        __nv_bfloat16 *pdu = a.dU + ro, *pdv = a.dV + ro, *pgh = a.gH + ro;
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const int j = j0 + hb + i;
-                            gb[i] = (f_ok && j < w.nvalid) ? a.row_gate[w.t0 + j] : 0.f;
-                        }
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int j = j0 + hb + i;
                             const float z = __uint_as_float(R[hb + i]);
+                            const float g = __shfl_sync(0xffffffffu, my_gate, hb + i);
                             const float uu = ub[i], vv = vb[i];
-                            const float sg = 1.f / (1.f + expf(-uu));
+                            // logistic with the fast exponential and reciprocal:
+                            // their ~1e-6 relative error vanishes next to the
+                            // bf16 rounding of everything this feeds
+                            const float sg = __frcp_rn(1.f + __expf(-uu));
                             const float su = uu * sg;
                             const float h = su * vv;
-                            const float dh = gb[i] * z;
-                            const bool ok = f_ok && j < w.nvalid;
+                            const float dh = g * z;
+                            const bool ok = half_ok && i < nv;
                             p[hb + i] = ok ? h * z : 0.f;
                             if (ok) {
-                                const size_t o = (size_t)(w.t0 + j) * a.ffn + f;
-                                a.dU[o] = __float2bfloat16_rn(dh * vv * (sg + uu * sg * (1.f - sg)));
-                                a.dV[o] = __float2bfloat16_rn(dh * su);
-                                a.gH[o] = __float2bfloat16_rn(gb[i] * h);
+                                pdu[(size_t)i * ld] =
+                                    __float2bfloat16_rn(dh * vv * (sg + uu * sg * (1.f - sg)));
+                                pdv[(size_t)i * ld] = __float2bfloat16_rn(dh * su);
+                                pgh[(size_t)i * ld] = __float2bfloat16_rn(g * h);
                             }
                         }
                     }
@@ -508,7 +522,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 float *col = a.dx_rows + f;
                 const bool f_ok = f < a.d;
 #pragma unroll 1
-                for (int j0 = 0; j0 < w.ntok; j0 += 32) {
+                for (int j0 = c_first; j0 < w.ntok; j0 += 64) {
                     uint32_t R[32];
                     ptx::tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(j0), R);
                     ptx::tmem_ld_wait();
@@ -529,7 +543,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 float *out = a.wgrad[w.g][w.e];
                 const int rsub = lane >> 3, c4 = (lane & 7) * 4;
 #pragma unroll 1
-                for (int j0 = 0; j0 < kMaxTok; j0 += 32) {
+                for (int j0 = c_first; j0 < kMaxTok; j0 += 64) {
                     uint32_t R[32];
                     ptx::tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(j0), R);
                     ptx::tmem_ld_wait();
