@@ -19,13 +19,17 @@
 // The accumulator is feature-major (lane = feature, column = token), so the
 // epilogue writes, per token, 32 consecutive features from one warp.
 //
+// Roles: warp 0 issues TMA copies, warp 1 the MMAs (even CTA), warps 2-9 are
+// the epilogue: two warps per tensor-memory lane quarter taking alternate
+// 32-token chunks.
+//
 // Barriers (same offsets in both CTAs):
 //   full[s]      even CTA only: one arrival with the stage's byte count from
 //                the even CTA's producer; both CTAs' TMA copies complete
 //                bytes on it;
 //   empty[s]     both CTAs: the even CTA's MMA commit multicasts to both;
 //   acc_full[a]  both CTAs: MMA commit multicast, read by each epilogue;
-//   acc_empty[a] even CTA only: one arrival per epilogue warp of both CTAs;
+//   acc_empty[a] even CTA only: one arrival per epilogue warp of both CTAs (16);
 //   drain, bye   teardown: the MMA drain, and a pair handshake so neither CTA
 //                leaves while the other may still touch its shared memory.
 // Every wait is bounded as in gemm_tc.cu.
@@ -44,19 +48,21 @@ constexpr int kTokMaps = kMaxTok / 16;  // token tensor maps, box heights 8, 16,
 constexpr int kGate = kHalfM / 2;  // gate/up: W1 rows, then the same rows of W3, per CTA
 constexpr int kStages = 6;
 constexpr int kMaxE = MOE_MAX_EXPERTS;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;  // two per tensor-memory lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kABytes = kHalfM * 128;       // weights, 64-wide contraction slice
 constexpr int kBBytes = (kMaxTok / 2) * 128;  // tokens, this CTA's half
 constexpr int kRing = kStages * (kABytes + kBBytes);
-// gate/up exchange: [warp pair 2][chunk parity 2][direction 2][16 tokens][32 lanes] fp32
+// gate/up exchange: [warp pair 4][chunk parity 2][direction 2][16 tokens][32 lanes] fp32
+constexpr int kXchPairs = kEpiWarps / 2;
 constexpr int kXchFloats = 16 * 32;
-constexpr int kXch = 2 * 2 * 2 * kXchFloats * 4;
-constexpr int kBars = (2 * kStages + 8) * 8;
+constexpr int kXch = kXchPairs * 2 * 2 * kXchFloats * 4;
+constexpr int kBars = (2 * kStages + 6 + kXchPairs) * 8;
 constexpr int kMisc = 16 + 4 * (4 * kMaxE + 2);
 constexpr size_t kSmem = 1024 + kRing + kXch + kBars + kMisc;
 constexpr uint32_t kAccCols = kMaxTok;
 constexpr uint32_t kTmemCols = 2 * kAccCols;
-constexpr int kAccEmptyArrivals = 8;  // lane 0 of the 4 epilogue warps of each CTA
+constexpr int kAccEmptyArrivals = 2 * kEpiWarps;  // lane 0 of each epilogue warp, both CTAs
 constexpr uint16_t kBothCtas = 0x3;
 
 struct PairArgs {
@@ -127,8 +133,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *drain = acc_empty + 2;
     uint64_t *bye = drain + 1;
-    uint64_t *xbar = bye + 1;  // [2] gate/up exchange, one per epilogue warp pair
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xbar + 2);
+    uint64_t *xbar = bye + 1;  // [kXchPairs] gate/up exchange, one per epilogue warp pair
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xbar + kXchPairs);
     volatile int *s_abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *s_bye_ok = reinterpret_cast<volatile int *>(tmem_slot + 2);
     int *s_off = reinterpret_cast<int *>(tmem_slot + 4);  // [kMaxE + 1]
@@ -153,8 +159,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         ptx::mbar_init(drain, 1);
         ptx::mbar_init(bye, 1);
-        ptx::mbar_init(&xbar[0], 2);
-        ptx::mbar_init(&xbar[1], 2);
+        for (int i = 0; i < kXchPairs; ++i) ptx::mbar_init(&xbar[i], 2);
         *s_abort = 0;
         *s_bye_ok = 0;
         ptx::fence_barrier_init();
@@ -300,10 +305,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;  // tensor-memory lanes 32*quad .. +31
+        // warps w and w + 4 read the same lane quarter and take alternate
+        // 32-token chunks
+        const int cset = (warp - 2) >> 2;
         const uint32_t acc_empty0 = ptx::map_to_rank(ptx::smem_addr(&acc_empty[0]), 0);
         // gate/up: quarters 0 and 1 hold the gate values of features 0-31 and
         // 32-63, quarters 2 and 3 the up values of the same features
-        const int pairq = quad & 1;
+        const int pairq = (quad & 1) + 2 * cset;
         const bool is_up = quad >= 2;
         float *xb = xch + pairq * (2 * 2 * kXchFloats);
         uint32_t xk = 0;  // exchanges done by this warp pair
@@ -322,11 +330,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (SWIGLU) {
                 // the gate warp finishes each chunk's first 16 tokens, the up
                 // warp the last 16; each sends the other the values it needs
-                const int f = w.n0 + static_cast<int>(rank) * kGate + pairq * 32 + lane;
+                const int f = w.n0 + static_cast<int>(rank) * kGate + (quad & 1) * 32 + lane;
                 __nv_bfloat16 *hcol = static_cast<__nv_bfloat16 *>(a.out) + f;
                 const bool f_ok = f < a.N;
 #pragma unroll 1
-                for (int j0 = 0; j0 < w.ntok; j0 += 32) {
+                for (int j0 = 32 * cset; j0 < w.ntok; j0 += 64) {
                     uint32_t V[32];
                     ptx::tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(j0), V);
                     ptx::tmem_ld_wait();
@@ -362,7 +370,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 float *ycol = static_cast<float *>(a.out) + (size_t)w.ks * a.rows * a.N + f;
                 const bool f_ok = f < a.N;
 #pragma unroll 1
-                for (int j0 = 0; j0 < w.ntok; j0 += 32) {
+                for (int j0 = 32 * cset; j0 < w.ntok; j0 += 64) {
                     uint32_t Y[32];
                     ptx::tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(j0), Y);
                     ptx::tmem_ld_wait();
