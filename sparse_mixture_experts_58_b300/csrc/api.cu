@@ -227,18 +227,40 @@ int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p) {
         const int kblocks = (ffn + kBlockK - 1) / kBlockK;
         const long long busy = q.rows < E ? q.rows : E;
         long long s = 1;
+        const long long smax = kblocks / 8 > 0 ? kblocks / 8 : 1;
+        // Split the down projection's contraction so every SM (pair) has work:
+        // among the splits giving lo..hi units per worker, the one whose last
+        // wave is fullest (fewer splits on a tie: less partial-sum traffic).
+        auto balanced = [&](long long base_units, long long workers, long long lo, long long hi) {
+            if (base_units <= 0) return 1LL;
+            long long best = 1;
+            double best_eff = -1.0;
+            const long long s_lo = (lo * workers + base_units - 1) / base_units;
+            const long long s_hi = (hi * workers + base_units - 1) / base_units;
+            for (long long c = s_lo < 1 ? 1 : s_lo; c <= s_hi && c <= smax; ++c) {
+                const long long units = base_units * c;
+                const long long waves = (units + workers - 1) / workers;
+                const double eff = (double)units / (double)(waves * workers);
+                if (eff > best_eff + 1e-9) {
+                    best_eff = eff;
+                    best = c;
+                }
+            }
+            return best;
+        };
         if (q.pair) {
             // down-projection units: 256 features x one token tile of <= 256
-            // rows; split the contraction until each pair has about 4 units
+            // rows; about 4 units per pair (measured: a fuller last wave does
+            // not pay for more fp32 partial sums here, T=1024: 3 splits 692 us,
+            // 4 splits 727 us)
             const long long ttiles = busy > (q.rows + 255) / 256 ? busy : (q.rows + 255) / 256;
             const long long base_units = ttiles * ((d + 255) / 256);
             s = (4LL * (kPlanSms / 2) + base_units - 1) / base_units;
         } else if (!q.wide) {
-            // one 128-feature x 128-row tile per busy expert; about 8 units per SM
-            const long long base_units = busy * ((d + 127) / 128);
-            s = base_units > 0 ? (8LL * kPlanSms + base_units - 1) / base_units : 1;
+            // one 128-feature x 128-row tile per busy expert (decode: 4 splits,
+            // 1024 units = 6.9 waves, 482 us per step against 484 us with 5)
+            s = balanced(busy * ((d + 127) / 128), kPlanSms, 4, 12);
         }
-        const long long smax = kblocks / 8 > 0 ? kblocks / 8 : 1;
         if (s > smax) s = smax;
         if (s < 1) s = 1;
         if (const char *sp = getenv("MOE_PLAN_SPLITS")) s = atoi(sp) > 0 ? atoi(sp) : s;
