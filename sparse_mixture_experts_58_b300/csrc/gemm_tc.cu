@@ -92,9 +92,10 @@ template <int NB, int STAGES, bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_constant__ TcArgs a) {
     using L = SmemLayout<NB, STAGES>;
     constexpr int NOUT = SWIGLU ? NB / 2 : NB;
-    constexpr uint32_t kTmemCols = 2 * NB;
+    // two NB-column accumulators, allocated as a power of two
+    constexpr uint32_t kTmemCols = 2 * NB <= 256 ? 256 : 512;
     constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, NB);
-    static_assert(kTmemCols == 256 || kTmemCols == 512, "accumulators must fill a power of two");
+    static_assert(2 * NB <= 512, "two accumulators must fit tensor memory");
     static_assert(NB % 16 == 0 && NB <= 256, "MMA N for M = 128");
 
     extern __shared__ uint8_t smem_raw[];
@@ -279,7 +280,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_cons
                         ptx::tmem_ld_32x32b_x32(tb + c, U);
                         ptx::tmem_ld_32x32b_x32(tb + NOUT + c, V);
                         ptx::tmem_ld_wait();
-                        if (row_ok && w.n0 + c < a.N) {
+                        // features of this chunk inside the tile and the
+                        // matrix (NOUT = 56 leaves a chunk of 24; columns read
+                        // past it are never stored)
+                        const int nval = min(32, min(NOUT - c, a.N - (w.n0 + c)));
+                        if (row_ok && nval > 0) {
                             uint32_t packed[16];
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
@@ -295,8 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_cons
                             uint4 *dst = reinterpret_cast<uint4 *>(hrow + c);
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
-                                dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1],
-                                                    packed[4 * q + 2], packed[4 * q + 3]);
+                                if (8 * q < nval)
+                                    dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1],
+                                                        packed[4 * q + 2], packed[4 * q + 3]);
                         }
                     }
                 } else {
@@ -380,7 +386,10 @@ int launch_swiglu_tc(const void *x_perm, const int *offsets, const void *const *
                      void *h, cudaStream_t s) {
     if (rows == 0) return MOE_OK;
     TcArgs args;  // copied into the launch's parameter space at enqueue
-    const int NB = wide ? 256 : 128;
+    // few rows per expert: 112-row tiles (56 W1 + 56 W3 rows) make the Mixtral
+    // shape's 8 x 256 units 13.8 waves of 148 SMs (128-row tiles: 12.1, the
+    // last wave 16 SMs streaming alone)
+    const int NB = wide ? 256 : 112;
     int rc = fill_common(args, x_perm, offsets, h, rows, d, ffn, E, bm);
     if (rc != MOE_OK) return rc;
     for (int e = 0; e < E; ++e) {
@@ -394,7 +403,7 @@ int launch_swiglu_tc(const void *x_perm, const int *offsets, const void *const *
     const int NT = (ffn + NB / 2 - 1) / (NB / 2);
     const int units_bound = ((rows + bm - 1) / bm + E) * NT;
     return wide ? run_tc<256, 4, true>(args, units_bound, s)
-                : run_tc<128, 6, true>(args, units_bound, s);
+                : run_tc<112, 6, true>(args, units_bound, s);
 }
 
 int launch_down_tc(const void *h, const int *offsets, const void *const *W2, int rows, int d,
