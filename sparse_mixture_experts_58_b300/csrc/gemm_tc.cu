@@ -26,7 +26,12 @@
 // The MMA is always M = 128 (one token row per tensor-memory lane).  The token
 // tile copied by TMA is `bm` <= 128 rows: rows past it are never written and
 // only affect accumulator lanes the epilogue never reads (row m of D depends
-// only on row m of A).
+// only on row m of A).  For a handful of tokens (bm <= ABM < 128) a stage
+// reserves only ABM token rows, so the ring holds about twice as many weight
+// stages and keeps twice the bytes in flight; the MMA's reads of rows past ABM
+// then land in the next slots of the ring (all token slots come first, so
+// every such read stays inside the CTA's shared memory) and, again, only reach
+// lanes that are never read.
 //
 // Every wait is bounded (see ptx::mbar_wait_bounded); on expiry the roles stop
 // issuing work, drain what is in flight, free tensor memory and return, and
@@ -78,19 +83,23 @@ __device__ __forceinline__ Unit decode_unit(int u, const int *s_off, const int *
     return w;
 }
 
-template <int NB, int STAGES>
+template <int NB, int STAGES, int ABM>
 struct SmemLayout {
-    static constexpr int kABytes = kTileM * 128;  // 128 rows x 64 bf16
+    static constexpr int kABytes = ABM * 128;     // ABM token rows x 64 bf16
     static constexpr int kBBytes = NB * 128;      // NB rows x 64 bf16
     static constexpr int kRing = STAGES * (kABytes + kBBytes);
     static constexpr int kBars = (2 * STAGES + 5) * 8;
     static constexpr int kMisc = 8 + 4 * (3 * kMaxE + 2);
     static constexpr size_t kTotal = 1024 + kRing + kBars + kMisc;  // + alignment slack
+    // the MMA reads 128 rows from the last token slot: past it lie weight slots
+    static_assert(STAGES * kABytes + STAGES * kBBytes >= (STAGES - 1) * kABytes + kTileM * 128,
+                  "MMA token reads must stay inside the ring");
+    static_assert(ABM % 8 == 0 && ABM <= kTileM, "token slot of whole 8-row swizzle atoms");
 };
 
-template <int NB, int STAGES, bool SWIGLU>
+template <int NB, int STAGES, bool SWIGLU, int ABM>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_constant__ TcArgs a) {
-    using L = SmemLayout<NB, STAGES>;
+    using L = SmemLayout<NB, STAGES, ABM>;
     constexpr int NOUT = SWIGLU ? NB / 2 : NB;
     // two NB-column accumulators, allocated as a power of two
     constexpr uint32_t kTmemCols = 2 * NB <= 256 ? 256 : 512;
@@ -340,10 +349,21 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_cons
 
 std::mutex g_attr_mutex;
 
-template <int NB, int STAGES, bool SWIGLU>
+// Measurement override: MOE_TC_NARROW=0 keeps 128-row token slots at any bm.
+bool narrow_token_slots() {
+    static const bool on = [] {
+        const char *v = getenv("MOE_TC_NARROW");
+        return v == nullptr || atoi(v) != 0;
+    }();
+    return on;
+}
+
+template <int NB, int STAGES, bool SWIGLU, int ABM = kTileM>
 int run_tc(TcArgs &args, int units_bound, cudaStream_t s) {
-    using L = SmemLayout<NB, STAGES>;
-    auto kernel = grouped_gemm_tc<NB, STAGES, SWIGLU>;
+    using L = SmemLayout<NB, STAGES, ABM>;
+    static_assert(L::kTotal <= 232448, "dynamic shared memory per CTA");
+    if (args.bm > ABM) return MOE_ERR_ARG;
+    auto kernel = grouped_gemm_tc<NB, STAGES, SWIGLU, ABM>;
     {
         // once per device, so later launches (and stream capture) only enqueue
         static bool attr_set[64];
@@ -402,8 +422,17 @@ int launch_swiglu_tc(const void *x_perm, const int *offsets, const void *const *
     args.kps = args.kblocks;
     const int NT = (ffn + NB / 2 - 1) / (NB / 2);
     const int units_bound = ((rows + bm - 1) / bm + E) * NT;
-    return wide ? run_tc<256, 4, true>(args, units_bound, s)
-                : run_tc<112, 6, true>(args, units_bound, s);
+    if (wide) return run_tc<256, 4, true>(args, units_bound, s);
+    // few tokens per tile: token slots of 16/32/64 rows and more stages, about
+    // 160-180 KB of ring either way (measured at 16 tokens: 6 stages of 128-row
+    // slots 310.7 us, 10 or 13 stages of 16-row slots 295.5 us, 14 stages
+    // 301.5 us)
+    if (narrow_token_slots()) {
+        if (bm <= 16) return run_tc<112, 10, true, 16>(args, units_bound, s);
+        if (bm <= 32) return run_tc<112, 10, true, 32>(args, units_bound, s);
+        if (bm <= 64) return run_tc<112, 8, true, 64>(args, units_bound, s);
+    }
+    return run_tc<112, 6, true>(args, units_bound, s);
 }
 
 int launch_down_tc(const void *h, const int *offsets, const void *const *W2, int rows, int d,
@@ -421,8 +450,15 @@ int launch_down_tc(const void *h, const int *offsets, const void *const *W2, int
     args.kps = kps;
     const int NT = (d + NB - 1) / NB;
     const int units_bound = ((rows + bm - 1) / bm + E) * NT * splits;
-    return wide ? run_tc<256, 4, false>(args, units_bound, s)
-                : run_tc<128, 6, false>(args, units_bound, s);
+    if (wide) return run_tc<256, 4, false>(args, units_bound, s);
+    // (measured at 16 tokens: 6, 8, 10, 12 stages of 16-row slots 153.2, 149.4,
+    // 147.5, 155.7 us; 6 stages of 128-row slots 153.0 us)
+    if (narrow_token_slots()) {
+        if (bm <= 16) return run_tc<128, 10, false, 16>(args, units_bound, s);
+        if (bm <= 32) return run_tc<128, 9, false, 32>(args, units_bound, s);
+        if (bm <= 64) return run_tc<128, 7, false, 64>(args, units_bound, s);
+    }
+    return run_tc<128, 6, false>(args, units_bound, s);
 }
 
 }  // namespace moe
