@@ -344,7 +344,8 @@ def measure(args, rank, world, local):
     if cap:
         overrides.append(f"capacity factor {args.capacity_factor} -> {cap} rows/expert, "
                          f"dropped mass {'renormalised' if policy else 'lost'}")
-    for var in ("MOE_PLAN_WIDE", "MOE_PLAN_PAIR", "MOE_PLAN_SPLITS", "MOE_PDL"):
+    for var in ("MOE_PLAN_WIDE", "MOE_PLAN_PAIR", "MOE_PLAN_SPLITS", "MOE_PLAN_BM", "MOE_PDL",
+                "MOE_TC_NARROW"):
         if os.environ.get(var):
             overrides.append(f"{var}={os.environ[var]}")
     workload = WORKLOAD_NAMES[args.config]

@@ -216,11 +216,27 @@ int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p) {
     if (dt == MOE_BF16) {
         const long long rows_per_expert = (long long)q.rows / E;
         q.wide = rows_per_expert >= 128 ? 1 : 0;
-        q.bm = T >= 128 ? 128 : ((T + 7) / 8) * 8;
-        if (q.bm < 8) q.bm = 8;
+        // Token tile height of the one-CTA GEMMs: about 1.25x the mean rows
+        // per expert, 32, 64 or 128 (and never past the batch): a shorter tile
+        // lets the ring hold more weight stages, an expert past it costs one
+        // more token tile.  Measured (Mixtral shape, per step): T=100 tile 104
+        // 490.0 us, 64 475.4, 32 466.6; T=200 tile 128 502.3, 64 487.3, 32
+        // 766.7; T=256 tile 128 507.7, 64 638.0.
+        {
+            const long long mu = ((long long)q.rows + E - 1) / E;
+            const long long need = (5 * mu + 3) / 4;
+            const int tile = need <= 32 ? 32 : need <= 64 ? 64 : 128;
+            const int whole = ((T + 7) / 8) * 8;
+            q.bm = tile < whole ? tile : whole;
+            if (q.bm < 8) q.bm = 8;
+        }
         // tuning overrides (measurement only): MOE_PLAN_WIDE=0|1, MOE_PLAN_PAIR=0|1,
-        // MOE_PLAN_SPLITS=n
+        // MOE_PLAN_SPLITS=n, MOE_PLAN_BM=rows (multiple of 8, 8..128)
         if (const char *w = getenv("MOE_PLAN_WIDE")) q.wide = atoi(w) != 0;
+        if (const char *b = getenv("MOE_PLAN_BM")) {
+            const int v = atoi(b);
+            if (v >= 8 && v <= 128 && v % 8 == 0) q.bm = v;
+        }
         // many rows per expert: CTA pairs with the tokens as the MMA's N side
         q.pair = q.wide;
         if (const char *pp = getenv("MOE_PLAN_PAIR")) q.pair = atoi(pp) != 0;
