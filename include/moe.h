@@ -49,6 +49,17 @@
  *   - The library allocates no device memory: scratch comes from the caller's
  *     `workspace` (size from moe_workspace_bytes, 256-byte aligned).  Calls on
  *     different streams need different workspaces.
+ *   - Launch graphs (moe_forward, moe_forward_ex, moe_block_forward,
+ *     moe_forward_host_io): the second call with exactly the same arguments
+ *     (every pointer, size, option and the tile plan) captures its launches
+ *     into a CUDA graph on a private stream, and that call and later ones
+ *     with the same arguments launch the graph on `stream`: the same kernels
+ *     with the same parameters, so the same bits.  The library keeps those
+ *     graphs, and the pointers inside them, for up to 64 argument sets per
+ *     process; a graph only runs for a call that passes the same pointers
+ *     again, and reads the buffers' contents as they are then.  A call on a
+ *     stream that is being captured enqueues its kernels directly, into the
+ *     caller's graph.  MOE_GRAPHS=0 in the environment turns graphs off.
  *   - Limits: 1 <= E <= 64, 1 <= k <= min(E, 8), T >= 0 (T = 0 is a no-op).
  *     ("Mixtral > Architecture Overview" weighs 4 or 64 experts against 8;
  *     Mixtral itself uses E = 8, k = 2.)  bf16 needs

@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <string>
 #include <unordered_map>
 
 #include "internal.h"
@@ -474,6 +475,117 @@ int make_bwd_plan(int T, int d, int ffn, int E, int k, int dt, BwdPlan *p) {
     return MOE_OK;
 }
 
+// ---- launch graphs -------------------------------------------------------
+// A call with the same arguments as an earlier one (every pointer, size,
+// option and the plan) replays a CUDA graph of that call's launches: one graph
+// launch instead of six kernel launches with parameter blocks of up to 18 KB,
+// and the kernels start back to back.  The first call of an argument set runs
+// directly (and does the one-time setup: function attributes, the status
+// word); the second captures its launches on a private stream (relaxed mode)
+// and launches the graph on the caller's stream, as do later calls.  A call on
+// a stream that is being captured itself enqueues its kernels directly, so
+// they land in the caller's graph.  At most kGraphSlots argument sets are
+// kept (later ones run directly).  MOE_GRAPHS=0 turns graphs off.
+constexpr size_t kGraphSlots = 64;
+
+struct GraphEntry {
+    cudaGraphExec_t exec = nullptr;
+    bool failed = false;
+};
+
+std::mutex g_graph_mutex;
+std::unordered_map<std::string, GraphEntry> g_graphs;
+cudaStream_t g_capture_stream[64];
+
+bool graphs_enabled() {
+    const char *v = getenv("MOE_GRAPHS");
+    return v == nullptr || atoi(v) != 0;
+}
+
+// Bytes of every argument that shapes the launches.
+class LaunchKey {
+  public:
+    explicit LaunchKey(int entry) { add(entry); }
+    template <typename V>
+    LaunchKey &add(const V &v) {
+        s_.append(reinterpret_cast<const char *>(&v), sizeof v);
+        return *this;
+    }
+    LaunchKey &ptrs(const void *const *p, int n) {
+        for (int i = 0; i < n; ++i) add(p[i]);
+        return *this;
+    }
+    LaunchKey &plan(const Plan &P) {
+        return add(P.T).add(P.d).add(P.ffn).add(P.E).add(P.k).add(P.dt).add(P.rows).add(P.wide)
+            .add(P.pair).add(P.bm).add(P.splits).add(P.kps).add(P.bytes);
+    }
+    LaunchKey &opts(const Options &O) { return add(O.gating).add(O.capacity).add(O.renorm); }
+    const std::string &str() const { return s_; }
+
+  private:
+    std::string s_;
+};
+
+template <typename F>
+int run_graphed(const LaunchKey &key, cudaStream_t user, F &&enqueue) {
+    if (!graphs_enabled()) return enqueue(user);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(user, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return enqueue(user);
+    }
+    if (cs != cudaStreamCaptureStatusNone) return enqueue(user);
+    const int dev = current_device();
+    if (dev < 0 || dev >= 64) return enqueue(user);
+    std::string k = key.str();
+    k.append(reinterpret_cast<const char *>(&dev), sizeof dev);
+    std::lock_guard<std::mutex> g(g_graph_mutex);
+    auto it = g_graphs.find(k);
+    if (it == g_graphs.end()) {
+        if (g_graphs.size() < kGraphSlots) g_graphs.emplace(k, GraphEntry());
+        return enqueue(user);
+    }
+    GraphEntry &e = it->second;
+    if (e.exec != nullptr)
+        return cudaGraphLaunch(e.exec, user) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    if (e.failed) return enqueue(user);
+    if (g_capture_stream[dev] == nullptr &&
+        cudaStreamCreateWithFlags(&g_capture_stream[dev], cudaStreamNonBlocking) != cudaSuccess) {
+        g_capture_stream[dev] = nullptr;
+        cudaGetLastError();
+        e.failed = true;
+        return enqueue(user);
+    }
+    cudaStream_t cap = g_capture_stream[dev];
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    int rc = MOE_ERR_CUDA;
+    if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeRelaxed) == cudaSuccess) {
+        rc = enqueue(cap);
+        if (cudaStreamEndCapture(cap, &graph) != cudaSuccess) graph = nullptr;
+    }
+    if (rc == MOE_OK && graph != nullptr && cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess)
+        exec = nullptr;
+    if (graph != nullptr) cudaGraphDestroy(graph);
+    if (exec == nullptr) {
+        cudaGetLastError();
+        e.failed = true;
+        return enqueue(user);
+    }
+    e.exec = exec;
+    return cudaGraphLaunch(exec, user) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+LaunchKey forward_key(int entry, const Plan &P, const Options &O, const void *x,
+                      const void *W_g, const float *bias, const void *const *W1,
+                      const void *const *W3, const void *const *W2, const void *out,
+                      const void *ws) {
+    LaunchKey key(entry);
+    key.plan(P).opts(O).add(x).add(W_g).add(bias).ptrs(W1, P.E).ptrs(W3, P.E).ptrs(W2, P.E)
+        .add(out).add(ws);
+    return key;
+}
+
 int run_backward(const BwdPlan &P, const void *x, const void *W_g, const float *bias,
                  const void *const *W1, const void *const *W3, const void *const *W2,
                  const void *d_out, void *d_x, float *d_Wg, float *const *d_W1,
@@ -643,8 +755,12 @@ int moe_forward(const void *x, const void *W_g, const float *router_bias, const 
     int rc = check_forward_args(x, W_g, W1, W3, W2, T, d, ffn, E, k, dtype, out, workspace,
                                 workspace_bytes, &P);
     if (rc != MOE_OK || T == 0) return rc;
-    return run_forward(P, Options(), x, W_g, router_bias, W1, W3, W2, out, workspace,
-                       static_cast<cudaStream_t>(stream));
+    const Options O;
+    return run_graphed(forward_key(1, P, O, x, W_g, router_bias, W1, W3, W2, out, workspace),
+                       static_cast<cudaStream_t>(stream), [&](cudaStream_t s) {
+                           return run_forward(P, O, x, W_g, router_bias, W1, W3, W2, out,
+                                              workspace, s);
+                       });
 }
 
 int moe_forward_ex(const void *x, const void *W_g, const float *router_bias,
@@ -658,8 +774,11 @@ int moe_forward_ex(const void *x, const void *W_g, const float *router_bias,
     rc = check_forward_args(x, W_g, W1, W3, W2, T, d, ffn, E, k, dtype, out, workspace,
                             workspace_bytes, &P);
     if (rc != MOE_OK || T == 0) return rc;
-    return run_forward(P, O, x, W_g, router_bias, W1, W3, W2, out, workspace,
-                       static_cast<cudaStream_t>(stream));
+    return run_graphed(forward_key(2, P, O, x, W_g, router_bias, W1, W3, W2, out, workspace),
+                       static_cast<cudaStream_t>(stream), [&](cudaStream_t s) {
+                           return run_forward(P, O, x, W_g, router_bias, W1, W3, W2, out,
+                                              workspace, s);
+                       });
 }
 
 int moe_block_forward(void *x, const void *W_g, const float *router_bias, const void *const *W1,
@@ -674,8 +793,11 @@ int moe_block_forward(void *x, const void *W_g, const float *router_bias, const 
     rc = check_forward_args(x, W_g, W1, W3, W2, T, d, ffn, E, k, dtype, x, workspace,
                             workspace_bytes, &P);
     if (rc != MOE_OK || T == 0) return rc;
-    return run_forward(P, O, x, W_g, router_bias, W1, W3, W2, x, workspace,
-                       static_cast<cudaStream_t>(stream), &eps);
+    LaunchKey key = forward_key(3, P, O, x, W_g, router_bias, W1, W3, W2, x, workspace);
+    key.add(eps);
+    return run_graphed(key, static_cast<cudaStream_t>(stream), [&](cudaStream_t s) {
+        return run_forward(P, O, x, W_g, router_bias, W1, W3, W2, x, workspace, s, &eps);
+    });
 }
 
 int moe_capacity(double capacity_factor, int T, int k, int E, int *capacity) {
@@ -700,16 +822,19 @@ int moe_forward_host_io(const void *x_host, void *out_host, void *x_dev, void *o
                                 workspace, workspace_bytes, &P);
     if (rc != MOE_OK || T == 0) return rc;
     if (x_host == nullptr || out_host == nullptr) return MOE_ERR_ARG;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t bytes = (size_t)T * d * elem_size(dtype);
-    if (cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    if ((rc = run_forward(P, Options(), x_dev, W_g, router_bias, W1, W3, W2, out_dev, workspace,
-                          s)) != MOE_OK)
-        return rc;
-    if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    return MOE_OK;
+    const Options O;
+    LaunchKey key = forward_key(4, P, O, x_dev, W_g, router_bias, W1, W3, W2, out_dev, workspace);
+    key.add(x_host).add(out_host);
+    return run_graphed(key, static_cast<cudaStream_t>(stream), [&](cudaStream_t s) {
+        if (cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return (int)MOE_ERR_CUDA;
+        int r = run_forward(P, O, x_dev, W_g, router_bias, W1, W3, W2, out_dev, workspace, s);
+        if (r != MOE_OK) return r;
+        if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+            return (int)MOE_ERR_CUDA;
+        return (int)MOE_OK;
+    });
 }
 
 int moe_router(const void *x, const void *W_g, const float *router_bias, int T, int d, int E,
