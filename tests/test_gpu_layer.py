@@ -191,6 +191,14 @@ def test_decode_config_all_tokens(moe, decode_case):
     check_layer(moe, x, layer, 2, label="decode T=16")
 
 
+@pytest.mark.parametrize("T", [1, 3, 5])
+def test_decode_weights_few_tokens(moe, decode_case, T):
+    """The decode layer's weights with 1, 3 and 5 tokens: two to ten expert
+    rows, most experts idle, token tiles of 8 rows."""
+    x, layer = decode_case
+    check_layer(moe, x[:T].contiguous(), layer, 2, label=f"decode weights T={T}")
+
+
 def test_prefill_config_sampled(moe):
     x, layer = inputs.make_named("prefill", device="cuda")
     rows = helpers.sample_rows(4096, 48, seed=1)
