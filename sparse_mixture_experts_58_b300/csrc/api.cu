@@ -1,6 +1,7 @@
 // C ABI of libmoe.so: argument checks, the per-call plan (tiles, splits,
 // workspace layout) and the sequence of kernel launches.  See include/moe.h.
 #include <cudaTypedefs.h>
+#include <math.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -245,38 +246,56 @@ int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p) {
         const long long busy = q.rows < E ? q.rows : E;
         long long s = 1;
         const long long smax = kblocks / 8 > 0 ? kblocks / 8 : 1;
-        // Split the down projection's contraction so every SM (pair) has work:
-        // among the splits giving lo..hi units per worker, the one whose last
-        // wave is fullest (fewer splits on a tie: less partial-sum traffic).
-        auto balanced = [&](long long base_units, long long workers, long long lo, long long hi) {
-            if (base_units <= 0) return 1LL;
-            long long best = 1;
-            double best_eff = -1.0;
-            const long long s_lo = (lo * workers + base_units - 1) / base_units;
-            const long long s_hi = (hi * workers + base_units - 1) / base_units;
-            for (long long c = s_lo < 1 ? 1 : s_lo; c <= s_hi && c <= smax; ++c) {
-                const long long units = base_units * c;
-                const long long waves = (units + workers - 1) / workers;
-                const double eff = (double)units / (double)(waves * workers);
-                if (eff > best_eff + 1e-9) {
-                    best_eff = eff;
-                    best = c;
-                }
-            }
-            return best;
-        };
         if (q.pair) {
             // down-projection units: 256 features x one token tile of <= 256
-            // rows; about 4 units per pair (measured: a fuller last wave does
-            // not pay for more fp32 partial sums here, T=1024: 3 splits 692 us,
-            // 4 splits 727 us)
+            // rows.  No split up to 1024 rows, two below 4 units per pair, none
+            // above: the fp32 partial sums cost more than a fuller last wave
+            // gains (Mixtral shape, per step, splits 1/2/3/4: T=512 524.3/
+            // 538.7/549.9/539.8 us, T=1024 670.4/657.7/683.9/682.9 us, T=2048
+            // 1100.9/1098.1/1109.3/1120.2 us)
             const long long ttiles = busy > (q.rows + 255) / 256 ? busy : (q.rows + 255) / 256;
             const long long base_units = ttiles * ((d + 255) / 256);
-            s = (4LL * (kPlanSms / 2) + base_units - 1) / base_units;
-        } else if (!q.wide) {
-            // one 128-feature x 128-row tile per busy expert (decode: 4 splits,
-            // 1024 units = 6.9 waves, 482 us per step against 484 us with 5)
-            s = balanced(busy * ((d + 127) / 128), kPlanSms, 4, 12);
+            s = q.rows <= 1024 ? 1 : base_units >= 4LL * (kPlanSms / 2) ? 1 : 2;
+        } else if (!q.wide && busy > 0) {
+            // Units: 128 output features x one token tile x one split, for each
+            // busy expert.  The split with the least estimated time, in
+            // microseconds at about 6.4 TB/s: the busy experts' W2 bytes over
+            // the waves of units (a last wave with fewer than 85% of the SMs
+            // busy cannot keep HBM saturated, so it costs as if it had 85%),
+            // about 0.8 us per unit an SM runs in turn, and the fp32 partial
+            // sums (written here, read by the combine: three passes).
+            // Busy experts: the expected count under even routing, e = E (1 -
+            // (1 - k/E)^T) (exactly k for one token); the cost is weighed
+            // between floor(e) and floor(e) + 1 busy experts.  Measured
+            // (Mixtral shape, per step): T=1 splits 2 144.7 us, 23 147.6;
+            // T=16 splits 1/3/4/5/8 458.3/465.2/452.6/455.7/455.5; T=256
+            // splits 1/4 498.5/506.6; T=400 1/4 506.7/522.4.
+            const double pk = 1.0 - (double)(k < E ? k : E) / (double)E;
+            double ebusy = (double)E * (1.0 - pow(pk, (double)T));
+            if (ebusy > (double)busy) ebusy = (double)busy;
+            if (ebusy < 1.0) ebusy = 1.0;
+            const long long nb_lo = (long long)ebusy;
+            const double w_hi = ebusy - (double)nb_lo;
+            auto est_us = [&](long long nb, long long c) {
+                const long long per_expert = (q.rows + nb - 1) / nb;
+                const long long tiles = (per_expert + q.bm - 1) / q.bm;
+                const long long units = nb * (tiles > 0 ? tiles : 1) * ((d + 127) / 128) * c;
+                const long long waves = (units + kPlanSms - 1) / kPlanSms;
+                const double f = (double)(units - (waves - 1) * kPlanSms) / kPlanSms;
+                const double t_w = (double)nb * d * ffn * 2 / 6.4e6;
+                return t_w * ((double)(waves - 1) + (f > 0.85 ? f : 0.85)) * kPlanSms /
+                           (double)units +
+                       0.8 * (double)waves + 3.0 * (double)c * q.rows * d * 4 / 6.4e6;
+            };
+            double best = 1e300;
+            for (long long c = 1; c <= smax; ++c) {
+                double cost = (1.0 - w_hi) * est_us(nb_lo, c);
+                if (w_hi > 0.0) cost += w_hi * est_us(nb_lo + 1, c);
+                if (cost < best - 1e-9) {
+                    best = cost;
+                    s = c;
+                }
+            }
         }
         if (s > smax) s = smax;
         if (s < 1) s = 1;
