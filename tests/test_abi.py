@@ -59,6 +59,27 @@ def test_workspace_sizes(moe):
     assert moe.workspace_bytes(0, 4096, 14336, 8, 2, moe.BF16) >= 0
     assert moe.down_splits(4096, 4096, 14336, 8, 2, moe.BF16) == 1
     assert moe.down_splits(16, 4096, 14336, 8, 2, moe.BF16) > 1
+
+
+def test_down_split_plan(moe):
+    """The split of the down projection's contraction (host-side plan, Mixtral
+    shape): measured best choices are kept -- two splits for one token (two
+    busy experts, 128 units on 148 SMs), four at decode (1024 units, the last
+    wave 136 of 148 SMs), none once the fp32 partial sums outweigh the wave
+    fill (one-CTA tiles from T=200, CTA pairs up to 1024 rows), two for pairs
+    at T=1024..2048; always a whole number of 64-deep blocks per split."""
+    S = lambda T, E=8, k=2: moe.down_splits(T, 4096, 14336, E, k, moe.BF16)
+    assert S(1) == 2
+    assert S(16) == 4
+    assert all(S(T) == 1 for T in (200, 256, 400, 511, 512, 3072, 4096, 16384))
+    assert S(1024) == 2 and S(2048) == 2
+    for T in (1, 2, 3, 4, 8, 16, 32, 64, 128, 199, 300, 1024, 8192):
+        s = S(T)
+        kps = -(-224 // s)
+        assert 1 <= s <= 28 and -(-224 // kps) == s, (T, s)
+    for E, k in ((4, 1), (4, 2), (16, 3), (64, 8)):
+        for T in (1, 7, 16, 300):
+            assert 1 <= S(T, E, k) <= 28
     assert moe.forward_launches(16, 4096, 14336, 8, 2, moe.BF16) == 6
     assert moe.forward_launches(0, 4096, 14336, 8, 2, moe.BF16) == 0
 
