@@ -59,6 +59,9 @@ constexpr int kTokMaps = kMaxTok / 16;
 constexpr int kStages = 5;
 constexpr int kMaxE = MOE_MAX_EXPERTS;
 constexpr int kEpiWarps = 8;  // two per tensor-memory lane quarter
+// a warp's 32-column chunks of an accumulator are kChunkStep apart
+constexpr int kChunkStep = 32 * (kEpiWarps / 4);
+static_assert(kEpiWarps % 4 == 0, "whole lane quarters per epilogue warp set");
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kBox = 64 * 128;              // one 64 x 64 bf16 box
 constexpr int kABytes = 2 * kBox;           // 128 weight-side rows x 64, or 64 x 128 MN-major
@@ -385,8 +388,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        // warps w and w + 4 read the same lane quarter (w % 4) and take
-        // alternate 32-column chunks
+        // warps w, w + 4, ... read the same lane quarter (w % 4) and take
+        // every (kEpiWarps / 4)-th 32-column chunk
         const int quad = warp & 3;
         const int c_first = 32 * ((warp - 2) >> 2);
         const uint32_t acc_empty0 = ptx::map_to_rank(ptx::smem_addr(&acc_empty[0]), 0);
@@ -409,7 +412,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 __nv_bfloat16 *dst = (quad >= 2 ? a.V : a.U) + (size_t)f * a.rows;
                 const bool f_ok = f < a.ffn;
 #pragma unroll 1
-                for (int j0 = c_first; j0 < w.ntok; j0 += 64) {
+                for (int j0 = c_first; j0 < w.ntok; j0 += kChunkStep) {
                     uint32_t R[32];
                     ptx::tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(j0), R);
                     ptx::tmem_ld_wait();
@@ -441,7 +444,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int cb = (w.n0 + static_cast<int>(rank) * kHalfM + 32 * quad) / 32;
                 const size_t ld = a.ffn;
 #pragma unroll 1
-                for (int j0 = c_first; j0 < w.ntok; j0 += 64) {
+                for (int j0 = c_first; j0 < w.ntok; j0 += kChunkStep) {
                     uint32_t R[32];
                     ptx::tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(j0), R);
                     // lane i fetches token j0 + i's gate; the warp shares them
@@ -522,7 +525,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 float *col = a.dx_rows + f;
                 const bool f_ok = f < a.d;
 #pragma unroll 1
-                for (int j0 = c_first; j0 < w.ntok; j0 += 64) {
+                for (int j0 = c_first; j0 < w.ntok; j0 += kChunkStep) {
                     uint32_t R[32];
                     ptx::tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(j0), R);
                     ptx::tmem_ld_wait();
@@ -543,7 +546,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 float *out = a.wgrad[w.g][w.e];
                 const int rsub = lane >> 3, c4 = (lane & 7) * 4;
 #pragma unroll 1
-                for (int j0 = c_first; j0 < kMaxTok; j0 += 64) {
+                for (int j0 = c_first; j0 < kMaxTok; j0 += kChunkStep) {
                     uint32_t R[32];
                     ptx::tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(j0), R);
                     ptx::tmem_ld_wait();
