@@ -318,9 +318,10 @@ int moe_forward_launches(int T, int d, int ffn, int E, int k, int dtype, int *la
 /*
  * The pages have no counterpart to this entry point: it is a convenience for
  * callers that cannot allocate device memory where they run the layer (an
- * inference-engine plugin handed fixed buffers, a serving process whose
- * memory budget was reserved at start-up, code running while a stream is
- * captured into a CUDA graph, where cudaMalloc is refused).
+ * inference-engine plugin handed fixed buffers that must not allocate in its
+ * enqueue step, a serving process whose memory budget was reserved at
+ * start-up).  Its kernels are enqueued directly on `stream` (the launch
+ * graphs described above are not used by this entry point).
  *
  * Same result as moe_forward, but the scratch is a fixed array of
  * MOE_STATIC_SCRATCH_BYTES inside the library on each device, held until the

@@ -668,6 +668,21 @@ int run_backward(const BwdPlan &P, const void *x, const void *W_g, const float *
 }
 
 }  // namespace
+
+// The layer with its kernels enqueued directly on `s`: validation, plan and
+// the launch sequence of moe_forward, without the launch-graph cache (so no
+// stream or graph is created on the way).
+int forward_direct(const void *x, const void *W_g, const float *router_bias,
+                   const void *const *W1, const void *const *W3, const void *const *W2, int T,
+                   int d, int ffn, int E, int k, int dtype, void *out, void *workspace,
+                   size_t workspace_bytes, cudaStream_t s) {
+    Plan P;
+    int rc = check_forward_args(x, W_g, W1, W3, W2, T, d, ffn, E, k, dtype, out, workspace,
+                                workspace_bytes, &P);
+    if (rc != MOE_OK || T == 0) return rc;
+    return run_forward(P, Options(), x, W_g, router_bias, W1, W3, W2, out, workspace, s);
+}
+
 }  // namespace moe
 
 using namespace moe;

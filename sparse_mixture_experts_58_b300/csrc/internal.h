@@ -32,6 +32,13 @@ struct Plan {
 
 int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p);
 
+// moe_forward's validation and launch sequence, enqueued directly on the
+// stream (no launch graph); the library's fixed-scratch entry point uses it.
+int forward_direct(const void *x, const void *W_g, const float *router_bias,
+                   const void *const *W1, const void *const *W3, const void *const *W2, int T,
+                   int d, int ffn, int E, int k, int dtype, void *out, void *workspace,
+                   size_t workspace_bytes, cudaStream_t s);
+
 // Launch with programmatic stream serialisation allowed, so the kernel may be
 // scheduled while the previous kernel on the stream drains (the kernel itself
 // calls pdl_wait() before reading earlier results).  A previous kernel that

@@ -3,11 +3,13 @@
 //
 // Who needs it: callers that cannot allocate device memory at the point where
 // they run the layer -- an inference-engine plugin whose enqueue step is
-// handed fixed buffers and must not allocate, a serving process that reserved
-// its whole memory budget at start-up, or code that runs while a stream is
-// being captured into a CUDA graph, where cudaMalloc is refused.  They pass
-// the tokens, the weights and the output buffer; the library supplies the
-// scratch.
+// handed fixed buffers and must not allocate, or a serving process that
+// reserved its whole memory budget at start-up, so that a later cudaMalloc
+// would fail or break its accounting.  They pass the tokens, the weights and
+// the output buffer; the library supplies the scratch.  The kernels are
+// enqueued directly on the caller's stream (the launch-graph cache of
+// moe_forward is not used here, since building a graph takes driver
+// resources).
 //
 // The array is MOE_STATIC_SCRATCH_BYTES per device and stays allocated, on
 // every device that loads the library, until the process exits.  All calls on
@@ -56,6 +58,7 @@ extern "C" int moe_forward_static_scratch(const void *x, const void *W_g,
     if (need > MOE_STATIC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
     void *scratch = nullptr;
     if ((rc = scratch_address(&scratch)) != MOE_OK) return rc;
-    return moe_forward(x, W_g, router_bias, W1, W3, W2, T, d, ffn, E, k, dtype, out, scratch,
-                       MOE_STATIC_SCRATCH_BYTES, stream);
+    return moe::forward_direct(x, W_g, router_bias, W1, W3, W2, T, d, ffn, E, k, dtype, out,
+                               scratch, MOE_STATIC_SCRATCH_BYTES,
+                               static_cast<cudaStream_t>(stream));
 }

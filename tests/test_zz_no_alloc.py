@@ -1,6 +1,6 @@
 """moe_forward_static_scratch: the layer for callers that cannot allocate
 device memory where they run it (an engine plugin handed fixed buffers, a
-process whose memory budget is spent, code under stream capture).  Its
+process whose memory budget was reserved up front).  Its
 scratch is a fixed array inside the library, so the caller passes only the
 tokens, the weights and the output.
 
