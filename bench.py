@@ -258,9 +258,12 @@ def run_reference(args, rank, world):
     from sparse_mixture_experts_58_b300 import inputs
 
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    x, layer = inputs.make_named(args.config, device=dev)
+    cfg, overrides = workload_cfg(args, args.config)
+    x, layer = inputs.make_workload(cfg["T"], cfg["d"], cfg["ffn"], cfg["E"], cfg["k"],
+                                    cfg["dtype"], cfg["seed"], dev, cfg.get("bias"),
+                                    cfg.get("dup_frac", 0.0))
     T = x.shape[0]
-    k = layer.meta["k"]
+    k = cfg["k"]
     host = inputs.layer_to_host(layer)
     xh = inputs.to_host(x)
     o = oracle.load()
@@ -284,7 +287,7 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD_NAMES[args.config], "T": T},
+        "config": config_record(args.config, cfg, overrides, world),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{n} seeded tokens of the {T}-token batch per step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -318,40 +321,68 @@ def cpu_baseline(x, layer, k, budget_s=12.0):
 
 # ---------------------------------------------------------------- our arm
 
-def measure(args, rank, world, local):
+def workload_cfg(args, name):
+    """The named workload's shape with the command line's overrides (T, E, k)
+    applied; returns (cfg, overrides)."""
+    from sparse_mixture_experts_58_b300 import inputs
+    cfg = dict(inputs.WORKLOADS[name])
+    overrides = []
+    for key in ("T", "E", "k"):
+        v = getattr(args, key, 0)
+        if v:
+            cfg[key] = v
+            overrides.append(f"{key}={v}")
+    if cfg.get("bias") is not None and len(cfg["bias"]) != cfg["E"]:
+        cfg["bias"] = (list(cfg["bias"]) + [0.0] * cfg["E"])[:cfg["E"]]
+    return cfg, overrides
+
+
+def config_record(name, cfg, overrides, world):
+    """The line's `config`: the workload and its shape only (the same for
+    both arms; what a run observes, such as the routing, goes elsewhere)."""
+    workload = WORKLOAD_NAMES[name]
+    if overrides:
+        workload = f"{workload} ({'; '.join(overrides)})"
+    T, d, ffn, E, k = cfg["T"], cfg["d"], cfg["ffn"], cfg["E"], cfg["k"]
+    return {"workload": workload, "T": T, "d": d, "ffn": ffn, "E": E, "k": k,
+            "tokens_per_gpu": T, "parallelism": f"replicas x{world} (no data-path collective)",
+            "l2": "no flush: each step streams the touched experts' weights (up to "
+                  f"{E * 3 * d * ffn * 2 / 1e9:.2f} GB) > 126 MB L2"}
+
+
+def route_options(args, T, k, E):
+    """Routing options from the command line: (moe.forward keywords,
+    descriptions for the workload name)."""
+    from sparse_mixture_experts_58_b300 import moe
+    cap = moe.capacity(args.capacity_factor, T, k, E) if args.capacity_factor > 0 else 0
+    policy = 1 if args.drop_policy == "renorm" else 0
+    route_kw = dict(gating=args.gating, capacity=cap, drop_policy=policy if cap else 0)
+    notes = []
+    if args.gating:
+        notes.append("gating: softmax over all experts, then top-k")
+    if cap:
+        notes.append(f"capacity factor {args.capacity_factor} -> {cap} rows/expert, "
+                     f"dropped mass {'renormalised' if policy else 'lost'}")
+    for var in ("MOE_PLAN_WIDE", "MOE_PLAN_PAIR", "MOE_PLAN_SPLITS", "MOE_PLAN_BM", "MOE_PDL",
+                "MOE_TC_NARROW", "MOE_FUSE_COMBINE", "MOE_GRAPHS"):
+        if os.environ.get(var):
+            notes.append(f"{var}={os.environ[var]}")
+    return route_kw, notes
+
+
+def bench_layer(args, name, cfg, route_kw, dev, rank, world, local, steps, warmup,
+                with_e2e=False, traffic_key=None):
+    """One workload: the forward as a CUDA-graph replay of one moe_forward
+    call per step (CUDA events on the launching stream, barriers and the
+    slowest rank's time), the same call made directly, a per-stage
+    breakdown through the stage entry points and, with `with_e2e`, the
+    end-to-end figure through the host-buffer entry point.  Returns a dict
+    (rank 0's view of the job)."""
     import torch
 
     from sparse_mixture_experts_58_b300 import inputs, moe
 
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    dist_init(world, "nccl")
-    cfg = dict(inputs.WORKLOADS[args.config])
-    overrides = []
-    for key in ("T", "E", "k"):
-        v = getattr(args, key)
-        if v:
-            cfg[key] = v
-            overrides.append(f"{key}={v}")
     T, d, ffn, E, k = cfg["T"], cfg["d"], cfg["ffn"], cfg["E"], cfg["k"]
-    if cfg.get("bias") is not None and len(cfg["bias"]) != E:
-        cfg["bias"] = (list(cfg["bias"]) + [0.0] * E)[:E]
-    cap = moe.capacity(args.capacity_factor, T, k, E) if args.capacity_factor > 0 else 0
-    policy = 1 if args.drop_policy == "renorm" else 0
-    route_kw = dict(gating=args.gating, capacity=cap, drop_policy=policy if cap else 0)
-    if args.gating:
-        overrides.append("gating: softmax over all experts, then top-k")
-    if cap:
-        overrides.append(f"capacity factor {args.capacity_factor} -> {cap} rows/expert, "
-                         f"dropped mass {'renormalised' if policy else 'lost'}")
-    for var in ("MOE_PLAN_WIDE", "MOE_PLAN_PAIR", "MOE_PLAN_SPLITS", "MOE_PLAN_BM", "MOE_PDL",
-                "MOE_TC_NARROW"):
-        if os.environ.get(var):
-            overrides.append(f"{var}={os.environ[var]}")
-    workload = WORKLOAD_NAMES[args.config]
-    if overrides:
-        workload = f"{workload} ({'; '.join(overrides)})"
-
     # weights shared by every rank; tokens per rank
     gen = inputs.generator(cfg["seed"], dev)
     x0, _ = inputs.draw_tokens(gen, T, d, "bf16", dev, cfg.get("dup_frac", 0.0))
@@ -363,6 +394,7 @@ def measure(args, rank, world, local):
     out = torch.empty_like(x)
     ws = moe.Workspace(dev)
     bias = layer.bias
+    cap = route_kw["capacity"]
 
     def step():
         moe.forward(x, layer.Wg, layer.W1, layer.W3, layer.W2, k, bias=bias, out=out,
@@ -370,13 +402,13 @@ def measure(args, rank, world, local):
 
     # routing of this batch: kept rows per expert (for the algorithmic counts)
     logits0, _, _ = moe.router(x, layer.Wg, k, bias)
-    _, _, kept_counts, _, _, _ = moe.route_from_logits(logits0, k, gating=args.gating,
+    _, _, kept_counts, _, _, _ = moe.route_from_logits(logits0, k, gating=route_kw["gating"],
                                                        capacity=cap)
     counts = kept_counts.cpu()
     n_touched = int((counts > 0).sum())
     rows_kept = int(counts.sum())
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
@@ -389,33 +421,33 @@ def measure(args, rank, world, local):
         with torch.cuda.graph(graph):
             step()
         torch.cuda.synchronize()
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             graph.replay()
         torch.cuda.synchronize()
     run = graph.replay if graph is not None else step
 
-    def timed(fn, n):
+    def timed(fn, n, on=stream):
         barrier(world)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        e0.record(on)
         for _ in range(n):
             fn()
-        e1.record(stream)
+        e1.record(on)
         torch.cuda.synchronize()
         barrier(world)
         return reduce_max(e0.elapsed_time(e1) / 1e3, world, dev)
 
     clocks = ClockSampler(local)
     clocks.start()
-    elapsed_max = timed(run, args.steps)
+    elapsed_max = timed(run, steps)
     clocks.stop()
     status = moe.device_status(clear=True)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
     # the same forward called directly (host launch overhead included)
-    direct_elapsed = timed(step, args.steps)
+    direct_elapsed = timed(step, steps)
 
     # -- per-stage breakdown through the stage entry points (same kernels),
     #    events on the launching stream between stages; a sleep kernel first
@@ -423,14 +455,14 @@ def measure(args, rank, world, local):
     stage_names = ["router", "route", "permute", "gate_up_swiglu", "down", "combine"]
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(stage_names) + 1)]
     acc = [0.0] * len(stage_names)
-    n_rep = max(3, min(args.steps, 50))
+    n_rep = max(3, min(steps, 50))
     for rep in range(n_rep + 2):
         torch.cuda._sleep(2_000_000)
         evs[0].record(stream)
         logits, _, _ = moe.router(x, layer.Wg, k, bias)
         evs[1].record(stream)
-        _, gates2, _, offsets, perm, inv = moe.route_from_logits(logits, k, gating=args.gating,
-                                                                 capacity=cap)
+        _, gates2, _, offsets, perm, inv = moe.route_from_logits(
+            logits, k, gating=route_kw["gating"], capacity=cap)
         evs[2].record(stream)
         xp = moe.permute(x, perm, k, rows=rows_kept)
         evs[3].record(stream)
@@ -447,77 +479,41 @@ def measure(args, rank, world, local):
     stage_s = [a / n_rep for a in acc]
     del h, y, xp
 
-    # -- end to end with host buffers, as a serving loop runs it: every step
-    #    copies its tokens from pinned host memory, runs the layer through the
-    #    public entry point (moe_forward) and copies the output back to pinned
-    #    host memory.  The layer runs on one stream, step after step; the
-    #    copies run on their own streams with two buffer sets, so step i's
-    #    input copy and step i-1's output copy overlap step i's neighbours'
-    #    kernels (events keep each buffer set's copy-in, layer and copy-out in
-    #    order)
-    n_sets = 2
-    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    e2e_sets = []
-    for _ in range(n_sets):
-        xh = x.cpu().pin_memory()
-        e2e_sets.append(dict(x_host=xh, out_host=torch.empty_like(xh).pin_memory(),
-                             x_dev=torch.empty_like(x), out_dev=torch.empty_like(x),
-                             ev_in=torch.cuda.Event(), ev_layer=torch.cuda.Event(),
-                             ev_out=torch.cuda.Event(), used=False))
-    e2e_i = [0]
+    res = {}
+    if with_e2e and not (route_kw["gating"] or cap):
+        # -- end to end through the C ABI's host-buffer call: every step is one
+        #    moe_forward_host_io call with the tokens in pinned host memory and
+        #    the output written back to pinned host memory; the library enqueues
+        #    the copy in, the layer and the copy out on the stream, so the
+        #    copies sit inside each step (nothing overlaps them)
+        x_host = x.cpu().pin_memory()
+        out_host = torch.empty_like(x_host).pin_memory()
+        x_dev, out_dev = torch.empty_like(x), torch.empty_like(x)
 
-    def e2e_step():
-        b = e2e_sets[e2e_i[0] % n_sets]
-        e2e_i[0] += 1
-        if b["used"]:  # the last layer call that read this set's x_dev is done
-            h2d_stream.wait_event(b["ev_layer"])
-        with torch.cuda.stream(h2d_stream):
-            b["x_dev"].copy_(b["x_host"], non_blocking=True)
-            b["ev_in"].record(h2d_stream)
-        stream.wait_event(b["ev_in"])
-        if b["used"]:  # this set's last output copy has left out_dev
-            stream.wait_event(b["ev_out"])
-        moe.forward(b["x_dev"], layer.Wg, layer.W1, layer.W3, layer.W2, k, bias=bias,
-                    out=b["out_dev"], workspace=ws, stream=stream)
-        b["ev_layer"].record(stream)
-        d2h_stream.wait_event(b["ev_layer"])
-        with torch.cuda.stream(d2h_stream):
-            b["out_host"].copy_(b["out_dev"], non_blocking=True)
-            b["ev_out"].record(d2h_stream)
-        b["used"] = True
+        def e2e_step():
+            moe.forward_host_io(x_host, layer.Wg, layer.W1, layer.W3, layer.W2, k, bias=bias,
+                                out_host=out_host, x_dev=x_dev, out_dev=out_dev, workspace=ws,
+                                stream=stream)
 
-    def e2e_timed(n):
-        barrier(world)
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        h2d_stream.wait_event(e0)
-        d2h_stream.wait_event(e0)
-        for _ in range(n):
+        for _ in range(warmup):
             e2e_step()
-        stream.wait_stream(h2d_stream)
-        stream.wait_stream(d2h_stream)
-        e1.record(stream)
         torch.cuda.synchronize()
-        barrier(world)
-        return reduce_max(e0.elapsed_time(e1) / 1e3, world, dev)
-
-    for _ in range(2 * n_sets):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_elapsed = e2e_timed(args.steps)
-    e2e_match = all(torch.equal(b["out_host"], out.cpu()) for b in e2e_sets)
-
-    if rank != 0:
-        return 0
+        e2e_elapsed = timed(e2e_step, steps)
+        res["e2e"] = {"value": T * world * steps / e2e_elapsed, "unit": "tokens/s",
+                      "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                      "d2h_bytes_per_step": out_host.numel() * out_host.element_size(),
+                      "how": "per step one moe_forward_host_io call (the C ABI's host-buffer "
+                             "entry point): pinned host tokens -> device, the layer, output -> "
+                             "pinned host memory, all on one stream",
+                      "output_matches_device_path": bool(torch.equal(out_host, out.cpu()))}
 
     peaks, peak_src = load_peaks()
     flops, bytes_ = algorithmic(T, d, ffn, E, k, n_touched, rows=rows_kept)
-    t_step = elapsed_max / args.steps
-    t_roof = max(bytes_ / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
-    layer_bound = "hbm" if bytes_ / peaks["hbm_gbs"] > flops / (peaks["bf16_tflops"] * 1e3) else "tensor"
-
+    t_step = elapsed_max / steps
+    t_hbm = bytes_ / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    t_roof = max(t_hbm, t_tc)
+    layer_bound = "hbm" if t_hbm > t_tc else "tensor"
     g_flops, g_bytes = gemm1_algorithmic(rows_kept, d, ffn, n_touched)
     t_g = stage_s[3]
     g_bound = "hbm" if g_bytes / (peaks["hbm_gbs"] * 1e9) > g_flops / (peaks["bf16_tflops"] * 1e12) else "tensor"
@@ -525,34 +521,17 @@ def measure(args, rank, world, local):
         achieved, peak, unit = g_bytes / t_g / 1e9, peaks["hbm_gbs"], "GB/s"
     else:
         achieved, peak, unit = g_flops / t_g / 1e12, peaks["bf16_tflops"], "TFLOP/s"
-
-    line = {
-        "metric": METRIC,
-        "value": T * world * args.steps / elapsed_max,
-        "unit": "tokens/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
+    res.update({
+        "value": T * world * steps / elapsed_max,
         "ms_per_step": t_step * 1e3,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic: seeded x~N(0,1), weights~N(0,1/fan_in), random init",
-        "config": {
-            "workload": workload, "T": T, "d": d, "ffn": ffn, "E": E, "k": k,
-            "tokens_per_gpu": T, "parallelism": f"replicas x{world} (no data-path collective)",
-            "l2": "no flush: each step streams the touched experts' weights "
-                  f"({n_touched * 3 * d * ffn * 2 / 1e9:.2f} GB) > 126 MB L2",
-            "experts_touched": n_touched, "rows_per_expert": counts.tolist(),
-            "rows_computed": rows_kept, "routing": route_kw,
-        },
+        "routing": {"experts_touched": n_touched, "rows_per_expert": counts.tolist(),
+                    "rows_computed": rows_kept, "options": route_kw},
         "roofline": {
             "kernel": "grouped gate/up GEMM + SwiGLU (tcgen05, "
                       + ("CTA pairs, tokens as N)" if uses_pairs(T, k, E) else "one CTA per tile)"),
             "bound": g_bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "peak_source": f"{peak_src} (burst)",
-            "traffic": None if overrides else recorded_traffic(f"gate_up_{args.config}"),
+            "traffic": recorded_traffic(traffic_key) if traffic_key else None,
             "traffic_source": "profiles/ncu_traffic.json (dram__bytes_read.sum + "
                               "dram__bytes_write.sum, one ncu capture; null if the kernel "
                               "source changed since)",
@@ -560,28 +539,76 @@ def measure(args, rank, world, local):
             "launch_us": t_g * 1e6,
         },
         "layer_roofline": {
-            "bound": layer_bound, "roofline_us": t_roof * 1e6, "measured_us": t_step * 1e3 * 1e3,
+            "bound": layer_bound, "roofline_us": t_roof * 1e6, "measured_us": t_step * 1e6,
             "frac": t_roof / t_step, "algorithmic_bytes": bytes_, "algorithmic_flops": flops,
-            "frac_vs_sustained_tc": (max(bytes_ / (peaks["hbm_gbs"] * 1e9),
-                                         flops / (peaks["bf16_tflops_sustained"] * 1e12)) / t_step),
+            "frac_vs_sustained_tc": (max(t_hbm, flops / (peaks["bf16_tflops_sustained"] * 1e12))
+                                     / t_step),
         },
         "stages_us": {n: s * 1e6 for n, s in zip(stage_names, stage_s)},
-        "e2e": {"value": T * world * args.steps / e2e_elapsed, "unit": "tokens/s",
-                "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2,
-                "how": "per step: pinned x -> device copy, moe_forward, output -> pinned "
-                       "host copy; the layer calls run one after another on one stream, the "
-                       "copies on two copy streams with two buffer sets, so they overlap the "
-                       "neighbouring steps' kernels" +
-                       ("" if not (args.gating or cap) else " (default routing options)"),
-                "output_matches_device_path": e2e_match},
         "timed_as": "CUDA graph replay of one moe_forward call per step" if graph is not None
                     else "moe_forward called per step",
-        "direct_call_tokens_per_s": T * world * args.steps / direct_elapsed,
-        "gpu_launches": moe.forward_launches(T, d, ffn, E, k, moe.BF16) * args.steps,
+        "direct_call_tokens_per_s": T * world * steps / direct_elapsed,
+        "gpu_launches": moe.forward_launches(T, d, ffn, E, k, moe.BF16) * steps,
         "clocks": clocks.summary(),
+    })
+    res["_x"], res["_layer"] = x, layer
+    return res
+
+
+def measure(args, rank, world, local):
+    import torch
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    cfg, overrides = workload_cfg(args, args.config)
+    T, E, k = cfg["T"], cfg["E"], cfg["k"]
+    route_kw, notes = route_options(args, T, k, E)
+    config = config_record(args.config, cfg, overrides + notes, world)
+    tkey = None if (overrides or notes) else f"gate_up_{args.config}"
+    r = bench_layer(args, args.config, cfg, route_kw, dev, rank, world, local, args.steps,
+                    args.warmup, with_e2e=True, traffic_key=tkey)
+    x, layer = r.pop("_x"), r.pop("_layer")
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(x, layer, k)
+    del x, layer
+    # the tensor-core half of the metric: prefill T=4096 in the same run
+    sub = None
+    if args.config == "decode" and not (overrides or notes) and not args.no_prefill:
+        torch.cuda.empty_cache()
+        pcfg, _ = workload_cfg(argparse.Namespace(), "prefill")
+        pkw, _ = route_options(argparse.Namespace(capacity_factor=0.0, drop_policy="lose",
+                                                  gating=0), pcfg["T"], pcfg["k"], pcfg["E"])
+        sub = bench_layer(args, "prefill", pcfg, pkw, dev, rank, world, local,
+                          max(args.steps, 10), args.warmup, traffic_key="gate_up_prefill")
+        sub.pop("_x")
+        sub.pop("_layer")
+        sub = {"config": config_record("prefill", pcfg, [], world), "unit": "tokens/s",
+               "steps": max(args.steps, 10), **sub}
+        torch.cuda.empty_cache()
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC,
+        "value": r.pop("value"),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": r.pop("ms_per_step"),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded x~N(0,1), weights~N(0,1/fan_in), random init",
+        "config": config,
+        **r,
     }
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(x, layer, k)
+    if sub is not None:
+        line["prefill"] = sub
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
     return 0
 
@@ -815,6 +842,57 @@ def measure_backward(args, rank, world, local):
     return 0
 
 
+def relaunch(n: int, argv) -> int:
+    """Run this script under torchrun with n ranks on this node (rendezvous on
+    127.0.0.1); returns its exit code.  Rank 0 prints the line."""
+    import socket
+    import subprocess
+    sock = socket.socket()
+    sock.bind(("127.0.0.1", 0))
+    port = sock.getsockname()[1]
+    sock.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.abspath(__file__), *argv]
+    return subprocess.run(cmd).returncode
+
+
+def measure_dry(args, rank, world):
+    """The multi-rank plumbing without a GPU: gloo process group, per-rank
+    token batches against shared weights (drawn on the CPU), barriers around
+    a timed region of host no-ops and the slowest rank's time.  Measures
+    nothing about the layer; the line is marked as a dry run."""
+    from sparse_mixture_experts_58_b300 import inputs
+    dist_init(world, "gloo")
+    T, d = 8, 64
+    x, _ = inputs.draw_tokens(inputs.generator(rank_token_seed(0, rank), "cpu"), T, d, "bf16",
+                              "cpu")
+    layer = inputs.draw_weights(inputs.generator(1000, "cpu"), d, 64, 4, "bf16", "cpu")
+    digest = (float(x.float().sum()), float(layer.W1.float().sum()))
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        time.sleep(0.001)
+    barrier(world)
+    elapsed = reduce_max(time.perf_counter() - t0, world, "cpu")
+    digests = [digest]
+    if world > 1:
+        import torch.distributed as dist
+        digests = [None] * world
+        dist.all_gather_object(digests, digest)
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC + " [dry run: no GPU work]", "dry_run": True,
+            "value": T * world * args.steps / elapsed, "unit": "host no-op steps x tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "scaling": "weak", "ranks": [{"rank": i, "tokens_sum": dg[0], "w1_sum": dg[1]}
+                                         for i, dg in enumerate(digests)]}), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -836,10 +914,22 @@ def main(argv=None):
                     help="time direct moe_forward calls instead of a captured CUDA graph")
     ap.add_argument("--backward", action="store_true",
                     help="time the layer's backward (moe_backward) instead of the forward")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the prefill (T=4096) sub-record of the default decode run")
+    ap.add_argument("--dry-run", action="store_true",
+                    help="rank plumbing only, on CPU over gloo: no GPU work, no kernels "
+                         "(the line says so); for tests of --gpus N")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # one process per GPU: relaunch this command under torchrun
+        return relaunch(args.gpus, sys.argv[1:] if argv is None else list(argv))
     rank, world, local = dist_env()
+    if world != args.gpus:
+        raise SystemExit(f"bench.py: --gpus {args.gpus} but the launch gives {world} rank(s)")
+    if args.dry_run:
+        return measure_dry(args, rank, world)
     if args.impl == "reference":
         if args.config == "sweep":
             args.config = "decode"

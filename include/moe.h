@@ -328,9 +328,12 @@ int moe_forward_launches(int T, int d, int ffn, int E, int k, int dtype, int *la
  * process exits, so no workspace is passed and nothing is allocated.  The
  * caller still passes x, the weights and out.
  *   - Shapes whose moe_workspace_bytes(...) exceeds MOE_STATIC_SCRATCH_BYTES
- *     are rejected with MOE_ERR_WORKSPACE before anything is enqueued (at the
- *     Mixtral shape, d = 4096 and ffn = 14336 with 8 experts and top-2,
- *     this covers batches of up to 70 tokens).
+ *     are rejected with MOE_ERR_WORKSPACE before anything is enqueued.  At
+ *     the Mixtral shape (d = 4096, ffn = 14336, 8 experts, top-2) every
+ *     batch of up to 81 tokens fits.  Whether a batch fits depends on its
+ *     tile plan (the token tile height and the down projection's split
+ *     change with T), so it is not monotone in T (some larger batches fit
+ *     too): check moe_workspace_bytes(...) <= MOE_STATIC_SCRATCH_BYTES.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture begins.

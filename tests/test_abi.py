@@ -216,3 +216,16 @@ def test_backward_validates_before_launch(moe):
     assert lib.moe_backward_workspace_bytes(16, 256, 512, E, 2, moe.BF16, ctypes.byref(n)) == 0
     assert n.value > 0
     assert lib.moe_backward_workspace_bytes(16, 256, 512, E, 2, moe.F32, ctypes.byref(n)) == -2
+
+
+def test_static_scratch_limit_stated_in_header():
+    """The header's statement of the fixed scratch array's reach: at the
+    Mixtral shape every batch of up to 81 tokens fits, 82 does not, and a
+    larger batch can fit again (the fit follows the tile plan)."""
+    from sparse_mixture_experts_58_b300 import moe
+    hdr = re.sub(r"\s*\n\s*\*\s*", " ", open(HEADER).read())
+    assert "every batch of up to 81 tokens fits" in hdr
+    fits = [moe.workspace_bytes(T, 4096, 14336, 8, 2, moe.BF16) <= moe.STATIC_SCRATCH_BYTES
+            for T in range(1, 200)]
+    assert all(fits[:81]) and not fits[81]
+    assert any(fits[82:])

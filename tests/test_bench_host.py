@@ -88,3 +88,21 @@ def test_pair_plan_predicate(monkeypatch):
     assert bench.uses_pairs(512, K, E)
     monkeypatch.setenv("MOE_PLAN_PAIR", "0")
     assert not bench.uses_pairs(4096, K, E)
+
+
+def test_config_is_the_same_for_both_arms():
+    """Both arms print config_record(...) of the same workload: the shape and
+    the workload's name only, nothing a run observes (routing)."""
+    import argparse
+    ns = argparse.Namespace(T=0, E=0, k=0)
+    for name in ("decode", "prefill", "skewed"):
+        cfg, over = bench.workload_cfg(ns, name)
+        a = bench.config_record(name, cfg, over, 1)
+        b = bench.config_record(name, dict(cfg), list(over), 1)
+        assert a == b
+        assert set(a) == {"workload", "T", "d", "ffn", "E", "k", "tokens_per_gpu",
+                          "parallelism", "l2"}
+        assert (a["d"], a["ffn"], a["E"], a["k"]) == (D, FFN, E, K)
+    cfg, over = bench.workload_cfg(argparse.Namespace(T=1024, E=0, k=0), "decode")
+    assert cfg["T"] == 1024 and over == ["T=1024"]
+    assert "T=1024" in bench.config_record("decode", cfg, over, 1)["workload"]

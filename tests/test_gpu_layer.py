@@ -43,7 +43,7 @@ def check_layer(moe, x, layer, k, rows=None, dtype=None, label="", exclude_ties=
     keep = ~helpers.near_tie_mask(rl, k) if exclude_ties else np.ones(len(rl), bool)
     err = helpers.rel_error(got[keep], ref[keep], dtype)
     raw = helpers.raw_rel_error(got[keep], ref[keep])
-    print(f"{label}: rel err {err:.3e} (raw max|d|/rms {raw:.3e}) over {keep.sum()} tokens, "
+    print(f"PARITY {label}: gated {err:.3e} raw max|d|/rms {raw:.3e} over {keep.sum()} tokens, "
           f"{(~keep).sum()} near ties")
     assert err <= helpers.tol(dtype), (label, err)
     assert keep.mean() > 0.9
@@ -199,31 +199,47 @@ def test_decode_weights_few_tokens(moe, decode_case, T):
     check_layer(moe, x[:T].contiguous(), layer, 2, label=f"decode weights T={T}")
 
 
+def _layout_sample(x, layer, k, per_expert, seed, must=(), row_tiles=()):
+    """Tokens to compare, chosen from the oracle's grouping of the whole
+    batch: every expert's first and last grouped rows, the edges and CTA
+    halves of its token tiles, and at least `per_expert` rows per expert."""
+    host = inputs.layer_to_host(layer)
+    _, idx, offsets, perm = helpers.oracle_layout(inputs.to_host(x), host, k)
+    rows = helpers.layout_rows(idx, offsets, perm, k, per_expert=per_expert, seed=seed,
+                               must=must, row_tiles=row_tiles)
+    return rows, host, idx
+
+
 def test_prefill_config_sampled(moe):
+    """Prefill T=4096: the tokens at every expert's grouped-layout edges and
+    tile edges, and at least 32 rows per expert."""
     x, layer = inputs.make_named("prefill", device="cuda")
-    rows = helpers.sample_rows(4096, 48, seed=1)
-    check_layer(moe, x, layer, 2, rows=rows, label="prefill T=4096 (48 sampled)")
+    rows, host, idx = _layout_sample(x, layer, 2, per_expert=32, seed=1)
+    for e in range(layer.E):
+        assert (idx[rows] == e).any(1).sum() >= 32
+    check_layer(moe, x, layer, 2, rows=rows, label=f"prefill T=4096 ({len(rows)} layout rows)")
     del x, layer
     torch.cuda.empty_cache()
 
 
 def test_skewed_config_sampled(moe):
+    """Skewed routing T=8192: layout edges of every expert (expert 0 holds
+    about 43% of the rows, expert 7 a handful), duplicate pairs, and at least
+    16 rows per expert (all of them for the rarest)."""
     x, layer = inputs.make_named("skewed", device="cuda")
     dst, src = layer.meta["dups"]
     must = list(dst[:12]) + list(src[:12])
-    rows = helpers.sample_rows(8192, 56, seed=2, must=must)
-    # expert 6 and 7 rows are rare: include some of them
-    logits, idx, _ = moe.router(x, layer.Wg, 2, layer.bias)
-    torch.cuda.synchronize()
-    rare = torch.nonzero((idx == 7).any(1)).flatten()[:4].cpu().numpy()
-    rows = np.union1d(rows, rare)
-    out, ref, keep = check_layer(moe, x, layer, 2, rows=rows, label="skewed T=8192 (sampled)")
+    rows, host, idx = _layout_sample(x, layer, 2, per_expert=16, seed=2, must=must)
+    out, ref, keep = check_layer(moe, x, layer, 2, rows=rows,
+                                 label=f"skewed T=8192 ({len(rows)} layout rows)")
     # exact duplicates give bit-identical outputs
     o = out[torch.as_tensor(dst, device="cuda")].view(torch.int16)
     s = out[torch.as_tensor(src, device="cuda")].view(torch.int16)
     assert torch.equal(o, s)
-    counts = torch.bincount(idx.flatten().long(), minlength=8).cpu().numpy()
+    counts = np.bincount(idx.flatten(), minlength=8)
     assert counts[0] > 5 * counts[2] and counts.sum() == 2 * 8192
+    for e in range(8):
+        assert (idx[rows] == e).any(1).sum() >= min(16, counts[e])
     del x, layer
     torch.cuda.empty_cache()
 
@@ -263,3 +279,68 @@ def test_stacked_layers_sampled(moe):
             helpers.rel_error(inputs.to_host(x), o.add(x_host, out_host), "bf16") <= 1e-2
         del layer
     print(f"stacked layers: worst per-layer rel err {worst:.3e}")
+
+
+# Token-count sweep at the Mixtral shape: the layers each token count is
+# checked at (the chain runs all 32).
+SWEEP_CHECK = {1: (0, 1, 15, 31), 1024: (0, 1, 31), 16384: (0, 31)}
+EPS = 1e-5
+
+
+def test_sweep_blocks_mixtral_shape(moe):
+    """The token-count sweep workload as the benchmark times it: 32 pre-norm
+    blocks x <- x + MoE(RMSNorm(x)) (moe_block_forward, RMSNorm fused into the
+    router and the grouping, residual into the combine) with independent
+    weights at hidden 4096, expert width 14336, 8 experts, top-2, for T = 1,
+    1024 and 16384.  At the checked layers the oracle gets the GPU's own
+    layer input: its RMSNorm, its layer (every token at T = 1, layout rows
+    otherwise) and the residual add.  The error beyond the block's two
+    roundings (the layer output, then the sum: half an ulp each) must be
+    within the bf16 bar of the layer output's RMS."""
+    cfg = inputs.WORKLOADS["sweep"]
+    d, ffn, E, k, L = cfg["d"], cfg["ffn"], cfg["E"], cfg["k"], cfg["layers"]
+    o = oracle.load()
+    xs = {T: inputs.sweep_tokens(T, d, device="cuda") for T in SWEEP_CHECK}
+    ws = moe.Workspace("cuda")
+    worst = {T: (0.0, 0.0) for T in SWEEP_CHECK}
+    for l in range(L):
+        layer = inputs.sweep_layer(l, d, ffn, E, device="cuda", seed0=cfg["layer_seed0"])
+        host = None
+        for T, x in xs.items():
+            check = l in SWEEP_CHECK[T]
+            x_before = inputs.to_host(x) if check else None
+            moe.block_forward(x, layer.Wg, layer.W1, layer.W3, layer.W2, k, eps=EPS,
+                              workspace=ws)
+            if not check:
+                continue
+            torch.cuda.synchronize()
+            if host is None:
+                host = inputs.layer_to_host(layer)
+            xn = o.rmsnorm(x_before, EPS)
+            if T <= 64:
+                rows = np.arange(T)
+            else:
+                _, idx, offsets, perm = helpers.oracle_layout(xn, host, k)
+                rows = helpers.layout_rows(idx, offsets, perm, k, per_expert=16,
+                                           seed=l + T, halves=T <= 4096,
+                                           row_tiles=(128,) if T <= 1024 else ())
+            out, rl, _, _, exact = o.moe_forward(xn[rows], *host[:4], k, exact=True)
+            got = helpers.host_f64(inputs.to_host(x)[rows])
+            ref = helpers.host_f64(x_before[rows]) + exact
+            keep = ~helpers.near_tie_mask(rl, k)
+            assert keep.mean() > 0.9 or T == 1
+            if not keep.any():
+                continue
+            rms = float(np.sqrt((exact[keep] ** 2).mean()))
+            excess = (np.abs(got - ref) - helpers.bf16_half_ulp(got)
+                      - helpers.bf16_half_ulp(exact))[keep]
+            err = max(float(excess.max()), 0.0) / rms
+            raw = float(np.abs(got - ref)[keep].max()) / rms
+            print(f"PARITY sweep T={T} layer {l}: gated {err:.3e} raw max|d|/rms {raw:.3e} "
+                  f"over {keep.sum()} tokens, {(~keep).sum()} near ties")
+            worst[T] = (max(worst[T][0], err), max(worst[T][1], raw))
+            assert err <= helpers.TOL_BF16, (T, l, err)
+        del layer, host
+    assert moe.device_status(clear=True) == 0
+    for T, (g, r) in worst.items():
+        print(f"PARITY sweep T={T} worst: gated {g:.3e} raw {r:.3e}")

@@ -69,3 +69,28 @@ def test_single_rank_helpers_are_identities():
     assert bench.reduce_max(3.5, 1, "cpu") == 3.5
     bench.barrier(1)
     assert bench.rank_token_seed(0, 0) == 0 and bench.rank_token_seed(0, 1) != 0
+
+
+def test_bench_main_two_ranks_dry_run(capfd):
+    """bench.main with --gpus 2 outside torchrun relaunches itself with two
+    ranks (gloo in the dry run, no GPU work); rank 0 prints one line for
+    the job: n_gpus 2, each rank its own batch, the weights shared."""
+    import json
+    assert "WORLD_SIZE" not in os.environ
+    rc = bench.main(["--gpus", "2", "--dry-run", "--steps", "3", "--warmup", "3"])
+    assert rc == 0
+    lines = [ln for ln in capfd.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["dry_run"] is True and rec["n_gpus"] == 2
+    assert [r["rank"] for r in rec["ranks"]] == [0, 1]
+    assert rec["ranks"][0]["tokens_sum"] != rec["ranks"][1]["tokens_sum"]
+    assert rec["ranks"][0]["w1_sum"] == rec["ranks"][1]["w1_sum"]
+
+
+def test_bench_refuses_a_world_that_differs_from_gpus(monkeypatch):
+    """A launch whose world size is not --gpus fails loudly."""
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    with pytest.raises(SystemExit):
+        bench.main(["--gpus", "2", "--dry-run", "--steps", "1"])
