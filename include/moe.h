@@ -56,8 +56,10 @@
  *     with the same arguments launch the graph on `stream`: the same kernels
  *     with the same parameters, so the same bits.  The library keeps those
  *     graphs, and the pointers inside them, for up to 64 argument sets per
- *     process; a graph only runs for a call that passes the same pointers
- *     again, and reads the buffers' contents as they are then.  A call on a
+ *     process (a new set replaces the least recently used one); a graph only
+ *     runs for a call that passes the same pointers again, and reads the
+ *     buffers' contents as they are then.  moe_graph_cache_stats reports how
+ *     often calls were served from the cache.  A call on a
  *     stream that is being captured enqueues its kernels directly, into the
  *     caller's graph.  MOE_GRAPHS=0 in the environment turns graphs off.
  *   - Limits: 1 <= E <= 64, 1 <= k <= min(E, 8), T >= 0 (T = 0 is a no-op).
@@ -314,6 +316,26 @@ int moe_selftest_wait_timeout(unsigned int limit_ns, void *stream);
 
 /* Number of kernels moe_forward launches for this shape (for launch counts). */
 int moe_forward_launches(int T, int d, int ffn, int E, int k, int dtype, int *launches);
+
+/*
+ * Counters of the launch-graph cache (see "Launch graphs" above), for all
+ * devices of the process since load or the last reset:
+ *   entries       argument sets held now (at most 64);
+ *   replays       calls served by launching a cached graph;
+ *   captures      graphs captured (the second call of an argument set);
+ *   direct_calls  calls that enqueued their kernels one by one (first call of
+ *                 an argument set, graphs off, a capturing caller stream, or a
+ *                 failed capture);
+ *   evictions     argument sets dropped, least recently used first, to make
+ *                 room for a new one.
+ * A serving loop whose pointers or sizes change every call shows replays near
+ * zero: the cache is not helping it (MOE_GRAPHS=0 turns it off).
+ * reset != 0 zeroes the four counts after reading them.  No device work.
+ */
+typedef struct {
+    long long entries, replays, captures, direct_calls, evictions;
+} moe_graph_stats;
+int moe_graph_cache_stats(moe_graph_stats *stats, int reset);
 
 /*
  * The pages have no counterpart to this entry point: it is a convenience for

@@ -303,6 +303,14 @@ int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p) {
         if (s > kblocks) s = kblocks;
         q.kps = (kblocks + (int)s - 1) / (int)s;
         q.splits = (kblocks + q.kps - 1) / q.kps;
+        // The combine folded into the down projection's epilogue: with one
+        // split and at most two slots per token, each output element gets at
+        // most two fp32 additions into zero, whose sum does not depend on
+        // their order.  MOE_FUSE_COMBINE=0|1 forces it off or on where it
+        // applies (measurement only).
+        q.fuse = (q.pair && q.splits == 1 && k <= 2) ? 1 : 0;
+        if (const char *fc = getenv("MOE_FUSE_COMBINE"))
+            q.fuse = q.fuse && atoi(fc) != 0;
     }
     const int elt = elem_size(dt);
     size_t off = 0;
@@ -380,6 +388,9 @@ int run_forward(const Plan &P, const Options &O, const void *x, const void *W_g,
     float *inv_rms = norm_eps != nullptr ? ws_at<float>(ws, P.o_rms) : nullptr;
     const float eps = norm_eps != nullptr ? *norm_eps : 0.f;
     const int elt = elem_size(P.dt);
+    // combine in the down projection's epilogue: the fp32 [T][d] accumulator
+    // takes the place of y (which holds splits * T * k * d floats)
+    const bool fuse = P.fuse && O.capacity == 0;
     int rc;
     if ((rc = cuda_rc(launch_router(x, W_g, bias, P.T, P.d, P.E, P.k, P.dt, O.gating, eps, inv_rms,
                                     logits, idx, gates, s))) != MOE_OK)
@@ -388,16 +399,19 @@ int run_forward(const Plan &P, const Options &O, const void *x, const void *W_g,
                                         s))) != MOE_OK)
         return rc;
     if ((rc = cuda_rc(launch_group_tokens(idx, cb, offsets, x, inv_rms, P.T, P.d, P.E, P.k,
-                                          O.capacity, elt, perm, inv, x_perm, s))) != MOE_OK)
+                                          O.capacity, elt, perm, inv, x_perm, s,
+                                          fuse ? y : nullptr))) != MOE_OK)
         return rc;
     if (P.dt == MOE_BF16) {
         if (P.pair) {
             if ((rc = launch_swiglu_pair(x_perm, offsets, W1, W3, P.rows, P.d, P.ffn, P.E, h,
                                          s)) != MOE_OK)
                 return rc;
-            if ((rc = launch_down_pair(h, offsets, W2, P.rows, P.d, P.ffn, P.E, P.splits, P.kps,
-                                       y, s)) != MOE_OK)
-                return rc;
+            rc = fuse ? launch_down_pair_combine(h, offsets, W2, P.rows, P.d, P.ffn, P.E, perm,
+                                                 gates, P.k, y, s)
+                      : launch_down_pair(h, offsets, W2, P.rows, P.d, P.ffn, P.E, P.splits,
+                                         P.kps, y, s);
+            if (rc != MOE_OK) return rc;
         } else {
             if ((rc = launch_swiglu_tc(x_perm, offsets, W1, W3, P.rows, P.d, P.ffn, P.E, P.bm,
                                        P.wide, h, s)) != MOE_OK)
@@ -415,6 +429,8 @@ int run_forward(const Plan &P, const Options &O, const void *x, const void *W_g,
                                           P.ffn, P.E, y, s))) != MOE_OK)
             return rc;
     }
+    if (fuse)
+        return cuda_rc(launch_finalize(y, P.T, P.d, norm_eps != nullptr ? 1 : 0, P.dt, out, s));
     return cuda_rc(launch_combine(y, P.splits, P.rows, gates, inv, P.T, P.d, P.k, O.renorm,
                                   norm_eps != nullptr ? 1 : 0, P.dt, out, s));
 }
@@ -504,17 +520,34 @@ int make_bwd_plan(int T, int d, int ffn, int E, int k, int dt, BwdPlan *p) {
 // and launches the graph on the caller's stream, as do later calls.  A call on
 // a stream that is being captured itself enqueues its kernels directly, so
 // they land in the caller's graph.  At most kGraphSlots argument sets are
-// kept (later ones run directly).  MOE_GRAPHS=0 turns graphs off.
+// kept: a new one takes the place of the one used least recently (its graph
+// is destroyed; one still running is freed when it completes).  Counters of
+// replays, captures, direct calls and evictions are read with
+// moe_graph_cache_stats.  MOE_GRAPHS=0 turns graphs off.
 constexpr size_t kGraphSlots = 64;
 
 struct GraphEntry {
     cudaGraphExec_t exec = nullptr;
     bool failed = false;
+    unsigned long long last_use = 0;
 };
 
 std::mutex g_graph_mutex;
 std::unordered_map<std::string, GraphEntry> g_graphs;
 cudaStream_t g_capture_stream[64];
+unsigned long long g_graph_tick = 0;
+moe_graph_stats g_graph_stats = {0, 0, 0, 0, 0};
+
+// Caller holds g_graph_mutex.  Drops the least recently used argument set.
+void evict_lru_graph() {
+    auto victim = g_graphs.end();
+    for (auto it = g_graphs.begin(); it != g_graphs.end(); ++it)
+        if (victim == g_graphs.end() || it->second.last_use < victim->second.last_use) victim = it;
+    if (victim == g_graphs.end()) return;
+    if (victim->second.exec != nullptr) cudaGraphExecDestroy(victim->second.exec);
+    g_graphs.erase(victim);
+    ++g_graph_stats.evictions;
+}
 
 bool graphs_enabled() {
     const char *v = getenv("MOE_GRAPHS");
@@ -536,7 +569,7 @@ class LaunchKey {
     }
     LaunchKey &plan(const Plan &P) {
         return add(P.T).add(P.d).add(P.ffn).add(P.E).add(P.k).add(P.dt).add(P.rows).add(P.wide)
-            .add(P.pair).add(P.bm).add(P.splits).add(P.kps).add(P.bytes);
+            .add(P.pair).add(P.bm).add(P.splits).add(P.kps).add(P.fuse).add(P.bytes);
     }
     LaunchKey &opts(const Options &O) { return add(O.gating).add(O.capacity).add(O.renorm); }
     const std::string &str() const { return s_; }
@@ -547,32 +580,50 @@ class LaunchKey {
 
 template <typename F>
 int run_graphed(const LaunchKey &key, cudaStream_t user, F &&enqueue) {
-    if (!graphs_enabled()) return enqueue(user);
+    auto direct = [&]() {
+        {
+            std::lock_guard<std::mutex> g(g_graph_mutex);
+            ++g_graph_stats.direct_calls;
+        }
+        return enqueue(user);
+    };
+    if (!graphs_enabled()) return direct();
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(user, &cs) != cudaSuccess) {
         cudaGetLastError();
-        return enqueue(user);
+        return direct();
     }
-    if (cs != cudaStreamCaptureStatusNone) return enqueue(user);
+    if (cs != cudaStreamCaptureStatusNone) return direct();
     const int dev = current_device();
-    if (dev < 0 || dev >= 64) return enqueue(user);
+    if (dev < 0 || dev >= 64) return direct();
     std::string k = key.str();
     k.append(reinterpret_cast<const char *>(&dev), sizeof dev);
     std::lock_guard<std::mutex> g(g_graph_mutex);
     auto it = g_graphs.find(k);
     if (it == g_graphs.end()) {
-        if (g_graphs.size() < kGraphSlots) g_graphs.emplace(k, GraphEntry());
+        if (g_graphs.size() >= kGraphSlots) evict_lru_graph();
+        GraphEntry fresh;
+        fresh.last_use = ++g_graph_tick;
+        g_graphs.emplace(k, fresh);
+        ++g_graph_stats.direct_calls;
         return enqueue(user);
     }
     GraphEntry &e = it->second;
-    if (e.exec != nullptr)
+    e.last_use = ++g_graph_tick;
+    if (e.exec != nullptr) {
+        ++g_graph_stats.replays;
         return cudaGraphLaunch(e.exec, user) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-    if (e.failed) return enqueue(user);
+    }
+    if (e.failed) {
+        ++g_graph_stats.direct_calls;
+        return enqueue(user);
+    }
     if (g_capture_stream[dev] == nullptr &&
         cudaStreamCreateWithFlags(&g_capture_stream[dev], cudaStreamNonBlocking) != cudaSuccess) {
         g_capture_stream[dev] = nullptr;
         cudaGetLastError();
         e.failed = true;
+        ++g_graph_stats.direct_calls;
         return enqueue(user);
     }
     cudaStream_t cap = g_capture_stream[dev];
@@ -589,9 +640,11 @@ int run_graphed(const LaunchKey &key, cudaStream_t user, F &&enqueue) {
     if (exec == nullptr) {
         cudaGetLastError();
         e.failed = true;
+        ++g_graph_stats.direct_calls;
         return enqueue(user);
     }
     e.exec = exec;
+    ++g_graph_stats.captures;
     return cudaGraphLaunch(exec, user) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -770,6 +823,15 @@ int moe_forward_launches(int T, int d, int ffn, int E, int k, int dtype, int *la
     const int rc = make_plan(T, d, ffn, E, k, dtype, &P);
     if (rc != MOE_OK) return rc;
     *launches = T == 0 ? 0 : 6;  // router, scan, group, gate/up, down, combine
+    return MOE_OK;
+}
+
+int moe_graph_cache_stats(moe_graph_stats *stats, int reset) {
+    if (stats == nullptr) return MOE_ERR_ARG;
+    std::lock_guard<std::mutex> g(g_graph_mutex);
+    *stats = g_graph_stats;
+    stats->entries = static_cast<long long>(g_graphs.size());
+    if (reset) g_graph_stats = moe_graph_stats{0, 0, 0, 0, 0};
     return MOE_OK;
 }
 

@@ -185,6 +185,40 @@ void launch_combine_dt(const float *y, int splits, int rows, const float *gates,
     launch(y, splits, rows, gates, inv, T_, d, k, renorm, residual, out, s);
 }
 
+// Gated sums accumulated by the down projection's epilogue (fp32 [T][d], the
+// gate-weighted outputs of a token's slots added into a zeroed row) rounded
+// once to the output type; with `residual`, out <- round(out + round(sum)),
+// the rounding of the combine's residual form.  One block per (token, 1024 * C
+// columns), 16-byte loads.
+template <typename T, int C>
+__global__ void __launch_bounds__(256) finalize_kernel(const float *__restrict__ acc, int d,
+                                                       int residual, T *out) {
+    pdl_wait();
+    pdl_trigger();
+    const int t = blockIdx.x;
+    const int nv = d / 4;
+    const float4 *src = reinterpret_cast<const float4 *>(acc) + (size_t)t * nv;
+    float4 a[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+        const int v = blockIdx.y * 256 * C + threadIdx.x + 256 * c;
+        a[c] = v < nv ? __ldcs(src + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+        const int v = blockIdx.y * 256 * C + threadIdx.x + 256 * c;
+        if (v >= nv) continue;
+        T *dst = out + (size_t)t * d + 4 * v;
+        float4 o = a[c];
+        if (residual) {
+            const float4 r = load4<T>(dst);
+            o = make_float4(r.x + round_to<T>(o.x), r.y + round_to<T>(o.y),
+                            r.z + round_to<T>(o.z), r.w + round_to<T>(o.w));
+        }
+        store4<T>(dst, o);
+    }
+}
+
 // One block of kNormThreads per row: optional residual add (rounded to the
 // storage type), then RMSNorm with gain 1 in the order common.cuh fixes, the
 // order the router's fused normalisation repeats.  d is a multiple of one
@@ -248,6 +282,18 @@ cudaError_t launch_combine(const float *y, int splits, int rows, const float *ga
     else
         launch_combine_dt<float>(y, splits, rows, gates, inv, T, d, k, renorm, residual, out, s);
     return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float *acc, int T, int d, int residual, int dt, void *out,
+                            cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    constexpr int C = 2;
+    const dim3 grid(T, (d / 4 + 256 * C - 1) / (256 * C));
+    if (dt == MOE_BF16)
+        return launch_pdl(finalize_kernel<__nv_bfloat16, C>, grid, 256, 0, s, acc, d, residual,
+                          static_cast<__nv_bfloat16 *>(out));
+    return launch_pdl(finalize_kernel<float, C>, grid, 256, 0, s, acc, d, residual,
+                      static_cast<float *>(out));
 }
 
 cudaError_t launch_add_rmsnorm(void *x, const void *add, void *xn, int T, int d, float eps, int dt,

@@ -126,6 +126,34 @@ __device__ __forceinline__ float warp_butterfly_sum(float v) {
     return v;
 }
 
+// The butterfly sums of N values per lane at once (N a power of two <= 32),
+// each lane keeping only some of them: at the step with offset o, while more
+// than one value is left, a lane keeps the half of its values selected by
+// (lane & o) and adds the partner lane's copy of that half, sending the other
+// half; from then on the one value left is summed as in warp_butterfly_sum.
+// Every sum is formed by the same additions, in the same order, as
+// warp_butterfly_sum gives it (a + b == b + a), so the bits are the same; it
+// costs N - 1 + (5 - log2 N) shuffles instead of 5 N.  On return v[0] holds
+// the sum of value lane >> (5 - log2 N), in every lane.
+template <int N>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[N], int lane) {
+    static_assert(N >= 1 && N <= 32 && (N & (N - 1)) == 0, "N: a power of two up to 32");
+    int off = 16;
+#pragma unroll
+    for (int n = N; n > 1; n >>= 1, off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = upper ? v[i] : v[i + n / 2];
+            const float keep = upper ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+#pragma unroll
+    for (; off > 0; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+    return v[0];
+}
+
 __device__ __forceinline__ float rms_scale(float sumsq, int d, float eps) {
     return 1.f / sqrtf(sumsq / static_cast<float>(d) + eps);
 }

@@ -33,6 +33,8 @@
 //   drain, bye   teardown: the MMA drain, and a pair handshake so neither CTA
 //                leaves while the other may still touch its shared memory.
 // Every wait is bounded as in gemm_tc.cu.
+#include <stdlib.h>
+
 #include <mutex>
 
 #include "internal.h"
@@ -70,10 +72,16 @@ struct PairArgs {
     CUtensorMap mapW0[kMaxE];      // W1[e] (gate/up, box {64, 64}) or W2[e] (down, box {64, 128})
     CUtensorMap mapW1[kMaxE];      // W3[e] (gate/up only, box {64, 64})
     const int *offsets;            // [E + 1]
-    void *out;                     // h bf16 [rows][N]  or  y fp32 [splits][rows][N]
+    void *out;                     // h bf16 [rows][N], y fp32 [splits][rows][N],
+                                   // or (combine) acc fp32 [T][N]
+    const int *perm;               // combine: row -> token * k + slot
+    const float *gates;            // combine: [T][k]
     int *status;
     unsigned long long wait_limit_ns;
     int E, rows, K, N, kblocks, kps, splits;
+    int k;        // combine: experts per token
+    int combine;  // down only: add gate x output into acc[token] (one split)
+    int hints;    // L2 policy of the copies: bit 0 weights evict-first, bit 1 tokens evict-last
 };
 
 struct PairUnit {
@@ -206,6 +214,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ producers
         if (lane == 0) {
             const uint32_t full0 = ptx::map_to_rank(ptx::smem_addr(&full[0]), 0);
+            const uint64_t pol_w = ptx::policy_evict_first();
+            const uint64_t pol_t = ptx::policy_evict_last();
+            const bool hint_w = (a.hints & 1) != 0, hint_t = (a.hints & 2) != 0;
             int stage = 0;
             uint32_t ph = 0;
             int issued = 0;
@@ -227,13 +238,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t fb = full0 + static_cast<uint32_t>(stage) * 8u;
                     uint8_t *dA = sA + stage * kABytes;
                     const int kx = kb * kBlockK;
-                    if (SWIGLU) {
-                        ptx::tma_load_2d_pair(dA, &a.mapW0[w.e], kx, wrow, fb);
-                        ptx::tma_load_2d_pair(dA + kGate * 128, &a.mapW1[w.e], kx, wrow, fb);
+                    if (hint_w) {
+                        ptx::tma_load_2d_pair_hint(dA, &a.mapW0[w.e], kx, wrow, fb, pol_w);
+                        if (SWIGLU)
+                            ptx::tma_load_2d_pair_hint(dA + kGate * 128, &a.mapW1[w.e], kx, wrow,
+                                                       fb, pol_w);
                     } else {
                         ptx::tma_load_2d_pair(dA, &a.mapW0[w.e], kx, wrow, fb);
+                        if (SWIGLU)
+                            ptx::tma_load_2d_pair(dA + kGate * 128, &a.mapW1[w.e], kx, wrow, fb);
                     }
-                    ptx::tma_load_2d_pair(sB + stage * kBBytes, mt, kx, trow, fb);
+                    if (hint_t)
+                        ptx::tma_load_2d_pair_hint(sB + stage * kBBytes, mt, kx, trow, fb, pol_t);
+                    else
+                        ptx::tma_load_2d_pair(sB + stage * kBBytes, mt, kx, trow, fb);
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;
@@ -365,6 +383,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
+            } else if (a.combine) {
+                // the combine: each of the chunk's rows adds gate x output into
+                // its token's accumulator row (lane i fetches row i's token and
+                // gate, shared across the warp)
+                const int f = w.n0 + static_cast<int>(rank) * kHalfM + quad * 32 + lane;
+                float *acol = static_cast<float *>(a.out) + f;
+                const bool f_ok = f < a.N;
+#pragma unroll 1
+                for (int j0 = 32 * cset; j0 < w.ntok; j0 += 64) {
+                    uint32_t Y[32];
+                    ptx::tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(j0), Y);
+                    int my_tok = 0;
+                    float my_gate = 0.f;
+                    if (j0 + lane < w.nvalid) {
+                        const int p = a.perm[w.t0 + j0 + lane];
+                        my_tok = a.k == 2 ? (p >> 1) : p / a.k;
+                        my_gate = a.gates[p];
+                    }
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int tok = __shfl_sync(0xffffffffu, my_tok, i);
+                        const float g = __shfl_sync(0xffffffffu, my_gate, i);
+                        if (f_ok && j0 + i < w.nvalid)
+                            atomicAdd(acol + (size_t)tok * a.N, g * __uint_as_float(Y[i]));
+                    }
+                }
             } else {
                 const int f = w.n0 + static_cast<int>(rank) * kHalfM + quad * 32 + lane;
                 float *ycol = static_cast<float *>(a.out) + (size_t)w.ks * a.rows * a.N + f;
@@ -445,6 +490,13 @@ int fill_pair(PairArgs &args, const void *tokens, const int *offsets, void *out,
               int N, int E) {
     args.offsets = offsets;
     args.out = out;
+    args.perm = nullptr;
+    args.gates = nullptr;
+    args.k = 1;
+    args.combine = 0;
+    // MOE_PAIR_HINTS (measurement only): bit 0 weights evict-first, bit 1 tokens evict-last
+    args.hints = 0;
+    if (const char *h = getenv("MOE_PAIR_HINTS")) args.hints = atoi(h) & 3;
     args.E = E;
     args.rows = rows;
     args.K = K;
@@ -499,6 +551,27 @@ int launch_down_pair(const void *h, const int *offsets, const void *const *W2, i
     args.kps = kps;
     const int NT = (d + kPairM - 1) / kPairM;
     return run_pair<false>(args, token_tiles_bound(rows, E) * NT * splits, s);
+}
+
+int launch_down_pair_combine(const void *h, const int *offsets, const void *const *W2, int rows,
+                             int d, int ffn, int E, const int *perm, const float *gates, int k,
+                             float *acc, cudaStream_t s) {
+    if (rows == 0) return MOE_OK;
+    if (k < 1 || k > 2 || perm == nullptr || gates == nullptr) return MOE_ERR_ARG;
+    PairArgs args;
+    int rc = fill_pair(args, h, offsets, acc, rows, ffn, d, E);
+    if (rc != MOE_OK) return rc;
+    for (int e = 0; e < E; ++e)
+        if ((rc = encode_map_bf16_2d(&args.mapW0[e], W2[e], ffn, d, kBlockK, kHalfM)) != MOE_OK)
+            return rc;
+    args.splits = 1;
+    args.kps = args.kblocks;
+    args.perm = perm;
+    args.gates = gates;
+    args.k = k;
+    args.combine = 1;
+    const int NT = (d + kPairM - 1) / kPairM;
+    return run_pair<false>(args, token_tiles_bound(rows, E) * NT, s);
 }
 
 }  // namespace moe

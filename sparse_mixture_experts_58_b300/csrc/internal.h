@@ -24,6 +24,9 @@ struct Plan {
     int bm;        // token rows per tile (<= 128)
     int splits;    // split of the down projection's contraction
     int kps;       // 64-wide contraction blocks per split
+    int fuse;      // 1: the down projection's epilogue adds gate x output into
+                   // a zeroed fp32 row per token (the combine), a finalize
+                   // pass rounds it; needs k <= 2, one split, the pair kernel
     // workspace layout (byte offsets, 256-aligned)
     size_t o_logits, o_idx, o_gates, o_ccount, o_cbase, o_counts, o_offsets, o_perm, o_inv;
     size_t o_rms;  // per-token RMSNorm scale (pre-norm blocks)
@@ -83,11 +86,12 @@ cudaError_t launch_chunk_scan(const int *idx, int T, int k, int E, int capacity,
                               int *chunk_base, int *counts, int *offsets, cudaStream_t s,
                               int pad = 1);
 // row_scale != nullptr: each copied row is multiplied by its token's scale
-// and rounded to the storage type (the fused RMSNorm).
+// and rounded to the storage type (the fused RMSNorm).  zero_acc != nullptr:
+// the chunk's rows of the fp32 [T][d] accumulator are set to zero.
 cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int *offsets,
                                 const void *x, const float *row_scale, int T, int d, int E, int k,
                                 int capacity, int elt, int *perm, int *inv, void *x_perm,
-                                cudaStream_t s);
+                                cudaStream_t s, float *zero_acc = nullptr);
 // x_perm[r] = x[perm[r] / k] for r < rows.
 cudaError_t launch_permute(const void *x, const int *perm, int rows, int d, int k, int elt,
                            void *x_perm, cudaStream_t s);
@@ -105,6 +109,13 @@ int launch_swiglu_pair(const void *x_perm, const int *offsets, const void *const
                        cudaStream_t s);
 int launch_down_pair(const void *h, const int *offsets, const void *const *W2, int rows, int d,
                      int ffn, int E, int splits, int kps, float *y, cudaStream_t s);
+// The down projection with the combine in its epilogue: for row r (token
+// perm[r] / k, slot perm[r] % k) it adds gates[perm[r]] * y[r] into acc[token]
+// (fp32 [T][d], zeroed beforehand); one split, k <= 2, so each element gets at
+// most two additions into zero and the sum does not depend on their order.
+int launch_down_pair_combine(const void *h, const int *offsets, const void *const *W2, int rows,
+                             int d, int ffn, int E, const int *perm, const float *gates, int k,
+                             float *acc, cudaStream_t s);
 size_t pair_gemm_smem_bytes();
 
 // Backward of the expert GEMMs (gemm_bwd.cu), on rows grouped by expert with
@@ -152,6 +163,10 @@ cudaError_t launch_down_f32(const float *h, const int *offsets, const void *cons
 cudaError_t launch_combine(const float *y, int splits, int rows, const float *gates,
                            const int *inv, int T, int d, int k, int renorm, int residual, int dt,
                            void *out, cudaStream_t s);
+// out[t] = round(acc[t]) (residual != 0: out[t] <- round(out[t] + round(acc[t])))
+// for the gated sums the down projection's epilogue accumulated.
+cudaError_t launch_finalize(const float *acc, int T, int d, int residual, int dt, void *out,
+                            cudaStream_t s);
 cudaError_t launch_add_rmsnorm(void *x, const void *add, void *xn, int T, int d, float eps,
                                int dt, cudaStream_t s);
 cudaError_t launch_wait_selftest(unsigned int limit_ns, cudaStream_t s);

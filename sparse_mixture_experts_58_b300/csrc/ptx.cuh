@@ -288,6 +288,18 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m
         : "memory");
 }
 
+// The same with an L2 cache-policy hint (from createpolicy).
+__device__ __forceinline__ void tma_load_2d_pair_hint(void *dst, const CUtensorMap *map, int c0,
+                                                      int c1, uint32_t bar_cluster_addr,
+                                                      uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+        "bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster_addr),
+        "l"(policy)
+        : "memory");
+}
+
 // D (+)= A * B^T over the pair: A's M = 256 rows are 128 rows from each CTA's
 // shared memory, B's N rows are split in halves between the CTAs, and each
 // CTA's tensor memory receives its own 128 rows of D.  Issued by one thread

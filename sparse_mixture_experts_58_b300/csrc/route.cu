@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(256) group_tokens_kernel(
     const int *__restrict__ idx, const int *__restrict__ chunk_base,
     const int *__restrict__ offsets, const uint8_t *__restrict__ x,
     const float *__restrict__ row_scale, int elt, int Tn, int E, int k, int capacity,
-    size_t row_bytes, int *perm, int *inv, uint8_t *x_perm) {
+    size_t row_bytes, int *perm, int *inv, uint8_t *x_perm, float *zero_acc) {
     __shared__ int s_idx[kChunk * MOE_MAX_TOPK];
     __shared__ int s_row[kChunk * MOE_MAX_TOPK];
     __shared__ float s_scale[kChunk];
@@ -147,6 +147,18 @@ __global__ void __launch_bounds__(256) group_tokens_kernel(
     const int rowvec_all = static_cast<int>(row_bytes / 16);
     const int vbeg = (int)((long long)rowvec_all * blockIdx.y / gridDim.y);
     const int vend = (int)((long long)rowvec_all * (blockIdx.y + 1) / gridDim.y);
+    if (zero_acc != nullptr) {
+        // the same columns of the tokens' fp32 accumulator rows (4 / elt
+        // float4 per 16-byte vector of x)
+        const int per = 4 / elt;
+        const int nf4 = (vend - vbeg) * per, f4_all = rowvec_all * per;
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 *acc4 = reinterpret_cast<float4 *>(zero_acc) + (size_t)first * f4_all + vbeg * per;
+        for (int i = threadIdx.x; i < ntok * nf4; i += blockDim.x) {
+            const int tk = i / nf4;
+            acc4[(size_t)tk * f4_all + (i - tk * nf4)] = z;
+        }
+    }
     const int rowvec = vend - vbeg;
     const int total = ntok * rowvec;
     const uint4 *xs = reinterpret_cast<const uint4 *>(x + (size_t)first * row_bytes);
@@ -209,7 +221,7 @@ cudaError_t launch_chunk_scan(const int *idx, int T, int k, int E, int capacity,
 cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int *offsets,
                                 const void *x, const float *row_scale, int T, int d, int E, int k,
                                 int capacity, int elt, int *perm, int *inv, void *x_perm,
-                                cudaStream_t s) {
+                                cudaStream_t s, float *zero_acc) {
     if (T == 0) return cudaSuccess;
     const int nchunks = (T + kChunk - 1) / kChunk;
     // few chunks (small batches): split each chunk's row copy over several
@@ -226,10 +238,11 @@ cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int
         return launch_pdl(group_tokens_kernel<2>, dim3(nchunks, parts), 256, 0, s, idx,
                           chunk_base, offsets, static_cast<const uint8_t *>(x), row_scale, elt, T,
                           E, k, capacity, (size_t)d * elt, perm, inv,
-                          static_cast<uint8_t *>(x_perm));
+                          static_cast<uint8_t *>(x_perm), zero_acc);
     return launch_pdl(group_tokens_kernel<MOE_MAX_TOPK>, dim3(nchunks, parts), 256, 0, s, idx,
                       chunk_base, offsets, static_cast<const uint8_t *>(x), row_scale, elt, T, E,
-                      k, capacity, (size_t)d * elt, perm, inv, static_cast<uint8_t *>(x_perm));
+                      k, capacity, (size_t)d * elt, perm, inv, static_cast<uint8_t *>(x_perm),
+                      zero_acc);
 }
 
 cudaError_t launch_permute(const void *x, const int *perm, int rows, int d, int k, int elt,

@@ -63,6 +63,16 @@ _sig("moe_forward_static_scratch", _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i,
 STATIC_SCRATCH_BYTES = 16 << 20
 
 
+class GraphStats(ctypes.Structure):
+    """moe_graph_stats: the launch-graph cache's counters."""
+    _fields_ = [("entries", ctypes.c_longlong), ("replays", ctypes.c_longlong),
+                ("captures", ctypes.c_longlong), ("direct_calls", ctypes.c_longlong),
+                ("evictions", ctypes.c_longlong)]
+
+
+_sig("moe_graph_cache_stats", _i, _P(GraphStats), _i)
+
+
 class Options(ctypes.Structure):
     """moe_options: gating (0 softmax over kept, 1 full softmax then top-k),
     capacity (rows per expert, 0 = no limit), drop_policy (0 lose, 1
@@ -93,6 +103,7 @@ EXPORTED = [
     "moe_add_rmsnorm", "moe_device_status", "moe_selftest_wait_timeout", "moe_forward_launches",
     "moe_forward_static_scratch", "moe_forward_ex", "moe_capacity", "moe_route_from_logits_ex",
     "moe_block_forward", "moe_backward_workspace_bytes", "moe_backward",
+    "moe_graph_cache_stats",
 ]
 
 
@@ -113,6 +124,14 @@ def _check(code, where):
 
 def lib():
     return _lib
+
+
+def graph_cache_stats(reset=False) -> dict:
+    """The launch-graph cache's counters (moe_graph_cache_stats)."""
+    st = GraphStats()
+    _check(_lib.moe_graph_cache_stats(ctypes.byref(st), int(bool(reset))),
+           "moe_graph_cache_stats")
+    return {name: getattr(st, name) for name, _ in GraphStats._fields_}
 
 
 def _dt(t: torch.Tensor) -> int:

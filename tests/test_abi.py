@@ -229,3 +229,13 @@ def test_static_scratch_limit_stated_in_header():
             for T in range(1, 200)]
     assert all(fits[:81]) and not fits[81]
     assert any(fits[82:])
+
+
+def test_graph_cache_stats_without_device_work():
+    """The cache counters are readable with no GPU work (all zero before any
+    forward call in this process); a null pointer is an argument error."""
+    from sparse_mixture_experts_58_b300 import moe
+    st = moe.graph_cache_stats()
+    assert set(st) == {"entries", "replays", "captures", "direct_calls", "evictions"}
+    assert all(v >= 0 for v in st.values())
+    assert moe.lib().moe_graph_cache_stats(None, 0) == moe.ERR_ARG

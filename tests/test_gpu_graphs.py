@@ -166,3 +166,42 @@ def test_call_inside_a_caller_capture(moe):
         ref = moe.forward(xi, layer.Wg, layer.W1, layer.W3, layer.W2, k)
         torch.cuda.synchronize()
         assert torch.equal(got, ref)
+
+
+def test_graph_cache_counts_and_evicts_least_recent(moe, monkeypatch):
+    """The cache's counters: first call direct, second a capture, then
+    replays; more than 64 argument sets evict the least recently used one,
+    whose next call starts over (direct), with the same bits as before."""
+    monkeypatch.setenv("MOE_GRAPHS", "1")
+    T, d, ffn, E, k = 8, 128, 256, 8, 2
+    x, layer = inputs.make_workload(T, d, ffn, E, k, "bf16", seed=41, device="cuda")
+    ws = moe.Workspace(x.device)
+    outs = [torch.empty_like(x) for _ in range(70)]   # one argument set per output buffer
+    moe.graph_cache_stats(reset=True)
+
+    def call(i):
+        return moe.forward(x, layer.Wg, layer.W1, layer.W3, layer.W2, k, out=outs[i],
+                           workspace=ws)
+
+    call(0)
+    call(0)
+    call(0)
+    torch.cuda.synchronize()
+    st = moe.graph_cache_stats()
+    assert (st["direct_calls"], st["captures"], st["replays"]) == (1, 1, 1)
+    ref = outs[0].clone()
+    for i in range(1, 70):
+        call(i)
+    torch.cuda.synchronize()
+    st = moe.graph_cache_stats()
+    assert st["entries"] == 64
+    assert st["evictions"] >= 6
+    # set 0 was the least recently used: gone, so it runs directly again
+    before = st["direct_calls"]
+    outs[0].zero_()
+    call(0)
+    torch.cuda.synchronize()
+    assert moe.graph_cache_stats()["direct_calls"] == before + 1
+    assert torch.equal(outs[0].view(torch.int16), ref.view(torch.int16))
+    for i in range(70):
+        assert torch.equal(outs[i].view(torch.int16), ref.view(torch.int16))

@@ -344,3 +344,37 @@ def test_sweep_blocks_mixtral_shape(moe):
     assert moe.device_status(clear=True) == 0
     for T, (g, r) in worst.items():
         print(f"PARITY sweep T={T} worst: gated {g:.3e} raw {r:.3e}")
+
+
+@pytest.mark.parametrize("fuse", ["0", "1"], ids=["combine_pass", "combine_in_down"])
+@pytest.mark.parametrize("T,d,ffn,E,k,gating", [
+    (700, 192, 384, 8, 2, 0),
+    (2300, 192, 320, 8, 2, 0),     # several token tiles per expert, ragged features
+    (1500, 128, 192, 4, 1, 0),     # one slot per token
+    (900, 256, 256, 8, 2, 1),      # gates from the full softmax (not renormalised)
+])
+def test_combine_in_down_epilogue(moe, monkeypatch, fuse, T, d, ffn, E, k, gating):
+    """The CTA-pair down projection with the gated combine in its epilogue
+    (fp32 additions of gate x output into a zeroed row per token, then one
+    rounding) against the separate combine pass: both against the oracle,
+    and the fused form gives the same bits on every call (at most two
+    additions into zero per element)."""
+    monkeypatch.setenv("MOE_PLAN_PAIR", "1")
+    monkeypatch.setenv("MOE_PLAN_SPLITS", "1")
+    monkeypatch.setenv("MOE_FUSE_COMBINE", fuse)
+    x, layer = inputs.make_workload(T, d, ffn, E, k, "bf16", seed=T + 3, device="cuda")
+    kw = dict(gating=gating) if gating else {}
+    out = moe.forward(x, layer.Wg, layer.W1, layer.W3, layer.W2, k, **kw)
+    out2 = moe.forward(x, layer.Wg, layer.W1, layer.W3, layer.W2, k, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    o = oracle.load()
+    Wg, W1, W3, W2, bias = inputs.layer_to_host(layer)
+    _, rl, _, _, exact = o.moe_forward(inputs.to_host(x), Wg, W1, W3, W2, k, exact=True,
+                                       gating=gating)
+    keep = ~helpers.near_tie_mask(rl, k)
+    got = inputs.to_host(out)
+    err = helpers.rel_error(got[keep], exact[keep], "bf16")
+    print(f"PARITY combine fuse={fuse} T{T} k{k} gating{gating}: gated {err:.3e} raw "
+          f"{helpers.raw_rel_error(got[keep], exact[keep]):.3e} over {keep.sum()} tokens")
+    assert err <= helpers.TOL_BF16
