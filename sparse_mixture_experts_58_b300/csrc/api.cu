@@ -165,8 +165,7 @@ int encode_map_bf16_2d(CUtensorMap *map, const void *base, unsigned long long in
 
 namespace {
 
-int encode_uncached(CUtensorMap *map, const void *base, unsigned long long inner,
-                    unsigned long long outer, unsigned int box_inner, unsigned int box_outer) {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -177,6 +176,37 @@ int encode_uncached(CUtensorMap *map, const void *base, unsigned long long inner
             q == cudaDriverEntryPointSuccess)
             encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     });
+    return encode;
+}
+
+struct GateUpKey {
+    const void *w1, *w3;
+    int d, ffn;
+    bool operator==(const GateUpKey &o) const {
+        return w1 == o.w1 && w3 == o.w3 && d == o.d && ffn == o.ffn;
+    }
+};
+
+struct GateUpKeyHash {
+    size_t operator()(const GateUpKey &k) const {
+        size_t h = std::hash<const void *>()(k.w1);
+        h ^= std::hash<const void *>()(k.w3) + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+        h ^= std::hash<long long>()(((long long)k.d << 32) | (unsigned)k.ffn) +
+             0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+        return h;
+    }
+};
+
+struct GateUpMap {
+    CUtensorMap map;
+    int swapped;
+};
+
+std::unordered_map<GateUpKey, GateUpMap, GateUpKeyHash> g_gate_up_cache;
+
+int encode_uncached(CUtensorMap *map, const void *base, unsigned long long inner,
+                    unsigned long long outer, unsigned int box_inner, unsigned int box_outer) {
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (encode == nullptr) return MOE_ERR_CUDA;
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {inner * 2};
@@ -190,6 +220,55 @@ int encode_uncached(CUtensorMap *map, const void *base, unsigned long long inner
 }
 
 }  // namespace
+
+// W1[e] and W3[e] ([ffn][d] each) as one 4-D tensor: dims (d, 16 rows, 2
+// matrices, ffn / 16 row groups), strides (2 d bytes, the distance from the
+// lower of the two matrices to the higher, 32 d bytes).  A box {64, 16, 2, 4}
+// lands in shared memory as four groups of [16 rows of one matrix, the same
+// 16 rows of the other]: 128 rows whose gate and up values of a feature sit
+// 16 rows apart.  *swapped = 1 when W3[e] lies below W1[e] (the box then puts
+// W3's rows first).  Returns MOE_ERR_UNSUPPORTED when the driver refuses the
+// layout (the caller falls back to two separate boxes).
+int encode_map_gate_up(CUtensorMap *map, const void *W1e, const void *W3e, int d, int ffn,
+                       int *swapped) {
+    const GateUpKey key{W1e, W3e, d, ffn};
+    {
+        std::lock_guard<std::mutex> g(g_map_mutex);
+        auto it = g_gate_up_cache.find(key);
+        if (it != g_gate_up_cache.end()) {
+            *map = it->second.map;
+            *swapped = it->second.swapped;
+            return MOE_OK;
+        }
+    }
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (encode == nullptr) return MOE_ERR_CUDA;
+    if (ffn % 64 != 0 || W1e == W3e) return MOE_ERR_UNSUPPORTED;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(W1e), b = reinterpret_cast<uintptr_t>(W3e);
+    const int sw = b < a ? 1 : 0;
+    const uintptr_t lo = sw ? b : a, hi = sw ? a : b;
+    const unsigned long long gap = static_cast<unsigned long long>(hi - lo);
+    if (gap % 16 != 0 || gap >= (1ull << 40)) return MOE_ERR_UNSUPPORTED;
+    const cuuint64_t dims[4] = {(cuuint64_t)d, 16, 2, (cuuint64_t)(ffn / 16)};
+    const cuuint64_t strides[3] = {(cuuint64_t)d * 2, gap, (cuuint64_t)d * 2 * 16};
+    const cuuint32_t box[4] = {64, 16, 2, 4};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUtensorMap m;
+    const CUresult r = encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                              reinterpret_cast<void *>(lo), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return MOE_ERR_UNSUPPORTED;
+    {
+        std::lock_guard<std::mutex> g(g_map_mutex);
+        if (g_gate_up_cache.size() >= kMapCacheMax) g_gate_up_cache.clear();
+        g_gate_up_cache.emplace(key, GateUpMap{m, sw});
+    }
+    *map = m;
+    *swapped = sw;
+    return MOE_OK;
+}
 
 // Tile plan.  Rows per expert decide the kernel: with 128 or more on average
 // (prefill) the CTA-pair kernel (256 weight rows x token tiles of up to 256
@@ -313,6 +392,18 @@ int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p) {
             q.fuse = q.fuse && atoi(fc) != 0;
     }
     const int elt = elem_size(dt);
+    // Small batches are grouped by one kernel (counts, scan, ranks and the row
+    // copies in one block) instead of two: up to 512 KB of rows to copy (32
+    // tokens at hidden 4096 in bf16, top-2), none of them accumulated by the
+    // down projection's epilogue (which needs its rows zeroed by the
+    // grouping pass).  MOE_ROUTE_SMALL=0|1 forces it where it applies
+    // (measurement only).
+    {
+        const bool fits = (long long)q.rows <= route_small_max();
+        q.small_route = fits && (long long)q.rows * d * elt <= (512LL << 10) && !q.fuse;
+        if (const char *rs = getenv("MOE_ROUTE_SMALL"))
+            q.small_route = fits && !q.fuse && atoi(rs) != 0;
+    }
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;
@@ -395,13 +486,19 @@ int run_forward(const Plan &P, const Options &O, const void *x, const void *W_g,
     if ((rc = cuda_rc(launch_router(x, W_g, bias, P.T, P.d, P.E, P.k, P.dt, O.gating, eps, inv_rms,
                                     logits, idx, gates, s))) != MOE_OK)
         return rc;
-    if ((rc = cuda_rc(launch_chunk_scan(idx, P.T, P.k, P.E, O.capacity, cc, cb, counts, offsets,
-                                        s))) != MOE_OK)
-        return rc;
-    if ((rc = cuda_rc(launch_group_tokens(idx, cb, offsets, x, inv_rms, P.T, P.d, P.E, P.k,
-                                          O.capacity, elt, perm, inv, x_perm, s,
-                                          fuse ? y : nullptr))) != MOE_OK)
-        return rc;
+    if (P.small_route) {
+        if ((rc = cuda_rc(launch_route_small(idx, P.T, P.k, P.E, O.capacity, x, inv_rms, P.d, elt,
+                                             counts, offsets, perm, inv, x_perm, s))) != MOE_OK)
+            return rc;
+    } else {
+        if ((rc = cuda_rc(launch_chunk_scan(idx, P.T, P.k, P.E, O.capacity, cc, cb, counts,
+                                            offsets, s))) != MOE_OK)
+            return rc;
+        if ((rc = cuda_rc(launch_group_tokens(idx, cb, offsets, x, inv_rms, P.T, P.d, P.E, P.k,
+                                              O.capacity, elt, perm, inv, x_perm, s,
+                                              fuse ? y : nullptr))) != MOE_OK)
+            return rc;
+    }
     if (P.dt == MOE_BF16) {
         if (P.pair) {
             if ((rc = launch_swiglu_pair(x_perm, offsets, W1, W3, P.rows, P.d, P.ffn, P.E, h,
@@ -569,7 +666,8 @@ class LaunchKey {
     }
     LaunchKey &plan(const Plan &P) {
         return add(P.T).add(P.d).add(P.ffn).add(P.E).add(P.k).add(P.dt).add(P.rows).add(P.wide)
-            .add(P.pair).add(P.bm).add(P.splits).add(P.kps).add(P.fuse).add(P.bytes);
+            .add(P.pair).add(P.bm).add(P.splits).add(P.kps).add(P.fuse).add(P.small_route)
+            .add(P.bytes);
     }
     LaunchKey &opts(const Options &O) { return add(O.gating).add(O.capacity).add(O.renorm); }
     const std::string &str() const { return s_; }
@@ -822,7 +920,9 @@ int moe_forward_launches(int T, int d, int ffn, int E, int k, int dtype, int *la
     Plan P;
     const int rc = make_plan(T, d, ffn, E, k, dtype, &P);
     if (rc != MOE_OK) return rc;
-    *launches = T == 0 ? 0 : 6;  // router, scan, group, gate/up, down, combine
+    // router, scan + group (one kernel for small batches), gate/up, down,
+    // combine (or the finalize of the combine folded into the down projection)
+    *launches = T == 0 ? 0 : (P.small_route ? 5 : 6);
     return MOE_OK;
 }
 

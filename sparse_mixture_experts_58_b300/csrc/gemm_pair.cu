@@ -48,20 +48,31 @@ constexpr int kHalfM = 128;        // weight rows per CTA
 constexpr int kMaxTok = 256;       // token rows per tile (MMA N)
 constexpr int kTokMaps = kMaxTok / 16;  // token tensor maps, box heights 8, 16, ..., 128
 constexpr int kGate = kHalfM / 2;  // gate/up: W1 rows, then the same rows of W3, per CTA
-constexpr int kStages = 6;
 constexpr int kMaxE = MOE_MAX_EXPERTS;
 constexpr int kEpiWarps = 8;  // two per tensor-memory lane quarter
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kABytes = kHalfM * 128;       // weights, 64-wide contraction slice
 constexpr int kBBytes = (kMaxTok / 2) * 128;  // tokens, this CTA's half
-constexpr int kRing = kStages * (kABytes + kBBytes);
-// gate/up exchange: [warp pair 4][chunk parity 2][direction 2][16 tokens][32 lanes] fp32
+// gate/up exchange (two-box layout): [warp pair 4][chunk parity 2][direction 2]
+// [16 tokens][32 lanes] fp32
 constexpr int kXchPairs = kEpiWarps / 2;
 constexpr int kXchFloats = 16 * 32;
 constexpr int kXch = kXchPairs * 2 * 2 * kXchFloats * 4;
-constexpr int kBars = (2 * kStages + 6 + kXchPairs) * 8;
 constexpr int kMisc = 16 + 4 * (4 * kMaxE + 2);
-constexpr size_t kSmem = 1024 + kRing + kXch + kBars + kMisc;
+
+// Shared memory of one instantiation.  Gate/up with the two-box weight layout
+// needs the 32 KB exchange and keeps six ring stages; the interleaved layout
+// (IL) and the down projection need no exchange and take a seventh stage.
+template <bool SWIGLU, bool IL>
+struct PairCfg {
+    static constexpr bool kXchOn = SWIGLU && !IL;
+    static constexpr int kStages = kXchOn ? 6 : 7;
+    static constexpr int kRing = kStages * (kABytes + kBBytes);
+    static constexpr int kXchBytes = kXchOn ? kXch : 0;
+    static constexpr int kBars = (2 * kStages + 6 + (kXchOn ? kXchPairs : 0)) * 8;
+    static constexpr size_t kSmem = 1024 + kRing + kXchBytes + kBars + kMisc;
+    static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
+};
 constexpr uint32_t kAccCols = kMaxTok;
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr int kAccEmptyArrivals = 2 * kEpiWarps;  // lane 0 of each epilogue warp, both CTAs
@@ -81,7 +92,9 @@ struct PairArgs {
     int E, rows, K, N, kblocks, kps, splits;
     int k;        // combine: experts per token
     int combine;  // down only: add gate x output into acc[token] (one split)
-    int hints;    // L2 policy of the copies: bit 0 weights evict-first, bit 1 tokens evict-last
+    // interleaved gate/up: mapW0[e] is the 4-D map of W1[e] and W3[e] (box
+    // {64, 16, 2, 4}); bit e set when W3[e]'s rows come first in each group
+    unsigned long long swap_mask;
 };
 
 struct PairUnit {
@@ -94,7 +107,9 @@ struct PairUnit {
 };
 
 // Units are ordered expert -> feature tile -> split -> token tile, so the
-// pairs running together share one weight tile through L2.
+// pairs running together share one weight tile through L2.  (Feature tile
+// first, spreading the pairs running together over the experts, measured
+// 1-10% slower at T = 512 .. 4096.)
 __device__ __forceinline__ PairUnit decode_pair_unit(int u, const int *s_off, const int *s_ntt,
                                                      const int *s_nt, const int *s_ustart,
                                                      const PairArgs &a, int NOUT) {
@@ -124,10 +139,13 @@ __device__ __forceinline__ PairUnit decode_pair_unit(int u, const int *s_off, co
     return w;
 }
 
-template <bool SWIGLU>
+template <bool SWIGLU, bool IL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_pair(const __grid_constant__ PairArgs a) {
     constexpr int NOUT = SWIGLU ? kPairM / 2 : kPairM;  // output features per pair tile
+    using C = PairCfg<SWIGLU, IL>;
+    constexpr int kStages = C::kStages;
+    constexpr int kRing = C::kRing;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -135,14 +153,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t *sA = smem;
     uint8_t *sB = smem + kStages * kABytes;
     float *xch = reinterpret_cast<float *>(smem + kRing);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRing + kXch);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRing + C::kXchBytes);
     uint64_t *empty = full + kStages;
     uint64_t *acc_full = empty + kStages;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *drain = acc_empty + 2;
     uint64_t *bye = drain + 1;
-    uint64_t *xbar = bye + 1;  // [kXchPairs] gate/up exchange, one per epilogue warp pair
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xbar + kXchPairs);
+    uint64_t *xbar = bye + 1;  // [kXchPairs] gate/up exchange (two-box layout)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xbar + (C::kXchOn ? kXchPairs : 0));
     volatile int *s_abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *s_bye_ok = reinterpret_cast<volatile int *>(tmem_slot + 2);
     int *s_off = reinterpret_cast<int *>(tmem_slot + 4);  // [kMaxE + 1]
@@ -167,7 +185,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         ptx::mbar_init(drain, 1);
         ptx::mbar_init(bye, 1);
-        for (int i = 0; i < kXchPairs; ++i) ptx::mbar_init(&xbar[i], 2);
+        if (C::kXchOn)
+            for (int i = 0; i < kXchPairs; ++i) ptx::mbar_init(&xbar[i], 2);
         *s_abort = 0;
         *s_bye_ok = 0;
         ptx::fence_barrier_init();
@@ -214,9 +233,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ producers
         if (lane == 0) {
             const uint32_t full0 = ptx::map_to_rank(ptx::smem_addr(&full[0]), 0);
-            const uint64_t pol_w = ptx::policy_evict_first();
-            const uint64_t pol_t = ptx::policy_evict_last();
-            const bool hint_w = (a.hints & 1) != 0, hint_t = (a.hints & 2) != 0;
             int stage = 0;
             uint32_t ph = 0;
             int issued = 0;
@@ -238,20 +254,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t fb = full0 + static_cast<uint32_t>(stage) * 8u;
                     uint8_t *dA = sA + stage * kABytes;
                     const int kx = kb * kBlockK;
-                    if (hint_w) {
-                        ptx::tma_load_2d_pair_hint(dA, &a.mapW0[w.e], kx, wrow, fb, pol_w);
-                        if (SWIGLU)
-                            ptx::tma_load_2d_pair_hint(dA + kGate * 128, &a.mapW1[w.e], kx, wrow,
-                                                       fb, pol_w);
+                    if (IL) {
+                        // 128 rows: four groups of 16 gate and the same 16 up rows
+                        ptx::tma_load_4d_pair(dA, &a.mapW0[w.e], kx, 0, 0, wrow / 16, fb);
                     } else {
                         ptx::tma_load_2d_pair(dA, &a.mapW0[w.e], kx, wrow, fb);
                         if (SWIGLU)
                             ptx::tma_load_2d_pair(dA + kGate * 128, &a.mapW1[w.e], kx, wrow, fb);
                     }
-                    if (hint_t)
-                        ptx::tma_load_2d_pair_hint(sB + stage * kBBytes, mt, kx, trow, fb, pol_t);
-                    else
-                        ptx::tma_load_2d_pair(sB + stage * kBBytes, mt, kx, trow, fb);
+                    ptx::tma_load_2d_pair(sB + stage * kBBytes, mt, kx, trow, fb);
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;
@@ -345,7 +356,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after_sync();
             const uint32_t tb = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                 static_cast<uint32_t>(acc) * kAccCols;
-            if (SWIGLU) {
+            if (IL) {
+                // interleaved rows: lanes 0-15 of this quarter hold one
+                // matrix's values of features 16 quad .. +15, lanes 16-31 the
+                // other's of the same features; lane pairs (l, l + 16) swap
+                // half of each 32-token chunk by shuffle and each finishes
+                // silu(u) * v for 16 tokens
+                const bool upper = lane >= 16;
+                const bool is_gate = upper == (((a.swap_mask >> w.e) & 1ull) != 0);
+                const int f = w.n0 + static_cast<int>(rank) * kGate + quad * 16 + (lane & 15);
+                __nv_bfloat16 *hcol = static_cast<__nv_bfloat16 *>(a.out) + f;
+                const bool f_ok = f < a.N;
+#pragma unroll 1
+                for (int j0 = 32 * cset; j0 < w.ntok; j0 += 64) {
+                    uint32_t V[32];
+                    ptx::tmem_ld_32x32b_x32(tb + static_cast<uint32_t>(j0), V);
+                    ptx::tmem_ld_wait();
+                    // the gate lane keeps tokens 0-15 of the chunk, the up lane 16-31
+                    const int jb = j0 + (is_gate ? 0 : 16);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float send = __uint_as_float(is_gate ? V[16 + i] : V[i]);
+                        const float other = __shfl_xor_sync(0xffffffffu, send, 16);
+                        const float g = is_gate ? __uint_as_float(V[i]) : other;
+                        const float v = is_gate ? other : __uint_as_float(V[16 + i]);
+                        const int j = jb + i;
+                        if (f_ok && j < w.nvalid)
+                            hcol[(size_t)(w.t0 + j) * a.N] =
+                                __float2bfloat16_rn(g / (1.f + expf(-g)) * v);
+                    }
+                }
+            } else if (SWIGLU) {
                 // the gate warp finishes each chunk's first 16 tokens, the up
                 // warp the last 16; each sends the other the values it needs
                 const int f = w.n0 + static_cast<int>(rank) * kGate + (quad & 1) * 32 + lane;
@@ -453,9 +494,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 std::mutex g_pair_mutex;
 
-template <bool SWIGLU>
+template <bool SWIGLU, bool IL = false>
 int run_pair(PairArgs &args, int units_bound, cudaStream_t s) {
-    auto kernel = grouped_gemm_pair<SWIGLU>;
+    auto kernel = grouped_gemm_pair<SWIGLU, IL>;
+    constexpr size_t kSmem = PairCfg<SWIGLU, IL>::kSmem;
     static bool attr_set[64];
     static int max_pairs[64];
     int dev = 0;
@@ -494,9 +536,7 @@ int fill_pair(PairArgs &args, const void *tokens, const int *offsets, void *out,
     args.gates = nullptr;
     args.k = 1;
     args.combine = 0;
-    // MOE_PAIR_HINTS (measurement only): bit 0 weights evict-first, bit 1 tokens evict-last
-    args.hints = 0;
-    if (const char *h = getenv("MOE_PAIR_HINTS")) args.hints = atoi(h) & 3;
+    args.swap_mask = 0;
     args.E = E;
     args.rows = rows;
     args.K = K;
@@ -517,7 +557,11 @@ int token_tiles_bound(int rows, int E) { return (rows + kMaxTok - 1) / kMaxTok +
 
 }  // namespace
 
-size_t pair_gemm_smem_bytes() { return kSmem; }
+size_t pair_gemm_smem_bytes() {
+    return PairCfg<true, false>::kSmem > PairCfg<false, false>::kSmem
+               ? PairCfg<true, false>::kSmem
+               : PairCfg<false, false>::kSmem;
+}
 
 int launch_swiglu_pair(const void *x_perm, const int *offsets, const void *const *W1,
                        const void *const *W3, int rows, int d, int ffn, int E, void *h,
@@ -526,16 +570,30 @@ int launch_swiglu_pair(const void *x_perm, const int *offsets, const void *const
     PairArgs args;
     int rc = fill_pair(args, x_perm, offsets, h, rows, d, ffn, E);
     if (rc != MOE_OK) return rc;
+    args.splits = 1;
+    args.kps = args.kblocks;
+    const int NT = (ffn + kPairM / 2 - 1) / (kPairM / 2);
+    // W1[e] and W3[e] interleaved by one 4-D map per expert (seven stages, no
+    // exchange buffer), unless the driver refuses that layout for some
+    // expert; MOE_PAIR_IL=0 forces the two-box layout (measurement only)
+    bool il = true;
+    if (const char *v = getenv("MOE_PAIR_IL")) il = atoi(v) != 0;
+    for (int e = 0; il && e < E; ++e) {
+        int sw = 0;
+        rc = encode_map_gate_up(&args.mapW0[e], W1[e], W3[e], d, ffn, &sw);
+        if (rc == MOE_ERR_UNSUPPORTED) il = false;
+        else if (rc != MOE_OK) return rc;
+        if (sw) args.swap_mask |= 1ull << e;
+    }
+    if (il) return run_pair<true, true>(args, token_tiles_bound(rows, E) * NT, s);
+    args.swap_mask = 0;
     for (int e = 0; e < E; ++e) {
         if ((rc = encode_map_bf16_2d(&args.mapW0[e], W1[e], d, ffn, kBlockK, kGate)) != MOE_OK)
             return rc;
         if ((rc = encode_map_bf16_2d(&args.mapW1[e], W3[e], d, ffn, kBlockK, kGate)) != MOE_OK)
             return rc;
     }
-    args.splits = 1;
-    args.kps = args.kblocks;
-    const int NT = (ffn + kPairM / 2 - 1) / (kPairM / 2);
-    return run_pair<true>(args, token_tiles_bound(rows, E) * NT, s);
+    return run_pair<true, false>(args, token_tiles_bound(rows, E) * NT, s);
 }
 
 int launch_down_pair(const void *h, const int *offsets, const void *const *W2, int rows, int d,

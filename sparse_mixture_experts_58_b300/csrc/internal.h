@@ -24,6 +24,7 @@ struct Plan {
     int bm;        // token rows per tile (<= 128)
     int splits;    // split of the down projection's contraction
     int kps;       // 64-wide contraction blocks per split
+    int small_route;  // 1: one kernel groups the batch (scan, ranks, row copies)
     int fuse;      // 1: the down projection's epilogue adds gate x output into
                    // a zeroed fp32 row per token (the combine), a finalize
                    // pass rounds it; needs k <= 2, one split, the pair kernel
@@ -86,12 +87,19 @@ cudaError_t launch_chunk_scan(const int *idx, int T, int k, int E, int capacity,
                               int *chunk_base, int *counts, int *offsets, cudaStream_t s,
                               int pad = 1);
 // row_scale != nullptr: each copied row is multiplied by its token's scale
-// and rounded to the storage type (the fused RMSNorm).  zero_acc != nullptr:
-// the chunk's rows of the fp32 [T][d] accumulator are set to zero.
+// and rounded to the storage type (the fused RMSNorm).  zero_acc != nullptr: the chunk's
+// rows of the fp32 [T][d] accumulator are set to zero.
 cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int *offsets,
                                 const void *x, const float *row_scale, int T, int d, int E, int k,
                                 int capacity, int elt, int *perm, int *inv, void *x_perm,
                                 cudaStream_t s, float *zero_acc = nullptr);
+// The grouping of a batch of at most route_small_max() selections (T * k) in
+// one kernel: counts, offsets, perm, inv and the row copies (row_scale: the
+// fused RMSNorm), as chunk_scan + group_tokens give them.
+int route_small_max();
+cudaError_t launch_route_small(const int *idx, int T, int k, int E, int capacity, const void *x,
+                               const float *row_scale, int d, int elt, int *counts, int *offsets,
+                               int *perm, int *inv, void *x_perm, cudaStream_t s);
 // x_perm[r] = x[perm[r] / k] for r < rows.
 cudaError_t launch_permute(const void *x, const int *perm, int rows, int d, int k, int elt,
                            void *x_perm, cudaStream_t s);
@@ -175,5 +183,9 @@ cudaError_t launch_wait_selftest(unsigned int limit_ns, cudaStream_t s);
 int encode_map_bf16_2d(CUtensorMap *map, const void *base, unsigned long long inner,
                        unsigned long long outer, unsigned int box_inner,
                        unsigned int box_outer);
+// W1[e] and W3[e] as one 4-D tensor whose box {64, 16, 2, 4} interleaves them
+// in 16-row groups (see api.cu); MOE_ERR_UNSUPPORTED if the driver refuses it.
+int encode_map_gate_up(CUtensorMap *map, const void *W1e, const void *W3e, int d, int ffn,
+                       int *swapped);
 
 }  // namespace moe

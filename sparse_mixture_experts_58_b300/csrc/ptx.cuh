@@ -288,15 +288,15 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m
         : "memory");
 }
 
-// The same with an L2 cache-policy hint (from createpolicy).
-__device__ __forceinline__ void tma_load_2d_pair_hint(void *dst, const CUtensorMap *map, int c0,
-                                                      int c1, uint32_t bar_cluster_addr,
-                                                      uint64_t policy) {
+// 4-D tiled load into this CTA's shared memory, completion on a barrier of
+// either CTA of the pair (cluster address); c0 innermost.
+__device__ __forceinline__ void tma_load_4d_pair(void *dst, const CUtensorMap *map, int c0, int c1,
+                                                 int c2, int c3, uint32_t bar_cluster_addr) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
-        "bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster_addr),
-        "l"(policy)
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+        "bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "r"(bar_cluster_addr)
         : "memory");
 }
 

@@ -76,6 +76,119 @@ __global__ void __launch_bounds__(1024) chunk_scan_kernel(const int *__restrict_
     }
 }
 
+// The whole grouping of a small batch (n = T * k <= kRouteSmallMax
+// selections) in one block: counts, offsets, perm, inv and the row copies,
+// in place of chunk_scan + group_tokens.  Selections are taken in order
+// s = t * k + j, in chunks of 32 (one per warp at a time).  Per chunk, the
+// lanes that hold the same expert find each other (match), the lowest of them
+// records the chunk's count for that expert; a scan over chunks per expert
+// gives each chunk's base; a selection's rank is its chunk's base plus the
+// matching lanes below it, so the row order is (expert, token) as in the two
+// kernels, and the results are the same.  Then the whole block copies the
+// kept rows (row_scale: scaled and rounded, the fused RMSNorm).
+constexpr int kRouteSmallMax = 1024;
+constexpr int kRouteSmallChunks = kRouteSmallMax / 32;
+
+template <typename T>
+__global__ void __launch_bounds__(1024) route_small_kernel(
+    const int *__restrict__ idx, int n, int k, int E, int capacity, const T *__restrict__ x,
+    const float *__restrict__ row_scale, int d, int *counts, int *offsets, int *perm, int *inv,
+    T *x_perm) {
+    __shared__ int s_sel[kRouteSmallMax];
+    __shared__ int s_src[kRouteSmallMax];  // row -> source token
+    __shared__ uint8_t s_cnt[kRouteSmallChunks][MOE_MAX_EXPERTS];
+    __shared__ uint16_t s_base[kRouteSmallChunks][MOE_MAX_EXPERTS];
+    __shared__ int s_tot[MOE_MAX_EXPERTS];
+    __shared__ int s_off[MOE_MAX_EXPERTS + 1];
+    pdl_wait();
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+    const int nch = (n + 31) / 32;
+    for (int i = threadIdx.x; i < nch * MOE_MAX_EXPERTS; i += blockDim.x)
+        s_cnt[i / MOE_MAX_EXPERTS][i % MOE_MAX_EXPERTS] = 0;
+    __syncthreads();
+    for (int c = warp; c < nch; c += nwarps) {
+        const int s0 = 32 * c + lane;
+        const int sel = s0 < n ? idx[s0] : -1;
+        s_sel[s0] = sel;
+        const unsigned m = __match_any_sync(0xffffffffu, sel);
+        if (sel >= 0 && (m & ((1u << lane) - 1u)) == 0) s_cnt[c][sel] = (uint8_t)__popc(m);
+    }
+    __syncthreads();
+    for (int e = warp; e < E; e += nwarps) {
+        int carry = 0;
+        for (int base = 0; base < nch; base += 32) {
+            const int c = base + lane;
+            const int v = c < nch ? s_cnt[c][e] : 0;
+            int sc = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, sc, off);
+                if (lane >= off) sc += t;
+            }
+            if (c < nch) s_base[c][e] = (uint16_t)(carry + sc - v);
+            carry += __shfl_sync(0xffffffffu, sc, 31);
+        }
+        if (lane == 0) s_tot[e] = capacity > 0 ? min(carry, capacity) : carry;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int acc = 0;
+        s_off[0] = 0;
+        for (int e = 0; e < E; ++e) {
+            counts[e] = s_tot[e];
+            acc += s_tot[e];
+            s_off[e + 1] = acc;
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) offsets[i] = s_off[i];
+    for (int c = warp; c < nch; c += nwarps) {
+        const int s0 = 32 * c + lane;
+        const int sel = s_sel[s0];
+        const unsigned m = __match_any_sync(0xffffffffu, sel);
+        if (sel >= 0) {
+            const int rank = s_base[c][sel] + __popc(m & ((1u << lane) - 1u));
+            const bool kept = capacity <= 0 || rank < capacity;
+            const int r = kept ? s_off[sel] + rank : -1;
+            inv[s0] = r;
+            if (kept) {
+                perm[r] = s0;
+                s_src[r] = s0 / k;
+            }
+        }
+    }
+    __syncthreads();
+    // rows r < offsets[E]: x_perm[r] = x[source token], flattened to (row,
+    // 16-byte vector) over the block, U loads in flight per thread
+    constexpr int VN = Vec<T>::n;
+    constexpr int U = 8;
+    const int rowvec = d / VN;
+    const int total = s_off[E] * rowvec;
+    for (int i0 = threadIdx.x; i0 < total; i0 += blockDim.x * U) {
+        uint4 val[U];
+        int row[U], vec[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + blockDim.x * u;
+            const int ii = i < total ? i : 0;
+            row[u] = ii / rowvec;
+            vec[u] = ii - row[u] * rowvec;
+            val[u] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)s_src[row[u]] * d) + vec[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (i0 + (int)blockDim.x * u < total) {
+                const uint4 v = row_scale != nullptr
+                                    ? scale_slice<T>(val[u], row_scale[s_src[row[u]]])
+                                    : val[u];
+                reinterpret_cast<uint4 *>(x_perm + (size_t)row[u] * d)[vec[u]] = v;
+            }
+        }
+    }
+}
+
 // Copy one row (rowvec 16-byte vectors) from src to one destination, one
 // warp; four loads per lane are issued before their stores.
 __device__ __forceinline__ void copy_row(const uint4 *__restrict__ src, uint4 *dst, int rowvec,
@@ -243,6 +356,28 @@ cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int
                       chunk_base, offsets, static_cast<const uint8_t *>(x), row_scale, elt, T, E,
                       k, capacity, (size_t)d * elt, perm, inv, static_cast<uint8_t *>(x_perm),
                       zero_acc);
+}
+
+int route_small_max() { return kRouteSmallMax; }
+
+cudaError_t launch_route_small(const int *idx, int T, int k, int E, int capacity, const void *x,
+                               const float *row_scale, int d, int elt, int *counts, int *offsets,
+                               int *perm, int *inv, void *x_perm, cudaStream_t s) {
+    const int n = T * k;
+    if (n > kRouteSmallMax || E > MOE_MAX_EXPERTS) return cudaErrorInvalidValue;
+    // a warp per 32-selection chunk and per 2 KB of rows to copy, 4 to 32 warps
+    int warps = (n + 31) / 32;
+    const long long copy_warps = ((long long)n * d * elt + 2047) / 2048;
+    if (copy_warps > warps) warps = copy_warps > 32 ? 32 : (int)copy_warps;
+    if (warps < 4) warps = 4;
+    if (warps > 32) warps = 32;
+    if (elt == 2)
+        return launch_pdl(route_small_kernel<__nv_bfloat16>, 1, 32 * warps, 0, s, idx, n, k, E,
+                          capacity, static_cast<const __nv_bfloat16 *>(x), row_scale, d, counts,
+                          offsets, perm, inv, static_cast<__nv_bfloat16 *>(x_perm));
+    return launch_pdl(route_small_kernel<float>, 1, 32 * warps, 0, s, idx, n, k, E, capacity,
+                      static_cast<const float *>(x), row_scale, d, counts, offsets, perm, inv,
+                      static_cast<float *>(x_perm));
 }
 
 cudaError_t launch_permute(const void *x, const int *perm, int rows, int d, int k, int elt,

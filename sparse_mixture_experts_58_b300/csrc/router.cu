@@ -183,6 +183,135 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
         finish_token(s_l[threadIdx.x], bias, t0 + threadIdx.x, E, k, gating, logits, idx, gates);
 }
 
+// Router for large batches (bf16, E <= 8, d <= 2 * 256 slices of 8): a
+// persistent grid of kRouterThreads-thread blocks, each with the router matrix
+// staged once in shared memory, walking groups of kWideTB tokens; the next
+// group's rows are loaded into registers while the current one is reduced.
+// Thread i takes the same slices i, i + 256 of every row as router_kernel and
+// sums in the same order (slices, then elements, in order; the butterfly's
+// sums via warp_reduce_scatter; warps in order), so the logits -- and, with
+// NORM, the RMSNorm scales -- are the same bits as router_kernel's.
+constexpr int kWideTB = 4;
+constexpr int kWideE = 8;
+constexpr int kWideNS = 2;  // slices per thread and row (d <= 4096 in bf16)
+
+template <bool NORM>
+__global__ void __launch_bounds__(kRouterThreads, 2) router_wide_kernel(
+    const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict__ Wg,
+    const float *__restrict__ bias, int Tn, int d, int E, int k, int gating, float eps,
+    float *inv_rms, float *logits, int *idx, float *gates) {
+    constexpr int NW = kRouterThreads / 32;
+    extern __shared__ uint4 s_w[];  // [kWideE][nvec] router rows, 16-byte slices
+    __shared__ float s_part[2][NW][kWideTB][kWideE];
+    __shared__ float s_ss[2][NW][kWideTB];
+    __shared__ float s_l[2][kWideTB][MOE_MAX_EXPERTS];
+    pdl_wait();
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nvec = d / 8;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < kWideE * nvec; i += kRouterThreads) {
+        const int e = i / nvec;
+        s_w[i] = e < E ? __ldg(reinterpret_cast<const uint4 *>(Wg) + i) : zero;
+    }
+    const int ngroups = (Tn + kWideTB - 1) / kWideTB;
+    auto load_group = [&](int g, uint4 (&xs)[kWideTB][kWideNS]) {
+        const int t0 = g * kWideTB;
+#pragma unroll
+        for (int j = 0; j < kWideTB; ++j) {
+            // rows past the batch repeat its last token (results unused)
+            const uint4 *xr =
+                reinterpret_cast<const uint4 *>(x + (size_t)min(t0 + j, Tn - 1) * d);
+#pragma unroll
+            for (int sl = 0; sl < kWideNS; ++sl) {
+                const int v = threadIdx.x + kRouterThreads * sl;
+                xs[j][sl] = (g < ngroups && v < nvec) ? __ldcs(xr + v) : zero;
+            }
+        }
+    };
+    uint4 xs[kWideTB][kWideNS];
+    load_group(blockIdx.x, xs);
+    __syncthreads();
+    int buf = 0;
+    for (int g = blockIdx.x; g < ngroups; g += gridDim.x, buf ^= 1) {
+        uint4 xn[kWideTB][kWideNS];
+        load_group(g + gridDim.x, xn);
+        const int t0 = g * kWideTB;
+        const int nt = min(kWideTB, Tn - t0);
+        float sc[kWideTB];
+#pragma unroll
+        for (int j = 0; j < kWideTB; ++j) sc[j] = 1.f;
+        if (NORM) {
+            float ss[kWideTB];
+#pragma unroll
+            for (int j = 0; j < kWideTB; ++j) {
+                ss[j] = 0.f;
+#pragma unroll
+                for (int sl = 0; sl < kWideNS; ++sl)
+                    if (threadIdx.x + kRouterThreads * sl < nvec)
+                        ss[j] = slice_sumsq<__nv_bfloat16>(ss[j], xs[j][sl]);
+            }
+            const float tot = warp_reduce_scatter<kWideTB>(ss, lane);
+            if ((lane & 7) == 0) s_ss[buf][warp][lane >> 3] = tot;
+            __syncthreads();
+#pragma unroll
+            for (int j = 0; j < kWideTB; ++j) {
+                float t = 0.f;
+#pragma unroll
+                for (int w2 = 0; w2 < NW; ++w2) t += s_ss[buf][w2][j];
+                sc[j] = rms_scale(t, d, eps);
+            }
+            if ((int)threadIdx.x < nt) inv_rms[t0 + threadIdx.x] = sc[threadIdx.x];
+        }
+        float acc[kWideTB][kWideE];
+#pragma unroll
+        for (int j = 0; j < kWideTB; ++j)
+#pragma unroll
+            for (int e = 0; e < kWideE; ++e) acc[j][e] = 0.f;
+#pragma unroll
+        for (int sl = 0; sl < kWideNS; ++sl) {
+            const int v = threadIdx.x + kRouterThreads * sl;
+            if (v >= nvec) break;
+            float a[kWideTB][8];
+#pragma unroll
+            for (int j = 0; j < kWideTB; ++j)
+                Vec<__nv_bfloat16>::unpack(
+                    NORM ? scale_slice<__nv_bfloat16>(xs[j][sl], sc[j]) : xs[j][sl], a[j]);
+#pragma unroll
+            for (int e = 0; e < kWideE; ++e) {
+                float wf[8];
+                Vec<__nv_bfloat16>::unpack(s_w[e * nvec + v], wf);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int j = 0; j < kWideTB; ++j) acc[j][e] = fmaf(a[j][i], wf[i], acc[j][e]);
+            }
+        }
+        float flat[kWideTB * kWideE];
+#pragma unroll
+        for (int j = 0; j < kWideTB; ++j)
+#pragma unroll
+            for (int e = 0; e < kWideE; ++e) flat[j * kWideE + e] = acc[j][e];
+        const float sum = warp_reduce_scatter<kWideTB * kWideE>(flat, lane);
+        s_part[buf][warp][lane >> 3][lane & 7] = sum;
+        __syncthreads();
+        if (warp == 0) {
+            const int j = lane >> 3, e = lane & 7;
+            float t = s_part[buf][0][j][e];
+#pragma unroll
+            for (int w2 = 1; w2 < NW; ++w2) t += s_part[buf][w2][j][e];
+            s_l[buf][j][e] = t;
+            __syncwarp();
+            if (lane < nt)
+                finish_token(s_l[buf][lane], bias, t0 + lane, E, k, gating, logits, idx, gates);
+        }
+#pragma unroll
+        for (int j = 0; j < kWideTB; ++j)
+#pragma unroll
+            for (int sl = 0; sl < kWideNS; ++sl) xs[j][sl] = xn[j][sl];
+    }
+}
+
 // Selection from given logits: one thread per token.
 __global__ void __launch_bounds__(128) topk_kernel(const float *__restrict__ logits, int Tn, int E,
                                                    int k, int gating, int *idx, float *gates) {
@@ -248,10 +377,55 @@ cudaError_t router_dispatch_n(const void *x, const void *Wg, const float *bias, 
 #undef MOE_ROUTER
 }
 
+// The persistent large-batch router where it applies (bf16, E <= 8, d <= 4096,
+// enough tokens for two blocks per SM); MOE_ROUTER_WIDE=0|1 forces it off or
+// on where it applies (measurement only).
+template <bool NORM>
+bool router_wide(const void *x, const void *Wg, const float *bias, int T_, int d, int E, int k,
+                 int gating, float eps, float *inv_rms, float *logits, int *idx, float *gates,
+                 cudaStream_t s, cudaError_t *err) {
+    if (E > kWideE || d % 8 != 0 || d / 8 > kWideNS * kRouterThreads) return false;
+    const int ngroups = (T_ + kWideTB - 1) / kWideTB;
+    bool on = T_ >= 8 * kPlanSms;
+    if (const char *v = getenv("MOE_ROUTER_WIDE")) on = atoi(v) != 0;
+    if (!on) return false;
+    const int sms = device_sm_count();
+    const int grid = ngroups < 2 * sms ? ngroups : 2 * sms;
+    const size_t smem = (size_t)kWideE * (d / 8) * 16;
+    static bool attr_done[2][64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        *err = cudaErrorInvalidDevice;
+        return true;
+    }
+    if (!attr_done[NORM][dev]) {
+        if ((*err = cudaFuncSetAttribute(router_wide_kernel<NORM>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kWideE * 512 * 16))) != cudaSuccess)
+            return true;
+        attr_done[NORM][dev] = true;
+    }
+    *err = launch_pdl(router_wide_kernel<NORM>, grid, kRouterThreads, smem, s,
+                      static_cast<const __nv_bfloat16 *>(x),
+                      static_cast<const __nv_bfloat16 *>(Wg), bias, T_, d, E, k, gating, eps,
+                      inv_rms, logits, idx, gates);
+    return true;
+}
+
 template <typename T>
 cudaError_t router_dispatch(const void *x, const void *Wg, const float *bias, int T_, int d,
                             int E, int k, int gating, float eps, float *inv_rms, float *logits,
                             int *idx, float *gates, cudaStream_t s) {
+    if (sizeof(T) == 2) {
+        cudaError_t err = cudaSuccess;
+        const bool done =
+            inv_rms != nullptr
+                ? router_wide<true>(x, Wg, bias, T_, d, E, k, gating, eps, inv_rms, logits, idx,
+                                    gates, s, &err)
+                : router_wide<false>(x, Wg, bias, T_, d, E, k, gating, eps, inv_rms, logits, idx,
+                                     gates, s, &err);
+        if (done) return err;
+    }
     if (inv_rms != nullptr)
         return router_dispatch_n<T, true>(x, Wg, bias, T_, d, E, k, gating, eps, inv_rms, logits,
                                           idx, gates, s);

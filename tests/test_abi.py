@@ -80,7 +80,11 @@ def test_down_split_plan(moe):
     for E, k in ((4, 1), (4, 2), (16, 3), (64, 8)):
         for T in (1, 7, 16, 300):
             assert 1 <= S(T, E, k) <= 28
-    assert moe.forward_launches(16, 4096, 14336, 8, 2, moe.BF16) == 6
+    # decode batches group in one kernel (5 launches); larger ones in two
+    assert moe.forward_launches(16, 4096, 14336, 8, 2, moe.BF16) == 5
+    assert moe.forward_launches(32, 4096, 14336, 8, 2, moe.BF16) == 5
+    assert moe.forward_launches(33, 4096, 14336, 8, 2, moe.BF16) == 6
+    assert moe.forward_launches(4096, 4096, 14336, 8, 2, moe.BF16) == 6
     assert moe.forward_launches(0, 4096, 14336, 8, 2, moe.BF16) == 0
 
 

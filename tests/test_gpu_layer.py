@@ -378,3 +378,69 @@ def test_combine_in_down_epilogue(moe, monkeypatch, fuse, T, d, ffn, E, k, gatin
     print(f"PARITY combine fuse={fuse} T{T} k{k} gating{gating}: gated {err:.3e} raw "
           f"{helpers.raw_rel_error(got[keep], exact[keep]):.3e} over {keep.sum()} tokens")
     assert err <= helpers.TOL_BF16
+
+
+@pytest.mark.parametrize("T,d,ffn,E,k,dtype,cap", [
+    (1, 256, 448, 8, 2, "bf16", 0),
+    (16, 256, 448, 8, 2, "bf16", 0),
+    (37, 192, 320, 5, 2, "bf16", 0),
+    (64, 128, 256, 64, 8, "bf16", 0),     # 512 selections over 64 experts
+    (100, 64, 64, 8, 2, "bf16", 20),      # capacity: dropped selections get no row
+    (65, 128, 448, 8, 2, "f32", 0),
+    (500, 64, 64, 8, 2, "bf16", 0),       # 1000 selections: every warp several chunks
+])
+def test_small_batch_grouping_kernel_equals_two_kernels(moe, monkeypatch, T, d, ffn, E, k,
+                                                        dtype, cap):
+    """Grouping a small batch in one kernel (counts, scan over 32-selection
+    chunks, ranks from matching lanes, row copies) gives the bits of the
+    two-kernel grouping (chunk counts + scan, then ranks and copies), for
+    the layer and for the pre-norm block (rows scaled on the way)."""
+    x, layer = inputs.make_workload(T, d, ffn, E, k, dtype, seed=T + 13, device="cuda")
+    kw = dict(capacity=cap) if cap else {}
+    outs, blocks = {}, {}
+    for r in ("0", "1"):
+        monkeypatch.setenv("MOE_ROUTE_SMALL", r)
+        outs[r] = moe.forward(x, layer.Wg, layer.W1, layer.W3, layer.W2, k, **kw)
+        xb = x.clone()
+        moe.block_forward(xb, layer.Wg, layer.W1, layer.W3, layer.W2, k, **kw)
+        blocks[r] = xb
+    torch.cuda.synchronize()
+    view = torch.int16 if dtype == "bf16" else torch.int32
+    assert torch.equal(outs["0"].view(view), outs["1"].view(view))
+    assert torch.equal(blocks["0"].view(view), blocks["1"].view(view))
+    if not cap:
+        check_layer(moe, x, layer, k, dtype=dtype, label=f"small grouping T{T} E{E} k{k}")
+
+
+@pytest.mark.parametrize("order", ["w1_first", "w3_first", "mixed"])
+@pytest.mark.parametrize("T,d,ffn,E,k", [
+    (700, 192, 384, 8, 2),
+    (2300, 192, 320, 8, 2),        # ffn = 5 x 64: the last pair tile is half outside
+    (1500, 128, 192, 4, 3),
+])
+def test_interleaved_gate_up_rows_equal_two_boxes(moe, monkeypatch, order, T, d, ffn, E, k):
+    """The CTA-pair gate/up GEMM loading W1[e] and W3[e] as one 4-D box that
+    interleaves them in 16-row groups (gate and up of a feature 16 lanes
+    apart, swapped by shuffle; seven ring stages) gives the bits of the
+    two-box layout (exchange through shared memory, six stages): the same
+    rows reach the same MMAs.  W3 is placed after W1 in memory, before it,
+    or alternately per expert (the map then starts at the lower matrix)."""
+    monkeypatch.setenv("MOE_PLAN_PAIR", "1")
+    x, layer = inputs.make_workload(T, d, ffn, E, k, "bf16", seed=T + 17, device="cuda")
+    buf = torch.empty(2, E, ffn, d, dtype=torch.bfloat16, device="cuda")
+    W1, W3 = [], []
+    for e in range(E):
+        first = 0 if order == "w1_first" else 1 if order == "w3_first" else e % 2
+        buf[first, e] = layer.W1[e]
+        buf[1 - first, e] = layer.W3[e]
+        W1.append(buf[first, e])
+        W3.append(buf[1 - first, e])
+    outs = {}
+    for il in ("0", "1"):
+        monkeypatch.setenv("MOE_PAIR_IL", il)
+        outs[il] = moe.forward(x, layer.Wg, W1, W3, layer.W2, k)
+    torch.cuda.synchronize()
+    assert torch.equal(outs["0"].view(torch.int16), outs["1"].view(torch.int16))
+    ref = moe.forward(x, layer.Wg, layer.W1, layer.W3, layer.W2, k)
+    torch.cuda.synchronize()
+    assert torch.equal(ref.view(torch.int16), outs["1"].view(torch.int16))

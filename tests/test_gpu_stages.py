@@ -189,3 +189,27 @@ def test_wait_timeout_selftest(moe):
     a = torch.ones(1024, device="cuda")
     assert a.sum().item() == 1024.0
     assert moe.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("T,d,E", [(1500, 4096, 8), (4096, 4096, 8), (2500, 1024, 5),
+                                   (3001, 2048, 8)])
+def test_wide_router_same_bits(moe, monkeypatch, T, d, E):
+    """The persistent large-batch router (router rows staged in shared
+    memory, groups of four tokens) sums in router_kernel's order: the same
+    logits, choices and gates bit for bit, and the same pre-norm block
+    (the fused RMSNorm's scales included)."""
+    x, layer = inputs.make_workload(T, d, 128, E, 2, "bf16", seed=T, device="cuda",
+                                    bias=inputs.SKEW_BIAS[:E] if E == 8 else None)
+    res = {}
+    for wide in ("0", "1"):
+        monkeypatch.setenv("MOE_ROUTER_WIDE", wide)
+        lg, idx, g = moe.router(x, layer.Wg, 2, layer.bias)
+        xb = x.clone()
+        moe.block_forward(xb, layer.Wg, layer.W1, layer.W3, layer.W2, 2, bias=layer.bias)
+        torch.cuda.synchronize()
+        res[wide] = (lg.clone(), idx.clone(), g.clone(), xb)
+    a, b = res["0"], res["1"]
+    assert torch.equal(a[0].view(torch.int32), b[0].view(torch.int32))
+    assert torch.equal(a[1], b[1])
+    assert torch.equal(a[2].view(torch.int32), b[2].view(torch.int32))
+    assert torch.equal(a[3].view(torch.int16), b[3].view(torch.int16))
