@@ -84,8 +84,10 @@ __global__ void __launch_bounds__(1024) chunk_scan_kernel(const int *__restrict_
 // records the chunk's count for that expert; a scan over chunks per expert
 // gives each chunk's base; a selection's rank is its chunk's base plus the
 // matching lanes below it, so the row order is (expert, token) as in the two
-// kernels, and the results are the same.  Then the whole block copies the
-// kept rows (row_scale: scaled and rounded, the fused RMSNorm).
+// kernels, and the results are the same.  Then the kept rows are copied
+// (row_scale: scaled and rounded, the fused RMSNorm), the copy split evenly
+// over the grid's blocks; every block ranks the (few) selections itself and
+// block 0 alone writes counts, offsets, perm and inv.
 constexpr int kRouteSmallMax = 1024;
 constexpr int kRouteSmallChunks = kRouteSmallMax / 32;
 
@@ -133,17 +135,19 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
         if (lane == 0) s_tot[e] = capacity > 0 ? min(carry, capacity) : carry;
     }
     __syncthreads();
+    const bool writer = blockIdx.x == 0;
     if (threadIdx.x == 0) {
         int acc = 0;
         s_off[0] = 0;
         for (int e = 0; e < E; ++e) {
-            counts[e] = s_tot[e];
+            if (writer) counts[e] = s_tot[e];
             acc += s_tot[e];
             s_off[e + 1] = acc;
         }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i <= E; i += blockDim.x) offsets[i] = s_off[i];
+    if (writer)
+        for (int i = threadIdx.x; i <= E; i += blockDim.x) offsets[i] = s_off[i];
     for (int c = warp; c < nch; c += nwarps) {
         const int s0 = 32 * c + lane;
         const int sel = s_sel[s0];
@@ -152,27 +156,29 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
             const int rank = s_base[c][sel] + __popc(m & ((1u << lane) - 1u));
             const bool kept = capacity <= 0 || rank < capacity;
             const int r = kept ? s_off[sel] + rank : -1;
-            inv[s0] = r;
+            if (writer) inv[s0] = r;
             if (kept) {
-                perm[r] = s0;
+                if (writer) perm[r] = s0;
                 s_src[r] = s0 / k;
             }
         }
     }
     __syncthreads();
     // rows r < offsets[E]: x_perm[r] = x[source token], flattened to (row,
-    // 16-byte vector) over the block, U loads in flight per thread
+    // 16-byte vector); this block's share of them, U loads in flight per thread
     constexpr int VN = Vec<T>::n;
     constexpr int U = 8;
     const int rowvec = d / VN;
-    const int total = s_off[E] * rowvec;
-    for (int i0 = threadIdx.x; i0 < total; i0 += blockDim.x * U) {
+    const int all = s_off[E] * rowvec;
+    const int beg = (int)((long long)all * blockIdx.x / gridDim.x);
+    const int total = (int)((long long)all * (blockIdx.x + 1) / gridDim.x);
+    for (int i0 = beg + threadIdx.x; i0 < total; i0 += blockDim.x * U) {
         uint4 val[U];
         int row[U], vec[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int i = i0 + blockDim.x * u;
-            const int ii = i < total ? i : 0;
+            const int ii = i < total ? i : beg;
             row[u] = ii / rowvec;
             vec[u] = ii - row[u] * rowvec;
             val[u] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)s_src[row[u]] * d) + vec[u]);
@@ -365,17 +371,21 @@ cudaError_t launch_route_small(const int *idx, int T, int k, int E, int capacity
                                int *perm, int *inv, void *x_perm, cudaStream_t s) {
     const int n = T * k;
     if (n > kRouteSmallMax || E > MOE_MAX_EXPERTS) return cudaErrorInvalidValue;
-    // a warp per 32-selection chunk and per 2 KB of rows to copy, 4 to 32 warps
+    // a warp per 32-selection chunk (at least 4, at most 32); one block per
+    // 16 KB of rows to copy, at most 32 (each ranks the selections itself)
     int warps = (n + 31) / 32;
-    const long long copy_warps = ((long long)n * d * elt + 2047) / 2048;
-    if (copy_warps > warps) warps = copy_warps > 32 ? 32 : (int)copy_warps;
     if (warps < 4) warps = 4;
     if (warps > 32) warps = 32;
+    const long long copy_bytes = (long long)n * d * elt;
+    int blocks = (int)((copy_bytes + (16 << 10) - 1) / (16 << 10));
+    if (blocks < 1) blocks = 1;
+    if (blocks > 32) blocks = 32;
+    const int threads = warps < 8 ? 256 : 32 * warps;
     if (elt == 2)
-        return launch_pdl(route_small_kernel<__nv_bfloat16>, 1, 32 * warps, 0, s, idx, n, k, E,
-                          capacity, static_cast<const __nv_bfloat16 *>(x), row_scale, d, counts,
-                          offsets, perm, inv, static_cast<__nv_bfloat16 *>(x_perm));
-    return launch_pdl(route_small_kernel<float>, 1, 32 * warps, 0, s, idx, n, k, E, capacity,
+        return launch_pdl(route_small_kernel<__nv_bfloat16>, blocks, threads, 0, s, idx, n, k,
+                          E, capacity, static_cast<const __nv_bfloat16 *>(x), row_scale, d,
+                          counts, offsets, perm, inv, static_cast<__nv_bfloat16 *>(x_perm));
+    return launch_pdl(route_small_kernel<float>, blocks, threads, 0, s, idx, n, k, E, capacity,
                       static_cast<const float *>(x), row_scale, d, counts, offsets, perm, inv,
                       static_cast<float *>(x_perm));
 }
