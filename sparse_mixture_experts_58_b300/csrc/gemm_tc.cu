@@ -377,7 +377,10 @@ int run_tc(TcArgs &args, int units_bound, cudaStream_t s) {
             attr_set[dev] = true;
         }
     }
-    const int grid = units_bound < device_sm_count() ? units_bound : device_sm_count();
+    int grid = units_bound < device_sm_count() ? units_bound : device_sm_count();
+    // MOE_TC_GRID=n caps the persistent grid at n CTAs (measurement only)
+    if (const char *g = getenv("MOE_TC_GRID"))
+        if (atoi(g) > 0 && atoi(g) < grid) grid = atoi(g);
     if (grid <= 0) return MOE_OK;
     return launch_pdl(kernel, grid, kThreads, L::kTotal, s, args) == cudaSuccess ? MOE_OK
                                                                                   : MOE_ERR_CUDA;
