@@ -95,6 +95,7 @@ struct PairArgs {
     // interleaved gate/up: mapW0[e] is the 4-D map of W1[e] and W3[e] (box
     // {64, 16, 2, 4}); bit e set when W3[e]'s rows come first in each group
     unsigned long long swap_mask;
+    int balance;  // balanced grid (see the kernel)
 };
 
 struct PairUnit {
@@ -226,8 +227,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncthreads();
     const uint32_t tmem_base = *tmem_slot;
     const int total = s_ustart[E];
-    const int first = static_cast<int>(ptx::cluster_id_x());
-    const int stride = static_cast<int>(ptx::cluster_count_x());
+    // Balanced grid (as in gemm_tc.cu): the fewest rounds of units over the
+    // launched pairs, and only as many pairs as it takes for every one to
+    // run that many; pairs past that count take no unit.  MOE_PAIR_BALANCE
+    // (a kernel argument) turns it off for measurement.
+    const int npairs = static_cast<int>(ptx::cluster_count_x());
+    const int rounds = (total + npairs - 1) / npairs;
+    const int stride = (a.balance && rounds > 0) ? (total + rounds - 1) / rounds : npairs;
+    const int cid = static_cast<int>(ptx::cluster_id_x());
+    const int first = cid < stride ? cid : total;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producers
@@ -537,6 +545,9 @@ int fill_pair(PairArgs &args, const void *tokens, const int *offsets, void *out,
     args.k = 1;
     args.combine = 0;
     args.swap_mask = 0;
+    // MOE_PAIR_BALANCE=0 turns the balanced grid off (measurement only)
+    args.balance = 1;
+    if (const char *b = getenv("MOE_PAIR_BALANCE")) args.balance = atoi(b) != 0;
     args.E = E;
     args.rows = rows;
     args.K = K;

@@ -170,6 +170,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_cons
     __syncthreads();
     const uint32_t tmem_base = *tmem_slot;
     const int total = s_ustart[E];
+    // Balanced grid: the fewest rounds of units over the launched CTAs, and
+    // only as many CTAs as it takes for every one to run that many (512 units
+    // on 148 CTAs: 4 rounds, 128 CTAs of 4 units, rather than 68 CTAs running
+    // a fourth unit alone).  An SM streams weights at about 42-50 GB/s
+    // whatever the load (B300: 148 CTAs at T=16 move 6.25 TB/s, 74 CTAs
+    // 3.7 TB/s), so a round run by few CTAs takes as long as a full one;
+    // measured at T=1 (2 experts busy, gate/up): 148 CTAs 92.5 us, 128 CTAs
+    // 86.7 us.  CTAs past the balanced count take no unit.
+    const int rounds = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int ustride = rounds > 0 ? (total + rounds - 1) / rounds : (int)gridDim.x;
+    const int ufirst = (int)blockIdx.x < ustride ? (int)blockIdx.x : total;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -179,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_cons
             uint32_t ph = 0;
             int issued = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+            for (int u = ufirst; ok && u < total; u += ustride) {
                 const Unit w = decode_unit(u, s_off, s_mt, s_ustart, a, NOUT);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!ptx::mbar_wait_bounded(&empty[stage], ph ^ 1u, s_abort, a.status,
@@ -223,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_cons
             uint32_t ph = 0;
             int it = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < total; u += gridDim.x, ++it) {
+            for (int u = ufirst; ok && u < total; u += ustride, ++it) {
                 const Unit w = decode_unit(u, s_off, s_mt, s_ustart, a, NOUT);
                 const int acc = it & 1;
                 const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
@@ -268,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_cons
         const int quad = warp & 3;  // tensor-memory lanes 32*quad .. +31
         const int r = quad * 32 + lane;
         int it = 0;
-        for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+        for (int u = ufirst; u < total; u += ustride, ++it) {
             const Unit w = decode_unit(u, s_off, s_mt, s_ustart, a, NOUT);
             const int acc = it & 1;
             const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
