@@ -503,8 +503,10 @@ def bench_layer(args, name, cfg, route_kw, dev, rank, world, local, steps, warmu
                       "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                       "d2h_bytes_per_step": out_host.numel() * out_host.element_size(),
                       "how": "per step one moe_forward_host_io call (the C ABI's host-buffer "
-                             "entry point): pinned host tokens -> device, the layer, output -> "
-                             "pinned host memory, all on one stream",
+                             "entry point), all on one stream: the pinned host tokens are read "
+                             "over the bus by the router (batches under 1536 tokens; larger "
+                             "ones are copied to the device first), the layer runs, and its "
+                             "last kernel writes the output into pinned host memory",
                       "output_matches_device_path": bool(torch.equal(out_host, out.cpu()))}
 
     peaks, peak_src = load_peaks()

@@ -200,9 +200,16 @@ int moe_capacity(double capacity_factor, int T, int k, int E, int *capacity);
 
 /*
  * Same as moe_forward, with the tokens and the result in HOST memory: copies
- * x_host -> x_dev, runs the layer into out_dev, copies out_dev -> out_host,
- * all enqueued on `stream`.  The caller synchronises the stream before
- * reading out_host; page-locked host buffers make the copies asynchronous.
+ * x_host -> x_dev, runs the layer, and delivers the result to out_host, all
+ * enqueued on `stream`.  When out_host is page-locked (pinned or registered)
+ * host memory, the layer's last kernel writes the result there directly and
+ * out_dev is not used; otherwise the layer writes out_dev and a copy
+ * out_dev -> out_host follows.  Likewise, for batches the router takes in
+ * one pass (bf16, up to 8 experts, fewer than 1536 tokens) a page-locked
+ * x_host is read by the router directly, which leaves the rows in x_dev for
+ * the later kernels; other batches copy x_host -> x_dev first.  The caller
+ * synchronises the stream before reading out_host, and keeps x_host unchanged
+ * until then.
  */
 int moe_forward_host_io(const void *x_host, void *out_host, void *x_dev, void *out_dev,
                         const void *W_g, const float *router_bias,

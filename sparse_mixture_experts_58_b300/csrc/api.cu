@@ -460,10 +460,13 @@ int read_options(const moe_options *o, Options *out) {
 // norm_eps != nullptr: a pre-norm block, out = x (in place):
 // x <- round(x + MoE(RMSNorm(x))), RMSNorm fused into the router and the
 // grouping, the residual add into the combine.
+// x_host_rows != nullptr: the router reads the tokens from page-locked host
+// memory (the device's address of it) and copies them to x (device memory)
+// for the kernels after it.
 int run_forward(const Plan &P, const Options &O, const void *x, const void *W_g,
                 const float *bias, const void *const *W1, const void *const *W3,
                 const void *const *W2, void *out, void *ws, cudaStream_t s,
-                const float *norm_eps = nullptr) {
+                const float *norm_eps = nullptr, const void *x_host_rows = nullptr) {
     float *logits = ws_at<float>(ws, P.o_logits);
     int *idx = ws_at<int>(ws, P.o_idx);
     float *gates = ws_at<float>(ws, P.o_gates);
@@ -483,9 +486,15 @@ int run_forward(const Plan &P, const Options &O, const void *x, const void *W_g,
     // takes the place of y (which holds splits * T * k * d floats)
     const bool fuse = P.fuse && O.capacity == 0;
     int rc;
-    if ((rc = cuda_rc(launch_router(x, W_g, bias, P.T, P.d, P.E, P.k, P.dt, O.gating, eps, inv_rms,
-                                    logits, idx, gates, s))) != MOE_OK)
+    if (x_host_rows != nullptr) {
+        if ((rc = cuda_rc(launch_router(x_host_rows, W_g, bias, P.T, P.d, P.E, P.k, P.dt,
+                                        O.gating, eps, inv_rms, logits, idx, gates, s,
+                                        const_cast<void *>(x)))) != MOE_OK)
+            return rc;
+    } else if ((rc = cuda_rc(launch_router(x, W_g, bias, P.T, P.d, P.E, P.k, P.dt, O.gating, eps,
+                                           inv_rms, logits, idx, gates, s))) != MOE_OK) {
         return rc;
+    }
     if (P.small_route) {
         if ((rc = cuda_rc(launch_route_small(idx, P.T, P.k, P.E, O.capacity, x, inv_rms, P.d, elt,
                                              counts, offsets, perm, inv, x_perm, s))) != MOE_OK)
@@ -1008,6 +1017,22 @@ int moe_capacity(double capacity_factor, int T, int k, int E, int *capacity) {
     return MOE_OK;
 }
 
+namespace {
+
+// The device's address for page-locked (pinned or registered) host memory,
+// or nullptr for any other pointer (pageable memory, device memory).
+void *device_alias_of_host(const void *p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return nullptr;
+    return at.devicePointer;
+}
+
+}  // namespace
+
 int moe_forward_host_io(const void *x_host, void *out_host, void *x_dev, void *out_dev,
                         const void *W_g, const float *router_bias, const void *const *W1,
                         const void *const *W3, const void *const *W2, int T, int d, int ffn,
@@ -1020,14 +1045,37 @@ int moe_forward_host_io(const void *x_host, void *out_host, void *x_dev, void *o
     if (x_host == nullptr || out_host == nullptr) return MOE_ERR_ARG;
     const size_t bytes = (size_t)T * d * elem_size(dtype);
     const Options O;
+    // A page-locked out_host is written by the layer's last kernel directly
+    // (no device-to-host copy; out_dev is then not touched).  For batches the
+    // router takes in one pass, a page-locked x_host is read by the router
+    // itself, which leaves the rows in x_dev for the later kernels (no
+    // host-to-device copy).  MOE_HOSTIO_DIRECT=0 keeps both copies
+    // (measurement only).
+    void *out_alias = nullptr;
+    const void *x_alias = nullptr;
+    {
+        const char *v = getenv("MOE_HOSTIO_DIRECT");
+        if (v == nullptr || atoi(v) != 0) {
+            out_alias = device_alias_of_host(out_host);
+            if (out_alias != nullptr && !aligned16(out_alias)) out_alias = nullptr;
+            if (dtype == MOE_BF16 && router_reads_host_rows(T, E)) {
+                x_alias = device_alias_of_host(x_host);
+                if (x_alias != nullptr && !aligned16(x_alias)) x_alias = nullptr;
+            }
+        }
+    }
     LaunchKey key = forward_key(4, P, O, x_dev, W_g, router_bias, W1, W3, W2, out_dev, workspace);
-    key.add(x_host).add(out_host);
+    key.add(x_host).add(out_host).add(out_alias).add(x_alias);
     return run_graphed(key, static_cast<cudaStream_t>(stream), [&](cudaStream_t s) {
-        if (cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        if (x_alias == nullptr &&
+            cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
             return (int)MOE_ERR_CUDA;
-        int r = run_forward(P, O, x_dev, W_g, router_bias, W1, W3, W2, out_dev, workspace, s);
+        int r = run_forward(P, O, x_dev, W_g, router_bias, W1, W3, W2,
+                            out_alias != nullptr ? out_alias : out_dev, workspace, s, nullptr,
+                            x_alias);
         if (r != MOE_OK) return r;
-        if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        if (out_alias == nullptr &&
+            cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
             return (int)MOE_ERR_CUDA;
         return (int)MOE_OK;
     });

@@ -74,9 +74,14 @@ int *device_status_ptr();
 // Kernel launchers (each returns the launch's cudaError_t).
 // inv_rms != nullptr: RMSNorm (eps) fused in front of the router; each
 // token's scale is written to inv_rms[T].
+// x_copy != nullptr: x is page-locked host memory (the device's address of
+// it) read over the bus, and the router also copies the rows to x_copy in
+// device memory; only where router_reads_host_rows(T, E) (one pass over the
+// rows, no fused RMSNorm).
 cudaError_t launch_router(const void *x, const void *Wg, const float *bias, int T, int d, int E,
                           int k, int dt, int gating, float eps, float *inv_rms, float *logits,
-                          int *idx, float *gates, cudaStream_t s);
+                          int *idx, float *gates, cudaStream_t s, void *x_copy = nullptr);
+bool router_reads_host_rows(int T, int E);
 cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, int gating,
                                     int *idx, float *gates, cudaStream_t s);
 // Per-chunk expert counts from idx (into chunk_counts), then their per-expert

@@ -58,11 +58,14 @@ __device__ __forceinline__ void finish_token(float *l, const float *bias, int t,
 // of a pass's loads in flight together.  Rows of experts >= E are clamped to
 // a valid row and their sums ignored, which keeps the loads free of branches.
 // NORM: the fused RMSNorm (eps; each token's scale written to inv_rms).
+// x_copy != nullptr (one pass over the rows: EG >= E): x is page-locked host
+// memory read over the bus, and each block also writes its rows to x_copy
+// in device memory for the kernels after it.
 template <typename T, int TB, int EG, int V, bool NORM>
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(
     const T *__restrict__ x, const T *__restrict__ Wg, const float *__restrict__ bias, int Tn,
     int d, int E, int k, int gating, float eps, float *inv_rms, float *logits, int *idx,
-    float *gates) {
+    float *gates, T *x_copy) {
     constexpr int VN = Vec<T>::n;
     constexpr int NW = kRouterThreads / 32;
     __shared__ float s_part[NW][TB][MOE_MAX_EXPERTS];
@@ -131,7 +134,15 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
                 // (experts taken EG at a time) they are kept for the next pass
 #pragma unroll
                 for (int j = 0; j < TB; ++j)
-                    xs[u][j] = v < nvec ? (EG >= E ? __ldcs(xr[j] + vv) : __ldg(xr[j] + vv)) : zero;
+                    xs[u][j] = v < nvec ? (x_copy != nullptr ? xr[j][vv]
+                                           : EG >= E ? __ldcs(xr[j] + vv) : __ldg(xr[j] + vv))
+                                        : zero;
+                if (x_copy != nullptr && v < nvec) {
+#pragma unroll
+                    for (int j = 0; j < TB; ++j)
+                        if (j < nt)
+                            reinterpret_cast<uint4 *>(x_copy + (size_t)(t0 + j) * d)[v] = xs[u][j];
+                }
 #pragma unroll
                 for (int e = 0; e < EG; ++e) w[u][e] = __ldg(wr[e] + vv);
             }
@@ -329,11 +340,12 @@ __global__ void __launch_bounds__(128) topk_kernel(const float *__restrict__ log
 template <typename T, int TB, int EG, int V, bool NORM>
 cudaError_t router_launch(const void *x, const void *Wg, const float *bias, int T_, int d, int E,
                           int k, int gating, float eps, float *inv_rms, float *logits, int *idx,
-                          float *gates, cudaStream_t s) {
+                          float *gates, cudaStream_t s, void *x_copy) {
+    if (x_copy != nullptr && (EG < E || NORM)) return cudaErrorInvalidValue;
     const int grid = (T_ + TB - 1) / TB;
     return launch_pdl(router_kernel<T, TB, EG, V, NORM>, grid, kRouterThreads, 0, s,
                       static_cast<const T *>(x), static_cast<const T *>(Wg), bias, T_, d, E, k,
-                      gating, eps, inv_rms, logits, idx, gates);
+                      gating, eps, inv_rms, logits, idx, gates, static_cast<T *>(x_copy));
 }
 
 // Tokens per block: 2 for small batches (blocks for every SM), 4 or 8 once
@@ -344,12 +356,12 @@ cudaError_t router_launch(const void *x, const void *Wg, const float *bias, int 
 template <typename T, bool NORM>
 cudaError_t router_dispatch_n(const void *x, const void *Wg, const float *bias, int T_, int d,
                               int E, int k, int gating, float eps, float *inv_rms, float *logits,
-                              int *idx, float *gates, cudaStream_t s) {
+                              int *idx, float *gates, cudaStream_t s, void *x_copy) {
 #define MOE_ROUTER(TB, EG, V)                                                                      \
     return router_launch<T, TB, EG, V, NORM>(x, Wg, bias, T_, d, E, k, gating, eps, inv_rms,      \
-                                             logits, idx, gates, s)
+                                             logits, idx, gates, s, x_copy)
     // MOE_ROUTER_CFG=TB,EG,V picks one of the configurations below (measurement only)
-    if (const char *c = getenv("MOE_ROUTER_CFG")) {
+    if (const char *c = x_copy == nullptr ? getenv("MOE_ROUTER_CFG") : nullptr) {
         int tb = 0, eg = 0, v = 0;
         if (sscanf(c, "%d,%d,%d", &tb, &eg, &v) == 3) {
             if (tb == 2 && eg == 8 && v == 2) MOE_ROUTER(2, 8, 2);
@@ -418,7 +430,13 @@ bool router_wide(const void *x, const void *Wg, const float *bias, int T_, int d
 template <typename T>
 cudaError_t router_dispatch(const void *x, const void *Wg, const float *bias, int T_, int d,
                             int E, int k, int gating, float eps, float *inv_rms, float *logits,
-                            int *idx, float *gates, cudaStream_t s) {
+                            int *idx, float *gates, cudaStream_t s, void *x_copy) {
+    if (x_copy != nullptr) {
+        // host rows: the single-pass configurations only
+        if (E > 8 || T_ >= 1536 || inv_rms != nullptr) return cudaErrorInvalidValue;
+        return router_dispatch_n<T, false>(x, Wg, bias, T_, d, E, k, gating, eps, inv_rms,
+                                           logits, idx, gates, s, x_copy);
+    }
     if (sizeof(T) == 2) {
         cudaError_t err = cudaSuccess;
         const bool done =
@@ -431,23 +449,25 @@ cudaError_t router_dispatch(const void *x, const void *Wg, const float *bias, in
     }
     if (inv_rms != nullptr)
         return router_dispatch_n<T, true>(x, Wg, bias, T_, d, E, k, gating, eps, inv_rms, logits,
-                                          idx, gates, s);
+                                          idx, gates, s, nullptr);
     return router_dispatch_n<T, false>(x, Wg, bias, T_, d, E, k, gating, eps, inv_rms, logits,
-                                       idx, gates, s);
+                                       idx, gates, s, nullptr);
 }
 
 }  // namespace
 
 cudaError_t launch_router(const void *x, const void *Wg, const float *bias, int T, int d, int E,
                           int k, int dt, int gating, float eps, float *inv_rms, float *logits,
-                          int *idx, float *gates, cudaStream_t s) {
+                          int *idx, float *gates, cudaStream_t s, void *x_copy) {
     if (T == 0) return cudaSuccess;
     if (dt == MOE_BF16)
         return router_dispatch<__nv_bfloat16>(x, Wg, bias, T, d, E, k, gating, eps, inv_rms,
-                                              logits, idx, gates, s);
+                                              logits, idx, gates, s, x_copy);
     return router_dispatch<float>(x, Wg, bias, T, d, E, k, gating, eps, inv_rms, logits, idx,
-                                  gates, s);
+                                  gates, s, x_copy);
 }
+
+bool router_reads_host_rows(int T, int E) { return E <= 8 && T < 1536; }
 
 cudaError_t launch_topk_from_logits(const float *logits, int T, int E, int k, int gating,
                                     int *idx, float *gates, cudaStream_t s) {

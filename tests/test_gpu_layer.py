@@ -444,3 +444,25 @@ def test_interleaved_gate_up_rows_equal_two_boxes(moe, monkeypatch, order, T, d,
     ref = moe.forward(x, layer.Wg, layer.W1, layer.W3, layer.W2, k)
     torch.cuda.synchronize()
     assert torch.equal(ref.view(torch.int16), outs["1"].view(torch.int16))
+
+
+@pytest.mark.parametrize("pinned_in", [True, False], ids=["pinned_in", "pageable_in"])
+@pytest.mark.parametrize("pinned_out", [True, False], ids=["pinned_out", "pageable_out"])
+@pytest.mark.parametrize("direct", ["1", "0"], ids=["direct", "copy"])
+def test_host_io_paths(moe, monkeypatch, pinned_in, pinned_out, direct):
+    """moe_forward_host_io delivers the device path's bits to out_host
+    whether the router reads page-locked x_host itself (leaving the rows in
+    x_dev) or a copy to x_dev comes first, and whether the last kernel writes
+    page-locked out_host directly or a copy from out_dev follows (pageable
+    buffers, or the direct paths turned off), on repeated calls (launch-graph
+    replays)."""
+    monkeypatch.setenv("MOE_HOSTIO_DIRECT", direct)
+    x, layer = inputs.make_workload(48, 256, 512, 8, 2, "bf16", 19, "cuda")
+    ref = moe.forward(x, layer.Wg, layer.W1, layer.W3, layer.W2, 2).cpu()
+    xh = x.cpu().pin_memory() if pinned_in else x.cpu()
+    for _ in range(3):
+        oh = torch.empty_like(xh, pin_memory=pinned_out)
+        oh.fill_(0)
+        moe.forward_host_io(xh, layer.Wg, layer.W1, layer.W3, layer.W2, 2, out_host=oh)
+        torch.cuda.synchronize()
+        assert torch.equal(oh.view(torch.int16), ref.view(torch.int16))
