@@ -298,15 +298,17 @@ int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p) {
         const long long rows_per_expert = (long long)q.rows / E;
         q.wide = rows_per_expert >= 128 ? 1 : 0;
         // Token tile height of the one-CTA GEMMs: about 1.25x the mean rows
-        // per expert, 32, 64 or 128 (and never past the batch): a shorter tile
-        // lets the ring hold more weight stages, an expert past it costs one
-        // more token tile.  Measured (Mixtral shape, per step): T=100 tile 104
-        // 490.0 us, 64 475.4, 32 466.6; T=200 tile 128 502.3, 64 487.3, 32
-        // 766.7; T=256 tile 128 507.7, 64 638.0.
+        // per expert, 32, 64, 96 or 128 (and never past the batch): a shorter
+        // tile lets the ring hold more weight stages, an expert past it costs
+        // one more token tile.  Measured (Mixtral shape, per step): T=100 tile
+        // 104 490.0 us, 64 475.4, 32 466.6; T=200 tile 128 502.3, 64 487.3, 32
+        // 766.7; T=256 (at most 80 rows an expert) tile 128 495.2, 96 478.5,
+        // 64 638.0; T=320 (at most 89) 128 500.3, 96 483.6; T=400 (at most
+        // 109) 128 504.0, 96 739.2.
         {
             const long long mu = ((long long)q.rows + E - 1) / E;
             const long long need = (5 * mu + 3) / 4;
-            const int tile = need <= 32 ? 32 : need <= 64 ? 64 : 128;
+            const int tile = need <= 32 ? 32 : need <= 64 ? 64 : need <= 96 ? 96 : 128;
             const int whole = ((T + 7) / 8) * 8;
             q.bm = tile < whole ? tile : whole;
             if (q.bm < 8) q.bm = 8;

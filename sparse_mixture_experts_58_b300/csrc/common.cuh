@@ -179,17 +179,20 @@ __device__ __forceinline__ uint4 scale_slice(const uint4 &v, float scale) {
 //   gating 0: z_j = exp(l_j - l0), g_j = z_j / sum_j' z_j' (softmax over kept);
 //   gating 1: g_j = exp(l_j - l0) / sum_e exp(l_e - l0) (full softmax, kept
 //             entries not renormalised).
-template <int KMAX>
-__device__ __forceinline__ void topk_gates(const float *l, int E, int k, int gating,
-                                           int (&sel)[KMAX], float (&g)[KMAX]) {
+// The logits are read through `at(e)`; with EMAX > 0 the loops over experts
+// are unrolled to EMAX (entries from E on ignored), so that logits held in a
+// register array stay in registers.
+template <int KMAX, int EMAX, typename At>
+__device__ __forceinline__ void topk_gates_from(At at, int E, int k, int gating,
+                                                int (&sel)[KMAX], float (&g)[KMAX]) {
     float val[KMAX];
 #pragma unroll
     for (int p = 0; p < KMAX; ++p) {
         val[p] = -INFINITY;
         sel[p] = -1;
     }
-    for (int e = 0; e < E; ++e) {
-        float v = l[e];
+    auto insert = [&](int e) {
+        float v = at(e);
         int id = e;
 #pragma unroll
         for (int p = 0; p < KMAX; ++p) {
@@ -201,6 +204,13 @@ __device__ __forceinline__ void topk_gates(const float *l, int E, int k, int gat
             v = gt ? tv : v;
             id = gt ? ti : id;
         }
+    };
+    if constexpr (EMAX > 0) {
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e)
+            if (e < E) insert(e);
+    } else {
+        for (int e = 0; e < E; ++e) insert(e);
     }
     float z[KMAX];
     float s = 0.f;
@@ -214,10 +224,22 @@ __device__ __forceinline__ void topk_gates(const float *l, int E, int k, int gat
     }
     if (gating == MOE_GATING_SOFTMAX_TOPK) {
         s = 0.f;
-        for (int e = 0; e < E; ++e) s += expf(l[e] - val[0]);
+        if constexpr (EMAX > 0) {
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e)
+                if (e < E) s += expf(at(e) - val[0]);
+        } else {
+            for (int e = 0; e < E; ++e) s += expf(at(e) - val[0]);
+        }
     }
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) g[j] = z[j] / s;
+}
+
+template <int KMAX>
+__device__ __forceinline__ void topk_gates(const float *l, int E, int k, int gating,
+                                           int (&sel)[KMAX], float (&g)[KMAX]) {
+    topk_gates_from<KMAX, 0>([l](int e) { return l[e]; }, E, k, gating, sel, g);
 }
 
 }  // namespace moe

@@ -445,6 +445,7 @@ int launch_swiglu_tc(const void *x_perm, const int *offsets, const void *const *
         if (bm <= 16) return run_tc<112, 10, true, 16>(args, units_bound, s);
         if (bm <= 32) return run_tc<112, 10, true, 32>(args, units_bound, s);
         if (bm <= 64) return run_tc<112, 8, true, 64>(args, units_bound, s);
+        if (bm <= 96) return run_tc<112, 8, true, 96>(args, units_bound, s);
     }
     return run_tc<112, 6, true>(args, units_bound, s);
 }
@@ -471,6 +472,7 @@ int launch_down_tc(const void *h, const int *offsets, const void *const *W2, int
         if (bm <= 16) return run_tc<128, 10, false, 16>(args, units_bound, s);
         if (bm <= 32) return run_tc<128, 9, false, 32>(args, units_bound, s);
         if (bm <= 64) return run_tc<128, 7, false, 64>(args, units_bound, s);
+        if (bm <= 96) return run_tc<128, 8, false, 96>(args, units_bound, s);
     }
     return run_tc<128, 6, false>(args, units_bound, s);
 }

@@ -93,6 +93,17 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// 1-D bulk copy global -> shared of `bytes` contiguous bytes (both addresses
+// 16-byte aligned, bytes a multiple of 16), completion counted on `bar`.
+__device__ __forceinline__ void bulk_load_1d(void *dst, const void *src, uint32_t bytes,
+                                             uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes),
+        "r"(smem_addr(bar))
+        : "memory");
+}
+
 // Same with an L2 cache-policy hint (from createpolicy).
 __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map, int c0, int c1,
                                                  uint64_t *bar, uint64_t policy) {

@@ -18,6 +18,7 @@
 #include <stdlib.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -195,60 +196,213 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
 }
 
 // Router for large batches (bf16, E <= 8, d <= 2 * 256 slices of 8): a
-// persistent grid of kRouterThreads-thread blocks, each with the router matrix
-// staged once in shared memory, walking groups of kWideTB tokens; the next
-// group's rows are loaded into registers while the current one is reduced.
-// Thread i takes the same slices i, i + 256 of every row as router_kernel and
-// sums in the same order (slices, then elements, in order; the butterfly's
-// sums via warp_reduce_scatter; warps in order), so the logits -- and, with
-// NORM, the RMSNorm scales -- are the same bits as router_kernel's.
+// persistent grid of one block per SM, warp-specialised around mbarriers.
+//   warps 0..7  compute: the logits' partial sums of a group of kWideTB
+//               consecutive tokens, from shared memory; each thread keeps its
+//               slices of the router matrix in registers for the whole run
+//   warp 8      lane 0 issues the bulk copies (cp.async.bulk), each group's
+//               rows (one contiguous chunk of x) into a ring of kWideStages
+//               stages, as soon as a stage is free
+//   warp 9      adds the compute warps' sums and writes each token's logits,
+//               choices and gates, from a ring of kWideSums sum buffers
+// The compute warps meet at no block barrier (with NORM, once a group over
+// the row sums of squares), so the selection and the stores of one group
+// overlap the products of the next, and up to kWideStages - 1 groups of rows
+// are in flight per SM.  Compute thread i takes the same slices i, i + 256 of
+// every row as router_kernel and sums in the same order (slices, then
+// elements, in order; the butterfly's sums via warp_reduce_scatter; warps in
+// order), so the logits -- and, with NORM, the RMSNorm scales -- are the same
+// bits as router_kernel's.  The products are issued two experts at a time as
+// packed fp32x2 FMAs, each lane of which rounds exactly as a scalar fmaf.
 constexpr int kWideTB = 4;
 constexpr int kWideE = 8;
-constexpr int kWideNS = 2;  // slices per thread and row (d <= 4096 in bf16)
+constexpr int kWideNS = 2;      // slices per thread and row (d <= 4096 in bf16)
+constexpr int kWideStages = 6;  // ring stages of kWideTB rows
+constexpr int kWideSums = 4;    // sum buffers between the compute warps and warp 9
+constexpr int kWideCompute = kRouterThreads;
+constexpr int kWideThreads = kWideCompute + 64;
+
+// dynamic shared memory: the ring
+__host__ __device__ constexpr size_t wide_smem_bytes(int d) {
+    return (size_t)kWideStages * kWideTB * d * 2;
+}
+
+// Element h (0: low half, 1: high half) of a word of two bf16 values, as
+// Vec<bf16>::unpack gives it.
+__device__ __forceinline__ float bf16_word_elt(uint32_t w, int h) {
+    return __uint_as_float(h ? (w & 0xFFFF0000u) : (w << 16));
+}
+
+// bar.red.and over the compute warps (named barrier 1): every compute thread
+// gets the AND of all their flags
+__device__ __forceinline__ bool compute_warps_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, %2, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(kWideCompute)
+        : "memory");
+    return r != 0;
+}
 
 template <bool NORM>
-__global__ void __launch_bounds__(kRouterThreads, 2) router_wide_kernel(
+__global__ void __launch_bounds__(kWideThreads, 1) router_wide_kernel(
     const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict__ Wg,
     const float *__restrict__ bias, int Tn, int d, int E, int k, int gating, float eps,
-    float *inv_rms, float *logits, int *idx, float *gates) {
-    constexpr int NW = kRouterThreads / 32;
-    extern __shared__ uint4 s_w[];  // [kWideE][nvec] router rows, 16-byte slices
-    __shared__ float s_part[2][NW][kWideTB][kWideE];
+    float *inv_rms, float *logits, int *idx, float *gates, int *status,
+    unsigned long long wait_limit_ns) {
+    constexpr int NW = kWideCompute / 32;
+    constexpr int EP = kWideE / 2;  // expert pairs
+    extern __shared__ __align__(128) uint4 s_ring[];  // [kWideStages][kWideTB][nvec]
+    __shared__ float s_part[kWideSums][NW][kWideTB][kWideE];
     __shared__ float s_ss[2][NW][kWideTB];
-    __shared__ float s_l[2][kWideTB][MOE_MAX_EXPERTS];
-    pdl_wait();
-    pdl_trigger();
+    __shared__ __align__(8) uint64_t s_full[kWideStages], s_empty[kWideStages];
+    __shared__ __align__(8) uint64_t s_sfull[kWideSums], s_sempty[kWideSums];
+    __shared__ int s_abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nvec = d / 8;
-    const uint4 zero = make_uint4(0, 0, 0, 0);
-    for (int i = threadIdx.x; i < kWideE * nvec; i += kRouterThreads) {
-        const int e = i / nvec;
-        s_w[i] = e < E ? __ldg(reinterpret_cast<const uint4 *>(Wg) + i) : zero;
-    }
     const int ngroups = (Tn + kWideTB - 1) / kWideTB;
-    auto load_group = [&](int g, uint4 (&xs)[kWideTB][kWideNS]) {
-        const int t0 = g * kWideTB;
+    const int nlocal = blockIdx.x < ngroups ? (ngroups - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    volatile int *abort = &s_abort;
+
+    if (threadIdx.x == 0) {
+        // the compute warps arrive once per warp (lane 0, after __syncwarp)
+        for (int st = 0; st < kWideStages; ++st) {
+            ptx::mbar_init(&s_full[st], 1);
+            ptx::mbar_init(&s_empty[st], NW);
+        }
+        for (int b = 0; b < kWideSums; ++b) {
+            ptx::mbar_init(&s_sfull[b], NW);
+            ptx::mbar_init(&s_sempty[b], 1);
+        }
+        s_abort = 0;
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp == NW) {
+        // ---- bulk copies: local group i is group blockIdx.x + i * gridDim.x,
+        //      in stage i % kWideStages ----
+        if (lane != 0) return;
+        auto issue = [&](int i) {
+            const int t0 = (blockIdx.x + i * gridDim.x) * kWideTB;
+            const uint32_t bytes = (uint32_t)min(kWideTB, Tn - t0) * (uint32_t)d * 2u;
+            uint64_t *bar = &s_full[i % kWideStages];
+            ptx::mbar_arrive_expect_tx(bar, bytes);
+            ptx::bulk_load_1d(s_ring + (size_t)(i % kWideStages) * kWideTB * nvec,
+                              x + (size_t)t0 * d, bytes, bar);
+        };
+        int issued = 0;
+        for (; issued < kWideStages && issued < nlocal; ++issued) issue(issued);
+        for (; issued < nlocal; ++issued) {
+            // stage of group issued - stages: free once the compute warps are done with it
+            const int j = issued - kWideStages;
+            if (!ptx::mbar_wait_bounded(&s_empty[j % kWideStages], (uint32_t)(j / kWideStages) & 1u,
+                                        abort, status, kStatusProducerWait, wait_limit_ns))
+                break;
+            issue(issued);
+        }
+        if (*abort) {
+            // a wait expired somewhere: let the copies still in flight land
+            // before the block's shared memory is released
+            for (int j = issued - kWideStages; j < issued; ++j)
+                if (j >= 0 && !ptx::mbar_wait_bounded(&s_full[j % kWideStages],
+                                                      (uint32_t)(j / kWideStages) & 1u, nullptr,
+                                                      status, kStatusDrainWait, wait_limit_ns))
+                    break;
+        }
+        return;
+    }
+    if (warp == NW + 1) {
+        // ---- the tokens' sums, selections and gates ----
+        static_assert(kWideTB * kWideE == 32, "one lane per (token, expert) of a group");
+        const int fj = lane >> 3, fe = lane & 7;
+        // the bias term of finish_token (0 without a bias)
+        const float bias_e = bias != nullptr && fe < E ? bias[fe] : 0.f;
+        for (int i = 0; i < nlocal; ++i) {
+            const int b = i % kWideSums;
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait_bounded(
+                                             &s_sfull[b], (uint32_t)(i / kWideSums) & 1u, abort,
+                                             status, kStatusEpilogueWait, wait_limit_ns)))
+                break;
+            const int t0 = (blockIdx.x + i * gridDim.x) * kWideTB;
+            const int nt = min(kWideTB, Tn - t0);
+            // one lane per (token j, expert e): the warps' sums added in
+            // order, the bias, the logit written out
+            float t = s_part[b][0][fj][fe];
 #pragma unroll
-        for (int j = 0; j < kWideTB; ++j) {
-            // rows past the batch repeat its last token (results unused)
-            const uint4 *xr =
-                reinterpret_cast<const uint4 *>(x + (size_t)min(t0 + j, Tn - 1) * d);
+            for (int w2 = 1; w2 < NW; ++w2) t += s_part[b][w2][fj][fe];
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&s_sempty[b]);
+            const float l = t + bias_e;
+            if (fj < nt && fe < E) logits[(size_t)(t0 + fj) * E + fe] = l;
+            // the token's logits gathered in registers by its lane e = 0,
+            // which selects and writes the choices and gates
+            float lv[kWideE];
 #pragma unroll
-            for (int sl = 0; sl < kWideNS; ++sl) {
-                const int v = threadIdx.x + kRouterThreads * sl;
-                xs[j][sl] = (g < ngroups && v < nvec) ? __ldcs(xr + v) : zero;
+            for (int e2 = 0; e2 < kWideE; ++e2)
+                lv[e2] = __shfl_sync(0xffffffffu, l, (lane & ~7) | e2);
+            if (fe == 0 && fj < nt) {
+                const size_t o = (size_t)(t0 + fj) * k;
+                if (k <= 2) {
+                    int sel[2];
+                    float g[2];
+                    topk_gates_from<2, kWideE>([&](int e2) { return lv[e2]; }, E, k, gating, sel,
+                                               g);
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+                        if (q < k) {
+                            idx[o + q] = sel[q];
+                            gates[o + q] = g[q];
+                        }
+                } else {
+                    int sel[MOE_MAX_TOPK];
+                    float g[MOE_MAX_TOPK];
+                    topk_gates_from<MOE_MAX_TOPK, kWideE>([&](int e2) { return lv[e2]; }, E, k,
+                                                          gating, sel, g);
+#pragma unroll
+                    for (int q = 0; q < MOE_MAX_TOPK; ++q)
+                        if (q < k) {
+                            idx[o + q] = sel[q];
+                            gates[o + q] = g[q];
+                        }
+                }
             }
         }
-    };
-    uint4 xs[kWideTB][kWideNS];
-    load_group(blockIdx.x, xs);
-    __syncthreads();
-    int buf = 0;
-    for (int g = blockIdx.x; g < ngroups; g += gridDim.x, buf ^= 1) {
-        uint4 xn[kWideTB][kWideNS];
-        load_group(g + gridDim.x, xn);
-        const int t0 = g * kWideTB;
+        return;
+    }
+
+    // ---- compute warps ----
+    // this thread's slices of the router rows (rows past E read as zero)
+    uint4 wr[kWideNS][kWideE];
+#pragma unroll
+    for (int sl = 0; sl < kWideNS; ++sl) {
+        const int v = threadIdx.x + kWideCompute * sl;
+#pragma unroll
+        for (int e = 0; e < kWideE; ++e)
+            wr[sl][e] = v < nvec && e < E ? __ldg(reinterpret_cast<const uint4 *>(Wg) +
+                                                  (size_t)e * nvec + v)
+                                          : make_uint4(0, 0, 0, 0);
+    }
+    bool ok = true;
+    for (int i = 0; i < nlocal; ++i) {
+        const int st = i % kWideStages, b = i % kWideSums;
+        const int t0 = (blockIdx.x + i * gridDim.x) * kWideTB;
         const int nt = min(kWideTB, Tn - t0);
+        ok = ok && ptx::mbar_wait_bounded(&s_full[st], (uint32_t)(i / kWideStages) & 1u, abort,
+                                          status, kStatusMmaWait, wait_limit_ns);
+        // sum buffer b is free once warp 9 has read group i - kWideSums
+        if (i >= kWideSums)
+            ok = ok && ptx::mbar_wait_bounded(&s_sempty[b], ((uint32_t)(i / kWideSums) & 1u) ^ 1u,
+                                              abort, status, kStatusMmaWait, wait_limit_ns);
+        // a warp leaves the loop as a whole (its lanes meet at __syncwarp below)
+        ok = __all_sync(0xffffffffu, ok);
+        const uint4 *xs = s_ring + (size_t)st * kWideTB * nvec;
         float sc[kWideTB];
 #pragma unroll
         for (int j = 0; j < kWideTB; ++j) sc[j] = 1.f;
@@ -258,68 +412,91 @@ __global__ void __launch_bounds__(kRouterThreads, 2) router_wide_kernel(
             for (int j = 0; j < kWideTB; ++j) {
                 ss[j] = 0.f;
 #pragma unroll
-                for (int sl = 0; sl < kWideNS; ++sl)
-                    if (threadIdx.x + kRouterThreads * sl < nvec)
-                        ss[j] = slice_sumsq<__nv_bfloat16>(ss[j], xs[j][sl]);
+                for (int sl = 0; sl < kWideNS; ++sl) {
+                    const int v = threadIdx.x + kWideCompute * sl;
+                    if (v < nvec) ss[j] = slice_sumsq<__nv_bfloat16>(ss[j], xs[j * nvec + v]);
+                }
             }
             const float tot = warp_reduce_scatter<kWideTB>(ss, lane);
-            if ((lane & 7) == 0) s_ss[buf][warp][lane >> 3] = tot;
-            __syncthreads();
+            if ((lane & 7) == 0) s_ss[i & 1][warp][lane >> 3] = tot;
+            // every compute warp leaves together when a wait failed
+            if (!compute_warps_and(ok)) {
+                *abort = 1;
+                break;
+            }
 #pragma unroll
             for (int j = 0; j < kWideTB; ++j) {
                 float t = 0.f;
 #pragma unroll
-                for (int w2 = 0; w2 < NW; ++w2) t += s_ss[buf][w2][j];
+                for (int w2 = 0; w2 < NW; ++w2) t += s_ss[i & 1][w2][j];
                 sc[j] = rms_scale(t, d, eps);
             }
-            if ((int)threadIdx.x < nt) inv_rms[t0 + threadIdx.x] = sc[threadIdx.x];
+#pragma unroll
+            for (int j = 0; j < kWideTB; ++j)
+                if ((int)threadIdx.x == j && j < nt) inv_rms[t0 + j] = sc[j];
+        } else if (!ok) {
+            break;
         }
-        float acc[kWideTB][kWideE];
+        float2 acc[kWideTB][EP];
 #pragma unroll
         for (int j = 0; j < kWideTB; ++j)
 #pragma unroll
-            for (int e = 0; e < kWideE; ++e) acc[j][e] = 0.f;
+            for (int p = 0; p < EP; ++p) acc[j][p] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int sl = 0; sl < kWideNS; ++sl) {
-            const int v = threadIdx.x + kRouterThreads * sl;
+            const int v = threadIdx.x + kWideCompute * sl;
             if (v >= nvec) break;
-            float a[kWideTB][8];
+            uint32_t xw[kWideTB][4];  // the slice of each row, bf16 pairs
 #pragma unroll
-            for (int j = 0; j < kWideTB; ++j)
-                Vec<__nv_bfloat16>::unpack(
-                    NORM ? scale_slice<__nv_bfloat16>(xs[j][sl], sc[j]) : xs[j][sl], a[j]);
+            for (int j = 0; j < kWideTB; ++j) {
+                const uint4 q = NORM ? scale_slice<__nv_bfloat16>(xs[j * nvec + v], sc[j])
+                                     : xs[j * nvec + v];
+                xw[j][0] = q.x;
+                xw[j][1] = q.y;
+                xw[j][2] = q.z;
+                xw[j][3] = q.w;
+            }
+            // element by element (the order of every sum): x of the four
+            // rows, then the expert pairs
 #pragma unroll
-            for (int e = 0; e < kWideE; ++e) {
-                float wf[8];
-                Vec<__nv_bfloat16>::unpack(s_w[e * nvec + v], wf);
+            for (int e8 = 0; e8 < 8; ++e8) {
+                const int wd = e8 >> 1;
+                float2 a2[kWideTB];
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
+                for (int j = 0; j < kWideTB; ++j) {
+                    const float a = bf16_word_elt(xw[j][wd], e8 & 1);
+                    a2[j] = make_float2(a, a);
+                }
 #pragma unroll
-                    for (int j = 0; j < kWideTB; ++j) acc[j][e] = fmaf(a[j][i], wf[i], acc[j][e]);
+                for (int p = 0; p < EP; ++p) {
+                    const uint4 &q0 = wr[sl][2 * p], &q1 = wr[sl][2 * p + 1];
+                    const uint32_t u0 = wd == 0 ? q0.x : wd == 1 ? q0.y : wd == 2 ? q0.z : q0.w;
+                    const uint32_t u1 = wd == 0 ? q1.x : wd == 1 ? q1.y : wd == 2 ? q1.z : q1.w;
+                    const float2 w2 =
+                        make_float2(bf16_word_elt(u0, e8 & 1), bf16_word_elt(u1, e8 & 1));
+#pragma unroll
+                    for (int j = 0; j < kWideTB; ++j) acc[j][p] = __ffma2_rn(a2[j], w2, acc[j][p]);
+                }
             }
         }
+        // the warp is done with stage st (every lane's reads have returned:
+        // their values fed the FMAs above)
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&s_empty[st]);
         float flat[kWideTB * kWideE];
 #pragma unroll
         for (int j = 0; j < kWideTB; ++j)
 #pragma unroll
-            for (int e = 0; e < kWideE; ++e) flat[j * kWideE + e] = acc[j][e];
+            for (int p = 0; p < EP; ++p) {
+                flat[j * kWideE + 2 * p] = acc[j][p].x;
+                flat[j * kWideE + 2 * p + 1] = acc[j][p].y;
+            }
         const float sum = warp_reduce_scatter<kWideTB * kWideE>(flat, lane);
-        s_part[buf][warp][lane >> 3][lane & 7] = sum;
-        __syncthreads();
-        if (warp == 0) {
-            const int j = lane >> 3, e = lane & 7;
-            float t = s_part[buf][0][j][e];
-#pragma unroll
-            for (int w2 = 1; w2 < NW; ++w2) t += s_part[buf][w2][j][e];
-            s_l[buf][j][e] = t;
-            __syncwarp();
-            if (lane < nt)
-                finish_token(s_l[buf][lane], bias, t0 + lane, E, k, gating, logits, idx, gates);
-        }
-#pragma unroll
-        for (int j = 0; j < kWideTB; ++j)
-#pragma unroll
-            for (int sl = 0; sl < kWideNS; ++sl) xs[j][sl] = xn[j][sl];
+        s_part[b][warp][lane >> 3][lane & 7] = sum;
+        // the warp's sums are in place: __syncwarp orders every lane's store
+        // before lane 0's (releasing) arrival
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&s_sfull[b]);
     }
 }
 
@@ -378,7 +555,8 @@ cudaError_t router_dispatch_n(const void *x, const void *Wg, const float *bias, 
     // Measured (B300, d = 4096, 8 experts, CUDA graph of 50 calls): T=16 (2,8,2)
     // 3.2 us; T=1024 (2,8,2) 7.7, (4,8,1) 6.2, (8,4,1) 6.4; T=2048 (4,8,1) 10.2,
     // (8,4,1) 8.8; T=4096 (4,8,1) 17.3, (8,4,1) 15.9; T=16384 (4,8,1) 66.0,
-    // (8,4,1) 57.2 us.
+    // (8,4,1) 57.2 us.  (From 592 tokens the streaming router_wide_kernel
+    // takes bf16 batches of up to 8 experts.)
     const int blocks_per_sm = 2;
     if (E <= 8) {
         if (T_ >= 1536) MOE_ROUTER(8, 4, 1);
@@ -390,23 +568,31 @@ cudaError_t router_dispatch_n(const void *x, const void *Wg, const float *bias, 
 #undef MOE_ROUTER
 }
 
-// The persistent large-batch router where it applies (bf16, E <= 8, d <= 4096,
-// enough tokens for two blocks per SM); MOE_ROUTER_WIDE=0|1 forces it off or
-// on where it applies (measurement only).
+// The streaming large-batch router where it applies (bf16, E <= 8, d <= 4096,
+// from one group of four tokens per SM); MOE_ROUTER_WIDE=0|1 forces it off or
+// on where it applies (measurement only).  Measured (B300, d = 4096, 8
+// experts, CUDA graph of 50 calls, x resident in L2; router_kernel's best
+// configuration against this one): T=592 6.4 / 4.7 us, T=1024 6.7 / 6.0,
+// T=2048 9.4 / 8.6, T=4096 17.7 / 12.9, T=8192 30.4 / 22.0, T=16384 63.3 /
+// 43.8 us.
+constexpr int kWideMinTokens = 4 * kPlanSms;
+
 template <bool NORM>
 bool router_wide(const void *x, const void *Wg, const float *bias, int T_, int d, int E, int k,
                  int gating, float eps, float *inv_rms, float *logits, int *idx, float *gates,
                  cudaStream_t s, cudaError_t *err) {
     if (E > kWideE || d % 8 != 0 || d / 8 > kWideNS * kRouterThreads) return false;
     const int ngroups = (T_ + kWideTB - 1) / kWideTB;
-    // measured (B300, d = 4096, 8 experts): T=4096 16.6 us against 15.9 with
-    // router_kernel (8 tokens, 4 experts a pass), T=16384 52.9 against 57.3
-    bool on = T_ >= 8192;
+    bool on = T_ >= kWideMinTokens;
     if (const char *v = getenv("MOE_ROUTER_WIDE")) on = atoi(v) != 0;
     if (!on) return false;
     const int sms = device_sm_count();
-    const int grid = ngroups < 2 * sms ? ngroups : 2 * sms;
-    const size_t smem = (size_t)kWideE * (d / 8) * 16;
+    const int grid = ngroups < sms ? ngroups : sms;
+    int *status = device_status_ptr();
+    if (status == nullptr) {
+        *err = cudaErrorInvalidValue;
+        return true;
+    }
     static bool attr_done[2][64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
@@ -414,16 +600,16 @@ bool router_wide(const void *x, const void *Wg, const float *bias, int T_, int d
         return true;
     }
     if (!attr_done[NORM][dev]) {
-        if ((*err = cudaFuncSetAttribute(router_wide_kernel<NORM>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kWideE * 512 * 16))) != cudaSuccess)
+        if ((*err = cudaFuncSetAttribute(
+                 router_wide_kernel<NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                 static_cast<int>(wide_smem_bytes(kWideNS * kRouterThreads * 8)))) != cudaSuccess)
             return true;
         attr_done[NORM][dev] = true;
     }
-    *err = launch_pdl(router_wide_kernel<NORM>, grid, kRouterThreads, smem, s,
+    *err = launch_pdl(router_wide_kernel<NORM>, grid, kWideThreads, wide_smem_bytes(d), s,
                       static_cast<const __nv_bfloat16 *>(x),
                       static_cast<const __nv_bfloat16 *>(Wg), bias, T_, d, E, k, gating, eps,
-                      inv_rms, logits, idx, gates);
+                      inv_rms, logits, idx, gates, status, kWaitLimitNs);
     return true;
 }
 

@@ -105,10 +105,10 @@ def test_forced_down_splits(moe, monkeypatch, splits, pair):
     check_layer(moe, x, layer, k, dtype="bf16", label=f"splits={splits} pair={pair}")
 
 
-@pytest.mark.parametrize("bm", ["8", "16", "24", "32", "64", "128"])
+@pytest.mark.parametrize("bm", ["8", "16", "24", "32", "64", "72", "96", "128"])
 def test_forced_token_tile(moe, monkeypatch, bm):
-    """The one-CTA GEMMs at every token tile height (token slots of 16, 32, 64
-    and 128 rows in shared memory), on a batch whose experts span several
+    """The one-CTA GEMMs at every token tile height (token slots of 16, 32, 64,
+    96 and 128 rows in shared memory), on a batch whose experts span several
     tiles at the small heights."""
     monkeypatch.setenv("MOE_PLAN_BM", bm)
     T, d, ffn, E, k = 150, 256, 448, 8, 2

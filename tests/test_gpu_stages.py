@@ -191,13 +191,17 @@ def test_wait_timeout_selftest(moe):
     assert moe.device_status(clear=True) == 0
 
 
-@pytest.mark.parametrize("T,d,E", [(1500, 4096, 8), (4096, 4096, 8), (2500, 1024, 5),
-                                   (3001, 2048, 8)])
+@pytest.mark.parametrize("T,d,E", [(7, 4096, 8), (600, 512, 3), (1500, 4096, 8),
+                                   (4096, 4096, 8), (2500, 1024, 5), (3001, 2048, 8),
+                                   (16383, 4096, 8)])
 def test_wide_router_same_bits(moe, monkeypatch, T, d, E):
-    """The persistent large-batch router (router rows staged in shared
-    memory, groups of four tokens) sums in router_kernel's order: the same
-    logits, choices and gates bit for bit, and the same pre-norm block
-    (the fused RMSNorm's scales included)."""
+    """The streaming large-batch router (router rows staged in shared memory,
+    groups of four token rows brought in by bulk copies through a ring of
+    stages, eight compute warps handing their sums to a ninth that selects,
+    products as packed fp32x2 FMAs) sums in router_kernel's order:
+    the same logits, choices and gates bit for bit, and the same pre-norm
+    block (the fused RMSNorm's scales included).  The shapes cover fewer
+    groups than SMs, a ragged last group and many trips around the ring."""
     x, layer = inputs.make_workload(T, d, 128, E, 2, "bf16", seed=T, device="cuda",
                                     bias=inputs.SKEW_BIAS[:E] if E == 8 else None)
     res = {}
