@@ -406,6 +406,20 @@ int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p) {
         if (const char *rs = getenv("MOE_ROUTE_SMALL"))
             q.small_route = fits && !q.fuse && atoi(rs) != 0;
     }
+    // The gate/up contraction split in two for the smallest batches (at most
+    // 8 expert rows: a few busy experts whose units fill the grid unevenly;
+    // the kernel halves them only where that takes fewer rounds), the
+    // halves' partial sums added by the later one; the one-kernel grouping
+    // zeroes the arrival counters.  Measured (Mixtral shape, per step, whole /
+    // halves): T=1 138.2 / 133.3 us, T=4 345.3 / 337.0 us; T=2 and T=3 keep
+    // whole units (no fewer rounds).  MOE_PLAN_GSPLIT=0|1 forces it off or on
+    // where it applies (measurement only).
+    {
+        const bool can = dt == MOE_BF16 && !q.wide && !q.pair && q.small_route;
+        q.gsplit = can && q.rows <= 8 ? 1 : 0;
+        if (const char *gs = getenv("MOE_PLAN_GSPLIT")) q.gsplit = can && atoi(gs) != 0;
+        q.nctr = q.gsplit ? ((q.rows + q.bm - 1) / q.bm + E) * ((ffn + 55) / 56) : 0;
+    }
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;
@@ -425,6 +439,8 @@ int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p) {
     q.o_xperm = take((size_t)q.rows * d * elt);
     q.o_h = take((size_t)q.rows * ffn * elt);
     q.o_y = take((size_t)q.splits * q.rows * d * 4);
+    q.o_gpart = take(q.gsplit ? (size_t)2 * q.rows * 2 * ffn * 4 : 0);
+    q.o_gctr = take((size_t)q.nctr * 4);
     q.bytes = off;
     *p = q;
     return MOE_OK;
@@ -499,7 +515,9 @@ int run_forward(const Plan &P, const Options &O, const void *x, const void *W_g,
     }
     if (P.small_route) {
         if ((rc = cuda_rc(launch_route_small(idx, P.T, P.k, P.E, O.capacity, x, inv_rms, P.d, elt,
-                                             counts, offsets, perm, inv, x_perm, s))) != MOE_OK)
+                                             counts, offsets, perm, inv, x_perm, s,
+                                             P.gsplit ? ws_at<int>(ws, P.o_gctr) : nullptr,
+                                             P.nctr))) != MOE_OK)
             return rc;
     } else {
         if ((rc = cuda_rc(launch_chunk_scan(idx, P.T, P.k, P.E, O.capacity, cc, cb, counts,
@@ -522,7 +540,9 @@ int run_forward(const Plan &P, const Options &O, const void *x, const void *W_g,
             if (rc != MOE_OK) return rc;
         } else {
             if ((rc = launch_swiglu_tc(x_perm, offsets, W1, W3, P.rows, P.d, P.ffn, P.E, P.bm,
-                                       P.wide, h, s)) != MOE_OK)
+                                       P.wide, h, s,
+                                       P.gsplit ? ws_at<float>(ws, P.o_gpart) : nullptr,
+                                       P.gsplit ? ws_at<int>(ws, P.o_gctr) : nullptr)) != MOE_OK)
                 return rc;
             if ((rc = launch_down_tc(h, offsets, W2, P.rows, P.d, P.ffn, P.E, P.bm, P.wide,
                                      P.splits, P.kps, y, s)) != MOE_OK)
@@ -678,7 +698,7 @@ class LaunchKey {
     LaunchKey &plan(const Plan &P) {
         return add(P.T).add(P.d).add(P.ffn).add(P.E).add(P.k).add(P.dt).add(P.rows).add(P.wide)
             .add(P.pair).add(P.bm).add(P.splits).add(P.kps).add(P.fuse).add(P.small_route)
-            .add(P.bytes);
+            .add(P.gsplit).add(P.bytes);
     }
     LaunchKey &opts(const Options &O) { return add(O.gating).add(O.capacity).add(O.renorm); }
     const std::string &str() const { return s_; }

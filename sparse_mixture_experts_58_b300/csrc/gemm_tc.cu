@@ -56,16 +56,25 @@ struct TcArgs {
     const int *offsets;        // [E + 1] expert row offsets (device)
     void *out;                 // h bf16 [rows][N]  or  y fp32 [splits][rows][N]
     int *status;               // device status word
+    // gate/up split in two over the contraction (gsplit == 2; the kernel
+    // takes it when it shortens the rounds of units): fp32 partial sums
+    // [2][rows][2 N] (W1 half, then W3 half) and one arrival counter per
+    // (expert, feature tile, token tile), zeroed before the launch
+    float *gpart;
+    int *gctr;
     unsigned long long wait_limit_ns;
-    int E, rows, K, N, bm, kblocks, kps, splits;
+    int E, rows, K, N, bm, kblocks, kps, splits, gsplit;
 };
 
 struct Unit {
-    int e, row0, nrows, n0, ks, kb0, kb1;
+    int e, row0, nrows, n0, ks, kb0, kb1, tile;
 };
 
+// tile: the unit's (expert, feature tile, token tile) index, the same for
+// every split of it
 __device__ __forceinline__ Unit decode_unit(int u, const int *s_off, const int *s_mt,
-                                            const int *s_ustart, const TcArgs &a, int NOUT) {
+                                            const int *s_ustart, const TcArgs &a, int NOUT,
+                                            int splits, int kps) {
     int e = 0;
     while (e + 1 < a.E && u >= s_ustart[e + 1]) ++e;
     const int local = u - s_ustart[e];
@@ -74,12 +83,13 @@ __device__ __forceinline__ Unit decode_unit(int u, const int *s_off, const int *
     const int rest = local / mtn;
     Unit w;
     w.e = e;
-    w.ks = rest % a.splits;
-    w.n0 = (rest / a.splits) * NOUT;
+    w.ks = rest % splits;
+    w.n0 = (rest / splits) * NOUT;
     w.row0 = s_off[e] + mt * a.bm;
     w.nrows = min(a.bm, s_off[e + 1] - w.row0);
-    w.kb0 = w.ks * a.kps;
-    w.kb1 = min(w.kb0 + a.kps, a.kblocks);
+    w.kb0 = w.ks * kps;
+    w.kb1 = min(w.kb0 + kps, a.kblocks);
+    w.tile = s_ustart[e] / splits + (rest / splits) * mtn + mt;
     return w;
 }
 
@@ -89,13 +99,32 @@ struct SmemLayout {
     static constexpr int kBBytes = NB * 128;      // NB rows x 64 bf16
     static constexpr int kRing = STAGES * (kABytes + kBBytes);
     static constexpr int kBars = (2 * STAGES + 5) * 8;
-    static constexpr int kMisc = 8 + 4 * (3 * kMaxE + 2);
+    static constexpr int kMisc = 8 + 4 * (3 * kMaxE + 5);
     static constexpr size_t kTotal = 1024 + kRing + kBars + kMisc;  // + alignment slack
     // the MMA reads 128 rows from the last token slot: past it lie weight slots
     static_assert(STAGES * kABytes + STAGES * kBBytes >= (STAGES - 1) * kABytes + kTileM * 128,
                   "MMA token reads must stay inside the ring");
     static_assert(ABM % 8 == 0 && ABM <= kTileM, "token slot of whole 8-row swizzle atoms");
 };
+
+// Named barrier 1 over the four epilogue warps; the AND form gives every
+// epilogue thread the AND of their flags.
+__device__ __forceinline__ void epilogue_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpilogueThreads) : "memory");
+}
+
+__device__ __forceinline__ bool epilogue_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, %2, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(kEpilogueThreads)
+        : "memory");
+    return r != 0;
+}
 
 template <int NB, int STAGES, bool SWIGLU, int ABM>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_constant__ TcArgs a) {
@@ -122,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_cons
     int *s_off = reinterpret_cast<int *>(tmem_slot + 2);  // [kMaxE + 1]
     int *s_mt = s_off + kMaxE + 1;                         // [kMaxE]
     int *s_ustart = s_mt + kMaxE;                          // [kMaxE + 1]
+    int *s_cfg = s_ustart + kMaxE + 1;  // [0] splits, [1] 64-wide blocks a split, [2] last arrival
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = a.E;
@@ -157,19 +187,36 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_cons
     __syncthreads();
     ptx::tc_fence_after_sync();
     if (threadIdx.x == 0) {
-        int acc = 0;
+        int units = 0;
         for (int e = 0; e < E; ++e) {
             const int cnt = s_off[e + 1] - s_off[e];
             const int mt = cnt > 0 ? (cnt + a.bm - 1) / a.bm : 0;
             s_mt[e] = mt;
+            units += mt * NT;
+        }
+        int splits = a.splits, kps = a.kps;
+        if (SWIGLU && a.gsplit > 1) {
+            // halves of the contraction when they take fewer rounds of the
+            // grid than whole units (T=1: 512 units are 4 rounds on 128 CTAs,
+            // 1024 halves 7 rounds on 147 CTAs, 3.5 units' bytes each)
+            const int g = (int)gridDim.x;
+            const int r1 = (units + g - 1) / g, r2 = (2 * units + g - 1) / g;
+            splits = r2 < 2 * r1 ? 2 : 1;
+            kps = (a.kblocks + splits - 1) / splits;
+        }
+        int acc = 0;
+        for (int e = 0; e < E; ++e) {
             s_ustart[e] = acc;
-            acc += mt * NT * a.splits;
+            acc += s_mt[e] * NT * splits;
         }
         s_ustart[E] = acc;
+        s_cfg[0] = splits;
+        s_cfg[1] = kps;
     }
     __syncthreads();
     const uint32_t tmem_base = *tmem_slot;
     const int total = s_ustart[E];
+    const int splits = s_cfg[0], kps = s_cfg[1];
     // Balanced grid: the fewest rounds of units over the launched CTAs, and
     // only as many CTAs as it takes for every one to run that many (512 units
     // on 148 CTAs: 4 rounds, 128 CTAs of 4 units, rather than 68 CTAs running
@@ -191,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_cons
             int issued = 0;
             bool ok = true;
             for (int u = ufirst; ok && u < total; u += ustride) {
-                const Unit w = decode_unit(u, s_off, s_mt, s_ustart, a, NOUT);
+                const Unit w = decode_unit(u, s_off, s_mt, s_ustart, a, NOUT, splits, kps);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!ptx::mbar_wait_bounded(&empty[stage], ph ^ 1u, s_abort, a.status,
                                                 kStatusProducerWait, a.wait_limit_ns)) {
@@ -235,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_cons
             int it = 0;
             bool ok = true;
             for (int u = ufirst; ok && u < total; u += ustride, ++it) {
-                const Unit w = decode_unit(u, s_off, s_mt, s_ustart, a, NOUT);
+                const Unit w = decode_unit(u, s_off, s_mt, s_ustart, a, NOUT, splits, kps);
                 const int acc = it & 1;
                 const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
                 if (!ptx::mbar_wait_bounded(&acc_empty[acc], aph ^ 1u, s_abort, a.status,
@@ -280,18 +327,41 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_cons
         const int r = quad * 32 + lane;
         int it = 0;
         for (int u = ufirst; u < total; u += ustride, ++it) {
-            const Unit w = decode_unit(u, s_off, s_mt, s_ustart, a, NOUT);
+            const Unit w = decode_unit(u, s_off, s_mt, s_ustart, a, NOUT, splits, kps);
             const int acc = it & 1;
             const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
-            if (!ptx::mbar_wait_bounded(&acc_full[acc], aph, s_abort, a.status,
-                                        kStatusEpilogueWait, a.wait_limit_ns))
-                break;
+            // gate/up halves: partial sums out, the last half of a tile adds them
+            const bool part = SWIGLU && splits > 1;
+            bool ok = ptx::mbar_wait_bounded(&acc_full[acc], aph, s_abort, a.status,
+                                             kStatusEpilogueWait, a.wait_limit_ns);
+            // the epilogue warps meet below when splitting: they leave together
+            if (part) ok = epilogue_and(ok);
+            if (!ok) break;
             ptx::tc_fence_after_sync();
             const uint32_t tb =
                 tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * NB);
             if (quad * 32 < w.nrows) {
                 const bool row_ok = r < w.nrows;
-                if (SWIGLU) {
+                if (part) {
+                    float *prow = a.gpart +
+                                  ((size_t)w.ks * a.rows + w.row0 + r) * (2 * (size_t)a.N) + w.n0;
+#pragma unroll 1
+                    for (int c = 0; c < NOUT; c += 32) {
+                        uint32_t U[32], V[32];
+                        ptx::tmem_ld_32x32b_x32(tb + c, U);
+                        ptx::tmem_ld_32x32b_x32(tb + NOUT + c, V);
+                        ptx::tmem_ld_wait();
+                        const int nval = min(32, min(NOUT - c, a.N - (w.n0 + c)));
+                        if (row_ok) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (i < nval) {
+                                    prow[c + i] = __uint_as_float(U[i]);
+                                    prow[a.N + c + i] = __uint_as_float(V[i]);
+                                }
+                        }
+                    }
+                } else if (SWIGLU) {
                     __nv_bfloat16 *hrow = static_cast<__nv_bfloat16 *>(a.out) +
                                           (size_t)(w.row0 + r) * a.N + w.n0;
 #pragma unroll 1
@@ -347,6 +417,32 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc(const __grid_cons
             }
             ptx::tc_fence_before_sync();
             ptx::mbar_arrive(&acc_empty[acc]);
+            if (part) {
+                // the tile's last half (an arrival counter) adds the halves'
+                // partial sums in split order and applies the SwiGLU
+                __threadfence();
+                epilogue_sync();
+                if (warp == 2 && lane == 0)
+                    s_cfg[2] = atomicAdd(&a.gctr[w.tile], 1) == splits - 1 ? 1 : 0;
+                epilogue_sync();
+                if (s_cfg[2]) {
+                    __threadfence();
+                    const size_t rs = 2 * (size_t)a.N, ss = (size_t)a.rows * rs;
+                    for (int q = (int)threadIdx.x - 64; q < w.nrows * NOUT; q += kEpilogueThreads) {
+                        const int row = q / NOUT, c = q - row * NOUT;
+                        if (w.n0 + c >= a.N) continue;
+                        const float *pp = a.gpart + (size_t)(w.row0 + row) * rs + w.n0 + c;
+                        float uu = pp[0], vv = pp[a.N];
+                        for (int s2 = 1; s2 < splits; ++s2) {
+                            uu += pp[s2 * ss];
+                            vv += pp[s2 * ss + a.N];
+                        }
+                        const float hv = uu / (1.f + expf(-uu)) * vv;
+                        static_cast<__nv_bfloat16 *>(a.out)[(size_t)(w.row0 + row) * a.N + w.n0 + c] =
+                            __float2bfloat16_rn(hv);
+                    }
+                }
+            }
         }
     }
 
@@ -417,7 +513,7 @@ int fill_common(TcArgs &args, const void *A, const int *offsets, void *out, int 
 
 int launch_swiglu_tc(const void *x_perm, const int *offsets, const void *const *W1,
                      const void *const *W3, int rows, int d, int ffn, int E, int bm, int wide,
-                     void *h, cudaStream_t s) {
+                     void *h, cudaStream_t s, float *gpart, int *gctr) {
     if (rows == 0) return MOE_OK;
     TcArgs args;  // copied into the launch's parameter space at enqueue
     // few rows per expert: 112-row tiles (56 W1 + 56 W3 rows) make the Mixtral
@@ -434,8 +530,11 @@ int launch_swiglu_tc(const void *x_perm, const int *offsets, const void *const *
     }
     args.splits = 1;
     args.kps = args.kblocks;
+    args.gpart = gpart;
+    args.gctr = gctr;
+    args.gsplit = (!wide && gpart != nullptr && gctr != nullptr) ? 2 : 1;
     const int NT = (ffn + NB / 2 - 1) / (NB / 2);
-    const int units_bound = ((rows + bm - 1) / bm + E) * NT;
+    const int units_bound = ((rows + bm - 1) / bm + E) * NT * args.gsplit;
     if (wide) return run_tc<256, 4, true>(args, units_bound, s);
     // few tokens per tile: token slots of 16/32/64 rows and more stages, about
     // 160-180 KB of ring either way (measured at 16 tokens: 6 stages of 128-row
@@ -463,6 +562,9 @@ int launch_down_tc(const void *h, const int *offsets, const void *const *W2, int
             return rc;
     args.splits = splits;
     args.kps = kps;
+    args.gpart = nullptr;
+    args.gctr = nullptr;
+    args.gsplit = 1;
     const int NT = (d + NB - 1) / NB;
     const int units_bound = ((rows + bm - 1) / bm + E) * NT * splits;
     if (wide) return run_tc<256, 4, false>(args, units_bound, s);

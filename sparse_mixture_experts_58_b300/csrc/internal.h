@@ -28,10 +28,14 @@ struct Plan {
     int fuse;      // 1: the down projection's epilogue adds gate x output into
                    // a zeroed fp32 row per token (the combine), a finalize
                    // pass rounds it; needs k <= 2, one split, the pair kernel
+    int gsplit;    // 1: the gate/up GEMM may split its contraction in two (the
+                   // kernel decides from the busy experts); counters zeroed by
+                   // the one-kernel grouping
+    int nctr;      // gate/up split arrival counters
     // workspace layout (byte offsets, 256-aligned)
     size_t o_logits, o_idx, o_gates, o_ccount, o_cbase, o_counts, o_offsets, o_perm, o_inv;
     size_t o_rms;  // per-token RMSNorm scale (pre-norm blocks)
-    size_t o_xperm, o_h, o_y, bytes;
+    size_t o_xperm, o_h, o_y, o_gpart, o_gctr, bytes;
 };
 
 int make_plan(int T, int d, int ffn, int E, int k, int dt, Plan *p);
@@ -100,19 +104,25 @@ cudaError_t launch_group_tokens(const int *idx, const int *chunk_base, const int
                                 cudaStream_t s, float *zero_acc = nullptr);
 // The grouping of a batch of at most route_small_max() selections (T * k) in
 // one kernel: counts, offsets, perm, inv and the row copies (row_scale: the
-// fused RMSNorm), as chunk_scan + group_tokens give them.
+// fused RMSNorm), as chunk_scan + group_tokens give them.  Block 0 also sets
+// zero_ctr[0 .. nzero) to zero (the gate/up split's arrival counters).
 int route_small_max();
 cudaError_t launch_route_small(const int *idx, int T, int k, int E, int capacity, const void *x,
                                const float *row_scale, int d, int elt, int *counts, int *offsets,
-                               int *perm, int *inv, void *x_perm, cudaStream_t s);
+                               int *perm, int *inv, void *x_perm, cudaStream_t s,
+                               int *zero_ctr = nullptr, int nzero = 0);
 // x_perm[r] = x[perm[r] / k] for r < rows.
 cudaError_t launch_permute(const void *x, const int *perm, int rows, int d, int k, int elt,
                            void *x_perm, cudaStream_t s);
 
 // Grouped expert GEMMs.  `rows` = total expert rows (T*k); `bm` rows per tile.
+// gpart/gctr (both or neither; one-CTA kernel only): scratch for splitting the
+// gate/up contraction in two where that shortens the rounds of units -- fp32
+// partial sums [2][rows][2 ffn] and (rows / bm + E) * ceil(ffn / 56) arrival
+// counters that must be zero at launch.
 int launch_swiglu_tc(const void *x_perm, const int *offsets, const void *const *W1,
                      const void *const *W3, int rows, int d, int ffn, int E, int bm, int wide,
-                     void *h, cudaStream_t s);
+                     void *h, cudaStream_t s, float *gpart = nullptr, int *gctr = nullptr);
 int launch_down_tc(const void *h, const int *offsets, const void *const *W2, int rows, int d,
                    int ffn, int E, int bm, int wide, int splits, int kps, float *y,
                    cudaStream_t s);

@@ -95,7 +95,7 @@ template <typename T>
 __global__ void __launch_bounds__(1024) route_small_kernel(
     const int *__restrict__ idx, int n, int k, int E, int capacity, const T *__restrict__ x,
     const float *__restrict__ row_scale, int d, int *counts, int *offsets, int *perm, int *inv,
-    T *x_perm) {
+    T *x_perm, int *zero_ctr, int nzero) {
     __shared__ int s_sel[kRouteSmallMax];
     __shared__ int s_src[kRouteSmallMax];  // row -> source token
     __shared__ uint8_t s_cnt[kRouteSmallChunks][MOE_MAX_EXPERTS];
@@ -104,6 +104,8 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
     __shared__ int s_off[MOE_MAX_EXPERTS + 1];
     pdl_wait();
     pdl_trigger();
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero_ctr[i] = 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwarps = blockDim.x >> 5;
     const int nch = (n + 31) / 32;
@@ -368,7 +370,8 @@ int route_small_max() { return kRouteSmallMax; }
 
 cudaError_t launch_route_small(const int *idx, int T, int k, int E, int capacity, const void *x,
                                const float *row_scale, int d, int elt, int *counts, int *offsets,
-                               int *perm, int *inv, void *x_perm, cudaStream_t s) {
+                               int *perm, int *inv, void *x_perm, cudaStream_t s, int *zero_ctr,
+                               int nzero) {
     const int n = T * k;
     if (n > kRouteSmallMax || E > MOE_MAX_EXPERTS) return cudaErrorInvalidValue;
     // a warp per 32-selection chunk (at least 4, at most 32); one block per
@@ -384,10 +387,11 @@ cudaError_t launch_route_small(const int *idx, int T, int k, int E, int capacity
     if (elt == 2)
         return launch_pdl(route_small_kernel<__nv_bfloat16>, blocks, threads, 0, s, idx, n, k,
                           E, capacity, static_cast<const __nv_bfloat16 *>(x), row_scale, d,
-                          counts, offsets, perm, inv, static_cast<__nv_bfloat16 *>(x_perm));
+                          counts, offsets, perm, inv, static_cast<__nv_bfloat16 *>(x_perm),
+                          zero_ctr, nzero);
     return launch_pdl(route_small_kernel<float>, blocks, threads, 0, s, idx, n, k, E, capacity,
                       static_cast<const float *>(x), row_scale, d, counts, offsets, perm, inv,
-                      static_cast<float *>(x_perm));
+                      static_cast<float *>(x_perm), zero_ctr, nzero);
 }
 
 cudaError_t launch_permute(const void *x, const int *perm, int rows, int d, int k, int elt,

@@ -116,6 +116,29 @@ def test_forced_token_tile(moe, monkeypatch, bm):
     check_layer(moe, x, layer, k, dtype="bf16", label=f"token tile {bm}")
 
 
+@pytest.mark.parametrize("T,d,ffn,E,k", [
+    (1, 256, 448, 8, 2),
+    (2, 256, 448, 8, 2),
+    (3, 128, 320, 8, 2),        # ffn = 320: the last 56-feature tile holds 40
+    (3, 512, 1024, 4, 2),
+    (1, 4096, 14336, 8, 2),     # Mixtral shape, one token
+])
+@pytest.mark.parametrize("gsplit", ["0", "1"], ids=["whole", "halves"])
+def test_gate_up_halves_for_the_smallest_batches(moe, monkeypatch, T, d, ffn, E, k, gsplit):
+    """The gate/up contraction in two halves for the smallest batches (fp32
+    partial sums; the later half of each tile adds them in split order and
+    applies the SwiGLU) and whole, against the oracle; repeated calls give
+    the same bits whichever half of a tile finishes last."""
+    monkeypatch.setenv("MOE_PLAN_GSPLIT", gsplit)
+    x, layer = inputs.make_workload(T, d, ffn, E, k, "bf16", seed=T + 31, device="cuda")
+    check_layer(moe, x, layer, k, dtype="bf16", label=f"T{T} d{d} ffn{ffn} gsplit={gsplit}")
+    outs = [moe.forward(x, layer.Wg, layer.W1, layer.W3, layer.W2, k) for _ in range(3)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    assert moe.device_status(clear=True) == 0
+
+
 def test_empty_batch(moe):
     x, layer = inputs.make_workload(0, 128, 256, 8, 2, "bf16", 0, "cuda")
     out = moe.forward(x, layer.Wg, layer.W1, layer.W3, layer.W2, 2)
