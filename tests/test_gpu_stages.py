@@ -195,13 +195,14 @@ def test_wait_timeout_selftest(moe):
                                    (4096, 4096, 8), (2500, 1024, 5), (3001, 2048, 8),
                                    (16383, 4096, 8)])
 def test_wide_router_same_bits(moe, monkeypatch, T, d, E):
-    """The streaming large-batch router (router rows staged in shared memory,
-    groups of four token rows brought in by bulk copies through a ring of
-    stages, eight compute warps handing their sums to a ninth that selects,
-    products as packed fp32x2 FMAs) sums in router_kernel's order:
-    the same logits, choices and gates bit for bit, and the same pre-norm
-    block (the fused RMSNorm's scales included).  The shapes cover fewer
-    groups than SMs, a ragged last group and many trips around the ring."""
+    """The streaming large-batch router (each compute thread's slices of the
+    router rows in registers, groups of four token rows brought in by bulk
+    copies through a ring of stages by one warp, the eight compute warps'
+    sums selected by another, products as packed fp32x2 FMAs) sums in
+    router_kernel's order: the same logits, choices and gates bit for bit,
+    and the same pre-norm block (the fused RMSNorm's scales included).  The
+    shapes cover fewer groups than SMs, a ragged last group and many trips
+    around the ring."""
     x, layer = inputs.make_workload(T, d, 128, E, 2, "bf16", seed=T, device="cuda",
                                     bias=inputs.SKEW_BIAS[:E] if E == 8 else None)
     res = {}
@@ -217,3 +218,35 @@ def test_wide_router_same_bits(moe, monkeypatch, T, d, E):
     assert torch.equal(a[1], b[1])
     assert torch.equal(a[2].view(torch.int32), b[2].view(torch.int32))
     assert torch.equal(a[3].view(torch.int16), b[3].view(torch.int16))
+
+
+@pytest.mark.parametrize("E,k,gating", [(8, 1, 0), (8, 3, 0), (8, 8, 0), (8, 2, 1), (4, 3, 1),
+                                        (6, 2, 0)])
+def test_wide_router_selection_variants(moe, monkeypatch, E, k, gating):
+    """The streaming router's selection (one lane per (token, expert) adds the
+    warps' sums and the bias; the token's logits, gathered in registers, go
+    through the same top-k and gate arithmetic as router_kernel's) for k from
+    1 to 8 and both gatings (softmax over the kept logits, or over all E):
+    the same logits, choices, gates and layer output bit for bit."""
+    T, d, ffn = 650, 256, 128   # 650 tokens: the last group of four holds two
+    bias = inputs.SKEW_BIAS[:E] if E == 8 else None
+    x, layer = inputs.make_workload(T, d, ffn, E, k, "bf16", seed=10 * E + k, device="cuda",
+                                    bias=bias)
+    res = {}
+    for wide in ("0", "1"):
+        monkeypatch.setenv("MOE_ROUTER_WIDE", wide)
+        routed = None
+        if gating == 0:
+            lg, idx, g = moe.router(x, layer.Wg, k, layer.bias)
+            routed = (lg.clone(), idx.clone(), g.clone())
+        out = moe.forward(x, layer.Wg, layer.W1, layer.W3, layer.W2, k, bias=layer.bias,
+                          gating=gating)
+        torch.cuda.synchronize()
+        res[wide] = (routed, out.clone())
+    (ra, oa), (rb, ob) = res["0"], res["1"]
+    if ra is not None:
+        assert torch.equal(ra[0].view(torch.int32), rb[0].view(torch.int32))
+        assert torch.equal(ra[1], rb[1])
+        assert torch.equal(ra[2].view(torch.int32), rb[2].view(torch.int32))
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+    assert moe.device_status(clear=True) == 0
