@@ -214,10 +214,11 @@ def test_decode_config_all_tokens(moe, decode_case):
     check_layer(moe, x, layer, 2, label="decode T=16")
 
 
-@pytest.mark.parametrize("T", [1, 3, 5])
+@pytest.mark.parametrize("T", [1, 3, 4, 5])
 def test_decode_weights_few_tokens(moe, decode_case, T):
-    """The decode layer's weights with 1, 3 and 5 tokens: two to ten expert
-    rows, most experts idle, token tiles of 8 rows."""
+    """The decode layer's weights with 1, 3, 4 and 5 tokens: two to ten expert
+    rows, most experts idle, token tiles of 8 rows (the gate/up contraction
+    in halves where the kernel takes them: one token, two busy experts)."""
     x, layer = decode_case
     check_layer(moe, x[:T].contiguous(), layer, 2, label=f"decode weights T={T}")
 
@@ -241,6 +242,19 @@ def test_prefill_config_sampled(moe):
     for e in range(layer.E):
         assert (idx[rows] == e).any(1).sum() >= 32
     check_layer(moe, x, layer, 2, rows=rows, label=f"prefill T=4096 ({len(rows)} layout rows)")
+    del x, layer
+    torch.cuda.empty_cache()
+
+
+def test_mixtral_shape_96_row_token_tiles(moe):
+    """T=256 at the Mixtral shape: 64 rows per expert on average, at most
+    about 80, so the one-CTA GEMMs take 96-row token tiles (8 ring stages);
+    every expert's layout edges and at least 16 rows per expert."""
+    T = 256
+    x, layer = inputs.make_workload(T, 4096, 14336, 8, 2, "bf16", seed=T, device="cuda")
+    assert moe.down_splits(T, 4096, 14336, 8, 2, moe.BF16) == 1
+    rows, host, idx = _layout_sample(x, layer, 2, per_expert=16, seed=3)
+    check_layer(moe, x, layer, 2, rows=rows, label=f"T=256 ({len(rows)} layout rows)")
     del x, layer
     torch.cuda.empty_cache()
 
