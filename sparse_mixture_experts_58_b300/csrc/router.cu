@@ -14,6 +14,11 @@
 // token's RMSNorm scale (stored for the grouping pass); the logits are then
 // taken of round(x * scale), the normalised row the stand-alone RMSNorm
 // kernel would have stored, read again from L1.
+//
+// Large bf16 batches (from four tokens per SM, up to 8 experts) go to
+// router_wide_kernel, which streams the token rows through shared memory with
+// bulk copies and keeps the router rows in registers; it sums in the same
+// order, so the logits are the same bits either way.
 #include <stdio.h>
 #include <stdlib.h>
 
