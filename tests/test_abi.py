@@ -222,6 +222,19 @@ def test_backward_validates_before_launch(moe):
     assert lib.moe_backward_workspace_bytes(16, 256, 512, E, 2, moe.F32, ctypes.byref(n)) == -2
 
 
+def test_gate_up_halves_scratch_in_workspace(moe):
+    """Batches of up to 8 expert rows (T <= 4 at top-2) reserve the gate/up
+    halves' scratch: fp32 partial sums [2][rows][2 ffn] and the arrival
+    counters; T = 5 (10 rows) does not, and shrinks below T = 4 despite the
+    larger batch."""
+    d, ffn = 4096, 14336
+    ws = {T: moe.workspace_bytes(T, d, ffn, 8, 2, moe.BF16) for T in range(1, 7)}
+    for T in range(1, 5):
+        assert ws[T] >= 2 * (2 * T) * 2 * ffn * 4
+    assert ws[5] < ws[4]
+    assert ws[5] < 2 * 10 * 2 * ffn * 4
+
+
 def test_static_scratch_limit_stated_in_header():
     """The header's statement of the fixed scratch array's reach: at the
     Mixtral shape every batch of up to 81 tokens fits, 82 does not, and a
