@@ -165,3 +165,27 @@ def test_backward_matches_rounding_emulation(moe, T, d, ffn, E, k):
     for key in ("dW1", "dW3", "dW2"):
         n = ((got[key] - ref[key]).norm() / ref[key].norm()).item()
         assert n <= 1e-3, (key, n)
+
+
+def _random_backward_case(i):
+    """The i-th seeded random backward shape: tokens 1..800, hidden and
+    expert widths in 64-wide steps, 1..16 experts, top-1..4."""
+    rng = np.random.default_rng(5000 + i)
+    band = rng.random()
+    T = int(rng.integers(1, 17) if band < 0.3 else rng.integers(17, 801))
+    d = 64 * int(rng.integers(1, 7))
+    ffn = 64 * int(rng.integers(1, 9))
+    E = int(rng.integers(1, 17))
+    k = int(rng.integers(1, min(E, 4) + 1))
+    return T, d, ffn, E, k, int(rng.integers(0, 1 << 30))
+
+
+@pytest.mark.parametrize("i", range(32))
+def test_random_backward_against_oracle(moe, i):
+    """Seeded random shapes (ragged token tiles, empty experts, one expert,
+    top-1 to top-4) against the oracle's backward with the same bars."""
+    T, d, ffn, E, k, seed = _random_backward_case(i)
+    x, layer, dout, ties = _case(T, d, ffn, E, k, seed=seed)
+    if ties.all():
+        pytest.skip("every token near a tie")
+    _compare(moe, x, layer, dout, k, f"random {i}: T{T} d{d} ffn{ffn} E{E} k{k}")
