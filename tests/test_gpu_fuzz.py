@@ -89,3 +89,30 @@ def test_random_layer_against_oracle(moe, monkeypatch, i):
     print(f"PARITY {label}: gated {err:.3e} over {keep.sum()} tokens, {(~keep).sum()} near ties")
     assert keep.mean() > 0.8, label
     assert err <= helpers.tol(dtype), (label, err)
+
+
+EPS = 1e-5
+
+
+@pytest.mark.parametrize("i", range(48))
+def test_random_block_equals_unfused_chain(moe, monkeypatch, i):
+    """The pre-norm block x <- x + MoE(RMSNorm(x)) (moe_block_forward: the
+    RMSNorm fused into the router and the grouping, the residual into the
+    combine) against the same block from the separate entry points
+    (add_rmsnorm, forward, add_rmsnorm), bit for bit, over random shapes,
+    routings and tile plans."""
+    c = _case(10_000 + i)
+    for name, v in c["knobs"].items():
+        monkeypatch.setenv(name, v)
+    T, d, ffn, E, k, dtype = c["T"], c["d"], c["ffn"], c["E"], c["k"], c["dtype"]
+    x0, layer = inputs.make_workload(T, d, ffn, E, k, dtype, seed=c["seed"], device="cuda")
+    a, b = x0.clone(), x0.clone()
+    xn = moe.add_rmsnorm(a, eps=EPS)
+    out = moe.forward(xn, layer.Wg, layer.W1, layer.W3, layer.W2, k, bias=layer.bias,
+                      gating=c["gating"])
+    moe.add_rmsnorm(a, out, eps=EPS)
+    moe.block_forward(b, layer.Wg, layer.W1, layer.W3, layer.W2, k, bias=layer.bias, eps=EPS,
+                      gating=c["gating"])
+    torch.cuda.synchronize()
+    view = torch.int16 if dtype == "bf16" else torch.int32
+    assert torch.equal(a.view(view), b.view(view)), f"case {10_000 + i}: {c}"
