@@ -116,3 +116,24 @@ def test_random_block_equals_unfused_chain(moe, monkeypatch, i):
     torch.cuda.synchronize()
     view = torch.int16 if dtype == "bf16" else torch.int32
     assert torch.equal(a.view(view), b.view(view)), f"case {10_000 + i}: {c}"
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_host_io_equals_device_path(moe, i):
+    """moe_forward_host_io with page-locked host tokens and output (the router
+    reading the rows over the bus below 1536 tokens, the last kernel writing
+    the output into host memory) gives the device path's bits, over random
+    shapes, dtypes and expert counts, on repeated calls."""
+    c = _case(20_000 + i)
+    T, d, ffn, E, k, dtype = c["T"], c["d"], c["ffn"], c["E"], c["k"], c["dtype"]
+    x, layer = inputs.make_workload(T, d, ffn, E, k, dtype, seed=c["seed"], device="cuda")
+    ref = moe.forward(x, layer.Wg, layer.W1, layer.W3, layer.W2, k, bias=layer.bias).cpu()
+    xh = x.cpu().pin_memory()
+    view = torch.int16 if dtype == "bf16" else torch.int32
+    for _ in range(2):
+        oh = torch.empty_like(xh, pin_memory=True)
+        oh.fill_(0)
+        moe.forward_host_io(xh, layer.Wg, layer.W1, layer.W3, layer.W2, k, bias=layer.bias,
+                            out_host=oh)
+        torch.cuda.synchronize()
+        assert torch.equal(oh.view(view), ref.view(view)), f"case {20_000 + i}: {c}"
