@@ -38,10 +38,17 @@ def _call_static(moe, x, layer, k, out):
     return rc
 
 
-@pytest.mark.parametrize("name,T,seed", [("decode", 16, None), ("small", 40, 21)])
+@pytest.mark.parametrize("name,T,seed", [("decode", 16, None), ("small", 40, 21),
+                                         ("one_token", 1, None), ("four_tokens", 4, None)])
 def test_static_scratch_matches_workspace_entry_point(moe, name, T, seed):
+    """Equal to moe_forward (its own workspace) at decode, at a small shape,
+    and at one and four tokens of the Mixtral shape, where the plan also
+    carves the gate/up halves' partial sums and counters out of the array."""
     if name == "decode":
         x, layer = inputs.make_named("decode", device="cuda")
+    elif seed is None:
+        x, layer = inputs.make_named("decode", device="cuda")
+        x = x[:T].contiguous()
     else:
         x, layer = inputs.make_workload(T, 256, 448, 8, 2, "bf16", seed, "cuda")
     k = 2
